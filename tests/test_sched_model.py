@@ -1,0 +1,104 @@
+"""Pins for the scheduler model (host logic, no GPU).
+
+The model states what each scheduler must do; these tests check it against
+hand-worked orders, closed forms of the grouped order at its extremes, and the
+coverage invariant ("Neither mode creates additional independent work at the
+tail of a grid": every tile is done exactly once).
+"""
+import json
+import os
+import random
+
+import pytest
+
+from oracle import sched as sm
+
+# (M, N, BM, BN) for every workload and both tile shapes (128x256 per CTA,
+# 256x256 per CTA pair)
+GRIDS = sorted({
+    (m, n, bm, bn)
+    for (m, n) in [(512, 512), (4096, 4096), (8192, 8192), (5120, 5120), (4224, 3968),
+                   (19200, 256), (1, 1), (129, 257)]
+    for (bm, bn) in [(128, 256), (256, 256)]
+})
+
+
+def test_swizzle_hand_worked(golden_dir):
+    with open(os.path.join(golden_dir, "swizzle_3x2_g2.json")) as f:
+        g = json.load(f)
+    got = [list(sm.swizzle(w, g["Tm"], g["Tn"], g["group_m"])) for w in range(g["Tm"] * g["Tn"])]
+    assert got == g["order"]
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+@pytest.mark.parametrize("group_m", [1, 8])
+def test_swizzle_is_a_bijection(grid, group_m):
+    Tm, Tn = sm.tile_grid(*grid)
+    seen = {sm.swizzle(w, Tm, Tn, group_m) for w in range(Tm * Tn)}
+    assert seen == {(i, j) for i in range(Tm) for j in range(Tn)}
+
+
+def test_swizzle_extremes():
+    Tm, Tn = 5, 7
+    # one row per group: plain row-major order
+    assert [sm.swizzle(w, Tm, Tn, 1) for w in range(Tm * Tn)] == \
+        [(w // Tn, w % Tn) for w in range(Tm * Tn)]
+    # a group taller than the grid: plain column-major order
+    assert [sm.swizzle(w, Tm, Tn, 8) for w in range(Tm * Tn)] == \
+        [(w % Tm, w // Tm) for w in range(Tm * Tn)]
+
+
+def test_tile_counts_of_the_workloads():
+    assert sm.tile_grid(512, 512, 128, 256) == (4, 2)
+    assert sm.tile_grid(4096, 4096, 128, 256) == (32, 16)
+    assert sm.tile_grid(5120, 5120, 128, 256) == (40, 20)
+    assert sm.tile_grid(4224, 3968, 128, 256) == (33, 16)       # 528 tiles
+    assert sm.tile_grid(19200, 256, 128, 256) == (150, 1)
+
+
+@pytest.mark.parametrize("T,G", [(8, 148), (512, 148), (2048, 148), (150, 148), (1, 1), (528, 74)])
+def test_static_covers_exactly_once(T, G):
+    G = sm.static_grid(T, G)
+    ev = sm.static_assignment(T, G)
+    assert sm.coverage(ev, T) == [1] * T
+    per = {}
+    for _, c, _ in ev:
+        per[c] = per.get(c, 0) + 1
+    assert max(per.values()) - min(per.values()) <= 1      # balanced to one tile
+    for w, c, it in ev:
+        assert c == w % G and it == w // G
+
+
+def test_nonpersistent_is_identity():
+    ev = sm.nonpersistent_assignment(37)
+    assert sm.coverage(ev, 37) == [1] * 37
+    assert all(w == c and it == 0 for w, c, it in ev)
+
+
+@pytest.mark.parametrize("T,resident", [(1, 148), (8, 148), (150, 148), (512, 148), (2048, 148),
+                                        (1024, 74), (800, 10)])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_clc_replay_covers_exactly_once(T, resident, seed):
+    ev, req, after_fail = sm.clc_replay(T, resident, seed=seed)
+    assert sm.coverage(ev, T) == [1] * T
+    assert after_fail == 0
+    # a cluster's first tile is its own id
+    firsts = {(c, w) for w, c, it in ev if it == 0}
+    assert all(c == w for c, w in firsts)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_clc_replay_with_injected_failures(seed):
+    rnd = random.Random(seed)
+    T, resident = 600, 40
+    fail_at = {c: rnd.randrange(0, 4) for c in rnd.sample(range(T), 60)}
+    ev, req, after_fail = sm.clc_replay(T, resident, fail_at=fail_at, seed=seed)
+    assert sm.coverage(ev, T) == [1] * T        # un-cancelled clusters run their own tile
+    assert after_fail == 0
+
+
+def test_clc_replay_uneven_costs_cover_exactly_once():
+    # tile costs that differ by 5x change who runs what, never how often
+    T, resident = 200, 20
+    ev, _, _ = sm.clc_replay(T, resident, cost=lambda w: 5.0 if w % 2 == 0 else 1.0)
+    assert sm.coverage(ev, T) == [1] * T
