@@ -1,0 +1,158 @@
+/*
+ * pts_gemm.h -- C ABI of the persistent, tile-scheduled GEMM for GB300 (sm_103a).
+ *
+ * Computes C = A . B with fp32 accumulation on the tensor cores:
+ *   A  M x K, row-major (leading dimension K)
+ *   B  stored N x K, row-major (leading dimension K), i.e. K x N column-major
+ *   C  M x N, row-major (leading dimension N); fp16 for fp16 inputs, bf16 for
+ *      bf16 and e4m3 inputs.  For e4m3, C = (A8 . B8) / (scale_a * scale_b).
+ *
+ * The output is cut into tiles (one tile per CTA, or per CTA pair with
+ * cta_group 2); a scheduler hands the tiles to CTAs:
+ *   - non-persistent: one CTA (pair) per tile, the hardware block scheduler
+ *     assigns them ("question about persistent kernel concept": "allocating
+ *     a thread block for each tile");
+ *   - static: a grid sized to the resident capacity of the SMs, each CTA
+ *     derives its later tiles in software ("Persistent Kernels with Cluster
+ *     Launch Control", first paragraph; "Choosing between static and CLC
+ *     scheduling", first bullet);
+ *   - CLC: a grid of one CTA (pair) per tile; running CTAs cancel clusters
+ *     that have not launched yet and take over their tiles
+ *     (clusterlaunchcontrol.try_cancel; same page, second paragraph).
+ * Tiles are visited in GROUP_SIZE_M-grouped order ("[Persistent] Performance
+ * on 09-persistent-matmul on A100 worse than non-persistent", the
+ * hyperparameter list: GROUP_SIZE_M 8).
+ *
+ * General rules for every call:
+ *   - Device pointers are plain CUDA device addresses of the current process
+ *     on the handle's device; host pointers are ordinary host memory (pinned
+ *     memory makes the copies asynchronous).
+ *   - Errors are reported only through the returned status; nothing aborts
+ *     the process and no call falls back to the CPU.
+ *   - Calls are asynchronous on the given stream unless stated otherwise.
+ *   - A handle is not thread-safe; use one handle per host thread.
+ */
+#ifndef PTS_GEMM_H
+#define PTS_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_E4M3 = 2 } gemm_dtype_t;
+
+typedef enum {
+    GEMM_SCHED_NONPERSISTENT = 0,
+    GEMM_SCHED_STATIC = 1,
+    GEMM_SCHED_CLC = 2
+} gemm_sched_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment, enum or option */
+    GEMM_ERR_UNSUPPORTED = 2,   /* device is not compute capability 10.3 */
+    GEMM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    GEMM_ERR_TIMEOUT = 4,       /* a device-side wait hit its time limit */
+    GEMM_ERR_COVERAGE = 5       /* tile records show a tile not visited exactly once */
+} gemm_status_t;
+
+/* debug_flags */
+#define GEMM_DEBUG_RECORDS 0x1u   /* fill one gemm_tile_record_t per tile */
+#define GEMM_DEBUG_CLC_STOP_AT 0x2u
+/* with GEMM_SCHED_CLC: every CTA (pair) behaves as if its fault_arg-th
+ * try_cancel request (0-based) had failed: it does not issue it and stops
+ * after its current tile.  Clusters that were therefore not cancelled launch
+ * and run their own tile, so coverage stays exact. */
+
+typedef struct gemm_opts {
+    int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair); 0 = 1 */
+    int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
+    int stages;                     /* shared-memory ring depth; 0 = the most that fits */
+    int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */
+    unsigned debug_flags;           /* GEMM_DEBUG_* */
+    int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT */
+    unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
+} gemm_opts_t;
+
+/* Per-tile record written when GEMM_DEBUG_RECORDS is set. */
+typedef struct gemm_tile_record {
+    uint32_t visits;   /* CTAs that stored this tile; exactly cta_group when coverage is exact */
+    uint32_t work;     /* linear work id that mapped to this tile */
+    uint32_t owner;    /* cluster index (blockIdx.x / cta_group) that ran it */
+    uint32_t iter;     /* how many tiles that cluster had run before it */
+    uint32_t smid;     /* SM of the (leader) CTA */
+    uint32_t reserved[3];
+} gemm_tile_record_t;
+
+/* Launch shape chosen for a problem. */
+typedef struct gemm_launch_info {
+    int tile_m, tile_n, tile_k;     /* output tile per cluster, k-block per stage (elements) */
+    int cta_group;
+    int stages;
+    int64_t tiles_m, tiles_n, tiles;
+    int64_t grid_ctas;              /* gridDim.x */
+    int max_active_clusters;        /* resident clusters the device holds for this kernel */
+    int smem_bytes;                 /* dynamic shared memory per CTA */
+    int threads;                    /* threads per CTA */
+} gemm_launch_info_t;
+
+typedef struct gemm_ctx *gemm_handle_t;
+
+/* Create a handle on `device` (made current for the call).  opts may be NULL
+ * (all defaults).  Allocates a small device status block; the handle owns it.
+ * Returns GEMM_ERR_UNSUPPORTED on anything but compute capability 10.3,
+ * GEMM_ERR_CUDA if the device cannot be used, GEMM_ERR_INVALID_ARG for bad
+ * options. */
+gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opts);
+
+/* C = A . B on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * A, B, C: device pointers, 16-byte aligned, caller-owned, not overlapping C.
+ * Sizes: M, N, K >= 0; K*elem_bytes and N*2 must be multiples of 16 bytes
+ * (K % 8 == 0 for fp16/bf16, K % 16 == 0 for e4m3, N % 8 == 0); each of
+ * M, N, K < 2^31.  M == 0 or N == 0 launches nothing; K == 0 writes zeros.
+ * scale_a, scale_b: e4m3 per-tensor scales (> 0, finite); ignored otherwise.
+ * Returns after the launch; device-side errors (wait time-outs) are read with
+ * gemm_check or gemm_read_debug. */
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                       const void *A, const void *B, void *C,
+                       gemm_dtype_t dtype, gemm_sched_t sched,
+                       float scale_a, float scale_b, void *stream);
+
+/* gemm_run on HOST buffers: copies A and B to device memory the handle owns
+ * (grown as needed), runs, copies C back to C_host, all on `stream`, then
+ * synchronises the stream and returns the device status like gemm_check.
+ * Same size rules as gemm_run; host pointers need no alignment. */
+gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                            const void *A_host, const void *B_host, void *C_host,
+                            gemm_dtype_t dtype, gemm_sched_t sched,
+                            float scale_a, float scale_b, void *stream);
+
+/* Launch shape gemm_run would use (no GPU work).  Same argument rules. */
+gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                         gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info);
+
+/* Synchronise `stream`, read and clear the device status block.
+ * device_status (may be NULL) receives the raw first error word (0 = none).
+ * Returns GEMM_ERR_TIMEOUT if a device wait timed out since the last check. */
+gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status);
+
+/* After a run with GEMM_DEBUG_RECORDS: synchronise `stream`, copy n_tiles
+ * records (tile-row-major order: index tm * tiles_n + tn) to host memory
+ * `records`, and do what gemm_check does.  Returns GEMM_ERR_COVERAGE if any
+ * visits count differs from the cta_group of the last run. */
+gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records,
+                              int64_t n_tiles, int *device_status);
+
+/* Free the handle and everything it owns.  NULL is accepted. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* Static string for a status code (never NULL). */
+const char *gemm_status_string(gemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTS_GEMM_H */

@@ -1,0 +1,409 @@
+// C ABI of the persistent tile-scheduled GEMM: argument checks, launch shape,
+// TMA tensor maps and the device status block.  Declared in pts_gemm.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/pts_gemm.h"
+#include "gemm_launch.h"
+#include "gemm_params.h"
+
+namespace {
+
+constexpr int kMapCache = 16;
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per wait
+
+struct MapEntry {
+    const void *ptr = nullptr;
+    uint64_t rows = 0, cols = 0;
+    int dtype = -1;
+    uint32_t box_rows = 0, box_cols = 0;
+    CUtensorMap map;
+};
+
+int elem_bytes(gemm_dtype_t d) { return d == GEMM_E4M3 ? 1 : 2; }
+
+}  // namespace
+
+struct gemm_ctx {
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    gemm_opts_t opts{};
+    int32_t *d_status = nullptr;              // 4 ints
+    pts::TileRecord *d_records = nullptr;
+    int64_t records_cap = 0;
+    int64_t last_tiles = 0;
+    int last_cta_group = 1;
+    void *d_host_bufs = nullptr;              // gemm_run_host staging (A | B | C)
+    size_t host_bufs_cap = 0;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    bool smem_set[3][2] = {};
+    int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
+    int occ_clusters[3][2] = {};
+    MapEntry maps[kMapCache];
+    int map_next = 0;
+};
+
+namespace {
+
+gemm_status_t cuda_fail(cudaError_t e)
+{
+    (void)cudaGetLastError();   // clear a non-sticky error so the next call starts clean
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Encode (or find) a 2-D row-major tensor map over rows x cols elements.
+const CUtensorMap *get_map(gemm_ctx *h, const void *ptr, uint64_t rows, uint64_t cols, int dtype,
+                           uint32_t box_rows, uint32_t box_cols)
+{
+    for (auto &m : h->maps)
+        if (m.ptr == ptr && m.rows == rows && m.cols == cols && m.dtype == dtype && m.box_rows == box_rows
+            && m.box_cols == box_cols)
+            return &m.map;
+    MapEntry &m = h->maps[h->map_next];
+    h->map_next = (h->map_next + 1) % kMapCache;
+    m.ptr = nullptr;
+    CUtensorMapDataType t = dtype == GEMM_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                            : dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int es = dtype == GEMM_E4M3 ? 1 : 2;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * static_cast<cuuint64_t>(es)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(&m.map, t, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nullptr;
+    m.ptr = ptr;
+    m.rows = rows;
+    m.cols = cols;
+    m.dtype = dtype;
+    m.box_rows = box_rows;
+    m.box_cols = box_cols;
+    return &m.map;
+}
+
+pts::KernelOps ops_for(int kind, int cg) { return cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind); }
+
+struct Plan {
+    int cg, stages, smem;
+    int64_t tiles_m, tiles_n, tiles;
+    int64_t grid_ctas;
+    int max_active_clusters;
+};
+
+gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_sched_t sched)
+{
+    if (dtype < GEMM_F16 || dtype > GEMM_E4M3) return GEMM_ERR_INVALID_ARG;
+    if (sched < GEMM_SCHED_NONPERSISTENT || sched > GEMM_SCHED_CLC) return GEMM_ERR_INVALID_ARG;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return GEMM_ERR_INVALID_ARG;
+    if ((K * elem_bytes(dtype)) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+    if ((N * 2) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, gemm_dtype_t dtype, gemm_sched_t sched, Plan &pl)
+{
+    pl.cg = h->opts.cta_group;
+    int stages = h->opts.stages;
+    if (stages == 0) {   // the deepest ring that fits
+        stages = pts::kMaxStages;
+        while (stages > 2 && pts::smem_bytes(pl.cg, stages) > h->max_smem_optin) --stages;
+    }
+    pl.stages = stages;
+    pl.smem = pts::smem_bytes(pl.cg, stages);
+    if (pl.smem > h->max_smem_optin) return GEMM_ERR_INVALID_ARG;
+    const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
+    pl.tiles_m = (M + tile_m - 1) / tile_m;
+    pl.tiles_n = (N + pts::kTileN - 1) / pts::kTileN;
+    pl.tiles = pl.tiles_m * pl.tiles_n;
+    if (pl.tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
+
+    const int kind = static_cast<int>(dtype);
+    const int ci = pl.cg - 1;
+    pts::KernelOps ops = ops_for(kind, pl.cg);
+    if (!h->smem_set[kind][ci]) {
+        if (ops.set_smem(h->max_smem_optin) != cudaSuccess) return cuda_fail(cudaErrorInvalidValue);
+        h->smem_set[kind][ci] = true;
+    }
+    if (h->occ_smem[kind][ci] != pl.smem) {
+        int n = 0;
+        if (ops.max_active_clusters(pl.smem, &n) != cudaSuccess) return cuda_fail(cudaErrorInvalidValue);
+        h->occ_smem[kind][ci] = pl.smem;
+        h->occ_clusters[kind][ci] = n;
+    }
+    pl.max_active_clusters = h->occ_clusters[kind][ci];
+    if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
+    int64_t clusters = pl.tiles;
+    if (sched == GEMM_SCHED_STATIC) {
+        int64_t cap = pl.max_active_clusters;
+        if (h->opts.max_clusters > 0 && h->opts.max_clusters < cap) cap = h->opts.max_clusters;
+        clusters = pl.tiles < cap ? pl.tiles : cap;
+    }
+    pl.grid_ctas = clusters * pl.cg;
+    return GEMM_OK;
+}
+
+gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                     gemm_dtype_t dtype, gemm_sched_t sched, float scale_a, float scale_b,
+                     cudaStream_t stream)
+{
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr || reinterpret_cast<uintptr_t>(C) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+    if (K == 0) return cuda_fail(pts::launch_zero_fill(C, M * N * 2, stream));
+    if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0)
+        return GEMM_ERR_INVALID_ARG;
+    float out_scale = 1.0f;
+    if (dtype == GEMM_E4M3) {
+        if (!(scale_a > 0.0f) || !(scale_b > 0.0f) || !std::isfinite(scale_a) || !std::isfinite(scale_b))
+            return GEMM_ERR_INVALID_ARG;
+        out_scale = 1.0f / (scale_a * scale_b);
+        if (!std::isfinite(out_scale)) return GEMM_ERR_INVALID_ARG;
+    }
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+
+    Plan pl;
+    gemm_status_t st = make_plan(h, M, N, dtype, sched, pl);
+    if (st != GEMM_OK) return st;
+
+    const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
+    const CUtensorMap *ma = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems);
+    const CUtensorMap *mb = get_map(h, B, uint64_t(N), uint64_t(K), dtype, pts::kTileN / pl.cg, kelems);
+    const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
+    const CUtensorMap *mc = get_map(h, C, uint64_t(M), uint64_t(N), cdt, pts::kEpiRowsPerWarp,
+                                    pts::kEpiChunkCols);
+    if (!ma || !mb || !mc) return GEMM_ERR_CUDA;
+
+    pts::GemmParams p{};
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_kb = static_cast<int32_t>((K + kelems - 1) / kelems);
+    p.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    p.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.group_m = h->opts.group_size_m;
+    p.sched = static_cast<int32_t>(sched);
+    p.stages = pl.stages;
+    p.out_scale = out_scale;
+    p.debug_flags = h->opts.debug_flags;
+    p.fault_arg = h->opts.fault_arg;
+    p.timeout_ns = h->opts.timeout_ns;
+    p.status = h->d_status;
+    p.records = nullptr;
+    if (h->opts.debug_flags & GEMM_DEBUG_RECORDS) {
+        if (h->records_cap < pl.tiles) {
+            cudaFree(h->d_records);
+            h->d_records = nullptr;
+            h->records_cap = 0;
+            if (cudaMalloc(&h->d_records, size_t(pl.tiles) * sizeof(pts::TileRecord)) != cudaSuccess)
+                return cuda_fail(cudaErrorMemoryAllocation);
+            h->records_cap = pl.tiles;
+        }
+        if (cudaMemsetAsync(h->d_records, 0, size_t(pl.tiles) * sizeof(pts::TileRecord), stream) != cudaSuccess)
+            return cuda_fail(cudaErrorInvalidValue);
+        p.records = h->d_records;
+    }
+    h->last_tiles = pl.tiles;
+    h->last_cta_group = pl.cg;
+
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(*ma, *mb, *mc, p, static_cast<int>(pl.grid_ctas),
+                                                                   pl.smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return cuda_fail(cudaGetLastError());
+}
+
+gemm_status_t read_status(gemm_ctx *h, cudaStream_t stream, int *device_status)
+{
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    int32_t s[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(s, h->d_status, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    if (s[0] != 0 && cudaMemset(h->d_status, 0, sizeof(s)) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    if (device_status) *device_status = s[0] == 0 ? 0 : (s[0] << 24) | ((s[1] & 0xff) << 16) | (s[2] & 0xffff);
+    return s[0] == pts::DEV_ERR_TIMEOUT ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gemm_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported device (needs compute capability 10.3)";
+    case GEMM_ERR_CUDA: return "CUDA error";
+    case GEMM_ERR_TIMEOUT: return "device wait timed out";
+    case GEMM_ERR_COVERAGE: return "a tile was not computed exactly once";
+    default: return "unknown status";
+    }
+}
+
+gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opts)
+{
+    if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_opts_t o{};
+    if (opts) o = *opts;
+    if (o.cta_group == 0) o.cta_group = 1;
+    if (o.group_size_m == 0) o.group_size_m = 8;
+    if (o.timeout_ns == 0) o.timeout_ns = kDefaultTimeoutNs;
+    if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT)) return GEMM_ERR_INVALID_ARG;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return cuda_fail(cudaErrorNoDevice);
+    if (cudaSetDevice(device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+
+    gemm_ctx *h = new (std::nothrow) gemm_ctx();
+    if (!h) return GEMM_ERR_CUDA;
+    h->device = device;
+    h->sm_count = sms;
+    h->max_smem_optin = smem;
+    h->opts = o;
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess
+        || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        delete h;
+        return cuda_fail(cudaErrorUnknown);
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (cudaMalloc(&h->d_status, 4 * sizeof(int32_t)) != cudaSuccess
+        || cudaMemset(h->d_status, 0, 4 * sizeof(int32_t)) != cudaSuccess) {
+        cudaFree(h->d_status);
+        delete h;
+        return cuda_fail(cudaErrorMemoryAllocation);
+    }
+    *out = h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                       gemm_dtype_t dtype, gemm_sched_t sched, float scale_a, float scale_b, void *stream)
+{
+    if (h == nullptr) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_sizes(M, N, K, dtype, sched);
+    if (st != GEMM_OK) return st;
+    return launch(h, M, N, K, A, B, C, dtype, sched, scale_a, scale_b, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A_host,
+                            const void *B_host, void *C_host, gemm_dtype_t dtype, gemm_sched_t sched,
+                            float scale_a, float scale_b, void *stream)
+{
+    if (h == nullptr) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_sizes(M, N, K, dtype, sched);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C_host == nullptr || (K > 0 && (A_host == nullptr || B_host == nullptr))) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    auto round_up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t a_bytes = size_t(M) * size_t(K) * elem_bytes(dtype);
+    const size_t b_bytes = size_t(N) * size_t(K) * elem_bytes(dtype);
+    const size_t c_bytes = size_t(M) * size_t(N) * 2;
+    const size_t need = round_up(a_bytes) + round_up(b_bytes) + round_up(c_bytes);
+    if (h->host_bufs_cap < need) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+        cudaFree(h->d_host_bufs);
+        h->d_host_bufs = nullptr;
+        h->host_bufs_cap = 0;
+        if (cudaMalloc(&h->d_host_bufs, need) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
+        h->host_bufs_cap = need;
+    }
+    char *dA = static_cast<char *>(h->d_host_bufs);
+    char *dB = dA + round_up(a_bytes);
+    char *dC = dB + round_up(b_bytes);
+    if (a_bytes && cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    if (b_bytes && cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    st = launch(h, M, N, K, dA, dB, dC, dtype, sched, scale_a, scale_b, s);
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    return read_status(h, s, nullptr);
+}
+
+gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                         gemm_sched_t sched, gemm_launch_info_t *info)
+{
+    if (h == nullptr || info == nullptr) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_sizes(M, N, K, dtype, sched);
+    if (st != GEMM_OK) return st;
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    Plan pl;
+    st = make_plan(h, M, N, dtype, sched, pl);
+    if (st != GEMM_OK) return st;
+    std::memset(info, 0, sizeof(*info));
+    info->tile_m = pts::kRowsPerCta * pl.cg;
+    info->tile_n = pts::kTileN;
+    info->tile_k = dtype == GEMM_E4M3 ? 128 : 64;
+    info->cta_group = pl.cg;
+    info->stages = pl.stages;
+    info->tiles_m = pl.tiles_m;
+    info->tiles_n = pl.tiles_n;
+    info->tiles = pl.tiles;
+    info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;
+    info->max_active_clusters = pl.max_active_clusters;
+    info->smem_bytes = pl.smem;
+    info->threads = pts::kThreads;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status)
+{
+    if (h == nullptr) return GEMM_ERR_INVALID_ARG;
+    return read_status(h, static_cast<cudaStream_t>(stream), device_status);
+}
+
+gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records, int64_t n_tiles,
+                              int *device_status)
+{
+    if (h == nullptr || n_tiles < 0 || (n_tiles > 0 && records == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (!(h->opts.debug_flags & GEMM_DEBUG_RECORDS) || n_tiles > h->records_cap || n_tiles != h->last_tiles)
+        return GEMM_ERR_INVALID_ARG;
+    static_assert(sizeof(gemm_tile_record_t) == sizeof(pts::TileRecord), "record layout");
+    gemm_status_t st = read_status(h, static_cast<cudaStream_t>(stream), device_status);
+    if (n_tiles > 0 && cudaMemcpy(records, h->d_records, size_t(n_tiles) * sizeof(gemm_tile_record_t),
+                                  cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    if (st != GEMM_OK) return st;
+    for (int64_t t = 0; t < n_tiles; ++t)
+        if (records[t].visits != static_cast<uint32_t>(h->last_cta_group)) return GEMM_ERR_COVERAGE;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h)
+{
+    if (h == nullptr) return GEMM_OK;
+    cudaSetDevice(h->device);
+    cudaFree(h->d_status);
+    cudaFree(h->d_records);
+    cudaFree(h->d_host_bufs);
+    delete h;
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Host-side wrappers around one gemm_kernel instantiation.
+#pragma once
+#include "gemm_kernel.cuh"
+#include "gemm_launch.h"
+
+namespace pts {
+
+template <int KIND, int CG>
+struct Inst {
+    static cudaError_t set_smem(int smem)
+    {
+        return cudaFuncSetAttribute(gemm_kernel<KIND, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    }
+
+    static void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid_ctas, int smem,
+                            cudaStream_t stream)
+    {
+        cfg = cudaLaunchConfig_t{};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = stream;
+        cfg.numAttrs = 0;
+        cfg.attrs = attr;
+        if (CG == 2) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.numAttrs = 1;
+        }
+    }
+
+    static cudaError_t max_active_clusters(int smem, int *out)
+    {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        fill_config(cfg, attr, 2 * CG, smem, nullptr);
+        if (CG == 1) {
+            int per_sm = 0, dev = 0, sms = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<KIND, CG>,
+                                                                          kThreads, static_cast<size_t>(smem));
+            if (e != cudaSuccess) return e;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            *out = per_sm * sms;
+            return cudaSuccess;
+        }
+        return cudaOccupancyMaxActiveClusters(out, gemm_kernel<KIND, CG>, &cfg);
+    }
+
+    static cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                              const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream)
+    {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        fill_config(cfg, attr, grid_ctas, smem, stream);
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, a, b, c, p);
+    }
+
+    static KernelOps ops() { return KernelOps{&set_smem, &max_active_clusters, &launch}; }
+};
+
+}  // namespace pts

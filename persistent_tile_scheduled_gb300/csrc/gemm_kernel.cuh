@@ -1,0 +1,522 @@
+// Persistent, tile-scheduled GEMM kernel for sm_103a.
+//
+//   C[M x N] = A[M x K] . B[N x K]^T      (fp32 accumulation in TMEM)
+//
+// One CTA (CG = 1) or one CTA pair (CG = 2, tcgen05 cta_group::2) computes a
+// (128*CG) x 256 output tile at a time.  Warp roles:
+//   warp 0     producer: TMA loads of A and B k-blocks into an S-stage
+//              shared-memory ring guarded by full/empty mbarriers; on the
+//              leader CTA it is also the tile scheduler (static arithmetic or
+//              Cluster Launch Control) and publishes every tile id into a
+//              small broadcast ring read by all other roles
+//   warp 1     MMA issuer (one thread of the leader CTA): tcgen05.mma into one
+//              of two 256-column TMEM accumulators, so the epilogue of tile i
+//              overlaps the mainloop of tile i+1
+//   warps 2-5  epilogue: tcgen05.ld -> (scale) -> fp16/bf16 -> swizzled
+//              shared-memory staging -> TMA store
+//
+// Scheduling follows "Persistent Kernels with Cluster Launch Control": a
+// static scheduler derives later tiles in software (w, w+G, w+2G, ...); a CLC
+// scheduler asks the hardware to cancel a not-yet-launched cluster of the same
+// grid and takes that cluster's id as its next tile, never asking again after
+// one failed request.  The non-persistent mode runs exactly one tile per
+// cluster ("question about persistent kernel concept": a thread block per tile).
+//
+// Every mbarrier wait is bounded: on time-out the kernel records an error in
+// the device status block, tells every role (and the peer CTA) to stop, drains
+// its own copies in flight, frees TMEM and returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace pts {
+
+enum : int32_t {
+    WHERE_EMPTY = 1,        // producer waiting for a free stage
+    WHERE_FULL = 2,         // MMA waiting for a loaded stage
+    WHERE_ACC_EMPTY = 3,    // MMA waiting for a drained accumulator
+    WHERE_ACC_FULL = 4,     // epilogue waiting for a finished accumulator
+    WHERE_RING_EMPTY = 5,   // scheduler waiting for a free broadcast slot
+    WHERE_RING_FULL = 6,    // a role waiting for the next tile id
+    WHERE_CLC = 7,          // scheduler waiting for a CLC response
+    WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
+};
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor for a K-major operand laid out by
+// TMA with the 128-byte swizzle: rows of 128 bytes, groups of 8 rows 1024
+// bytes apart (stride byte offset), leading byte offset unused (set to 16 B),
+// descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46)
+           | (2ull << 61);
+}
+
+// tcgen05 instruction descriptor: fp32 D (bits 4-5 = 1), A/B formats at bits
+// 7-9 / 10-12 (kind::f16: fp16 0, bf16 1; kind::f8f6f4: e4m3 0), both
+// operands K-major (bits 15/16 = 0), N >> 3 at bits 17-22, M >> 4 at 24-28.
+template <int KIND, int CG>
+__host__ __device__ constexpr uint32_t make_idesc()
+{
+    constexpr uint32_t fmt = (KIND == 1) ? 1u : 0u;
+    constexpr uint32_t m = 128u * CG, n = static_cast<uint32_t>(kTileN);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Work id -> (tile-row, tile-col) in GROUP_SIZE_M-grouped order: ids walk down
+// a group of at most group_m tile-rows one column at a time.
+__device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int group_m, int &tm, int &tn)
+{
+    const int per_group = group_m * tiles_n;
+    const int g = w / per_group;
+    const int first = g * group_m;
+    const int rows = min(tiles_m - first, group_m);
+    const int r = w - g * per_group;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+struct WaitCtl {
+    uint32_t abort_addr;       // this CTA's abort flag (shared::cta)
+    uint32_t peer_abort;       // the peer's abort flag (shared::cluster), 0 if none
+    uint64_t timeout_ns;
+    int32_t *status;
+
+    __device__ void fail(int32_t where) const
+    {
+        if (atomicCAS(status, 0, DEV_ERR_TIMEOUT) == 0) {
+            status[1] = where;
+            status[2] = static_cast<int32_t>(blockIdx.x);
+        }
+        atomicAdd(status + 3, 1);
+        st_shared_u32(abort_addr, 1u);
+        if (peer_abort) st_cluster_u32(peer_abort, 1u);
+    }
+
+    // Wait for phase `parity` of `bar`.  False when this CTA was told to stop
+    // or the wait ran past the time limit (which is then recorded).
+    __device__ bool wait(uint32_t bar, uint32_t parity, int32_t where) const
+    {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t n = 1;; ++n) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((n & 15u) == 0) {
+                if (ld_shared_u32(abort_addr)) return false;
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    fail(where);
+                    return false;
+                }
+            }
+        }
+    }
+
+    // Bounded wait used only while shutting down after an error: ignores the
+    // abort flag, gives up silently after `limit_ns`.
+    __device__ bool drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
+    {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity))
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        return true;
+    }
+};
+
+template <int KIND>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits, float scale)
+{
+    float lo = __uint_as_float(lo_bits), hi = __uint_as_float(hi_bits);
+    if constexpr (KIND == 2) {
+        lo *= scale;
+        hi *= scale;
+    }
+    if constexpr (KIND == 0) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <int KIND, int CG>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p)
+{
+    constexpr int SA = stage_bytes_a();
+    constexpr int SB = stage_bytes_b(CG);
+    constexpr int KELEMS = (KIND == 2) ? kKBlockBytes : kKBlockBytes / 2;   // K elements per k-block
+    constexpr uint32_t TX_BYTES = static_cast<uint32_t>(CG * (SA + SB));   // per stage, whole pair
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int S = p.stages;
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * SA;
+    const uint32_t sEpi = sB + S * SB;
+    const uint32_t bar0 = sEpi + epi_bytes();
+    const uint32_t full0 = bar0;                             // + 8*s
+    const uint32_t empty0 = bar0 + 8 * kMaxStages;           // + 8*s
+    const uint32_t acc_full0 = bar0 + 16 * kMaxStages;       // + 8*b
+    const uint32_t acc_empty0 = acc_full0 + 16;              // + 8*b
+    const uint32_t ring_full0 = acc_empty0 + 16;             // + 8*r
+    const uint32_t ring_empty0 = ring_full0 + 8 * kRing;     // + 8*r
+    const uint32_t clc_bar = ring_empty0 + 8 * kRing;
+    const uint32_t clc_resp = (clc_bar + 8 + 15) & ~15u;
+    const uint32_t ring_w0 = clc_resp + 16;                  // + 4*r
+    const uint32_t tmem_slot = ring_w0 + 4 * kRing;
+    const uint32_t abort_flag = tmem_slot + 4;
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+    WaitCtl ctl;
+    ctl.abort_addr = abort_flag;
+    ctl.peer_abort = (CG == 2) ? mapa(abort_flag, rank ^ 1u) : 0u;
+    ctl.timeout_ns = p.timeout_ns;
+    ctl.status = p.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full0 + 8 * b, 1);
+            mbar_init(acc_empty0 + 8 * b, kEpiWarps * CG);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(ring_full0 + 8 * r, 1);
+            mbar_init(ring_empty0 + 8 * r, CG == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps);
+        }
+        mbar_init(clc_bar, 1);
+        st_shared_u32(abort_flag, 0u);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(tmem_slot, kTmemCols);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+
+    // ---- tile-id broadcast ring -------------------------------------------
+    // Slot r holds the id of tile i (i % kRing == r), or -1 = no more tiles.
+    auto publish = [&](int i, int w) -> bool {
+        const int slot = i % kRing;
+        if (i >= kRing && !ctl.wait(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
+            return false;
+        st_shared_u32(ring_w0 + 4 * slot, static_cast<uint32_t>(w));
+        if constexpr (CG == 2) {
+            st_cluster_u32(mapa(ring_w0 + 4 * slot, 1u), static_cast<uint32_t>(w));
+            mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
+        }
+        mbar_arrive(ring_full0 + 8 * slot);
+        return true;
+    };
+    auto ring_read = [&](int i, int &w) -> bool {
+        const int slot = i % kRing;
+        if (!ctl.wait(ring_full0 + 8 * slot, (i / kRing) & 1, WHERE_RING_FULL)) return false;
+        w = static_cast<int>(ld_shared_u32(ring_w0 + 4 * slot));
+        if (CG == 2 && !leader)
+            mbar_arrive_cluster(mapa(ring_empty0 + 8 * slot, 0u));
+        else
+            mbar_arrive(ring_empty0 + 8 * slot);
+        return true;
+    };
+
+    if (warp == 0) {
+        // =========================== producer / scheduler ======================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            auto load_tile = [&](int tm, int tn) -> bool {
+                const int ya = tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
+                const int yb = tn * kTileN + static_cast<int>(rank) * (kTileN / CG);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ctl.wait(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
+                    const int x = kb * KELEMS;
+                    const uint32_t fb = full0 + 8 * stage;
+                    if constexpr (CG == 1) {
+                        mbar_arrive_expect_tx(fb, TX_BYTES);
+                        tma_load_2d(sA + stage * SA, &tmA, fb, x, ya);
+                        tma_load_2d(sB + stage * SB, &tmB, fb, x, yb);
+                    } else {
+                        if (leader) mbar_arrive_expect_tx(fb, TX_BYTES);
+                        const uint32_t fbc = mapa(fb, 0u);
+                        tma_load_2d_pair(sA + stage * SA, &tmA, fbc, x, ya);
+                        tma_load_2d_pair(sB + stage * SB, &tmB, fbc, x, yb);
+                    }
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                return true;
+            };
+
+            bool clc_pending = false;
+            if (leader) {
+                int w = cluster_id < p.num_tiles ? cluster_id : -1;
+                bool may_request = p.sched == SCHED_CLC;
+                uint32_t clc_phase = 0;
+                ok = publish(0, w);
+                for (int i = 0; ok && w >= 0; ++i) {
+                    if (may_request) {
+                        if ((p.debug_flags & DBG_CLC_STOP_AT) && i == p.fault_arg) {
+                            may_request = false;   // behave as if this request had failed
+                        } else {
+                            fence_proxy_async_smem();   // earlier reads of the slot before the async write
+                            mbar_arrive_expect_tx(clc_bar, 16);
+                            clc_try_cancel(clc_resp, clc_bar);
+                            clc_pending = true;
+                        }
+                    }
+                    int tm, tn;
+                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                    if (!load_tile(tm, tn)) {
+                        ok = false;
+                        break;
+                    }
+                    int next = -1;
+                    if (p.sched == SCHED_STATIC) {
+                        next = (w + num_clusters < p.num_tiles) ? w + num_clusters : -1;
+                    } else if (clc_pending) {
+                        if (!ctl.wait(clc_bar, clc_phase, WHERE_CLC)) {
+                            ok = false;
+                            break;
+                        }
+                        clc_phase ^= 1u;
+                        clc_pending = false;
+                        uint32_t x;
+                        if (clc_decode(clc_resp, x)) {
+                            next = static_cast<int>(x / CG);
+                            if (next >= p.num_tiles) {   // cannot happen for a well-formed grid
+                                ctl.fail(WHERE_BAD_TILE);
+                                next = -1;
+                            }
+                        } else {
+                            may_request = false;   // a failed request is never repeated
+                        }
+                    }
+                    ok = publish(i + 1, next);
+                    w = next;
+                }
+                if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
+            } else {
+                for (int i = 0;; ++i) {
+                    int w;
+                    if (!ring_read(i, w)) {
+                        ok = false;
+                        break;
+                    }
+                    if (w < 0) break;
+                    int tm, tn;
+                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                    if (!load_tile(tm, tn)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) {
+                // Stopped early: let the loads already issued land before the
+                // CTA can exit (bounded; the pair's loads signal the leader).
+                if (CG == 1 || leader) {
+                    const long long n = issued < S ? issued : S;
+                    for (long long j = 0; j < n; ++j) {
+                        const long long g = issued - 1 - j;
+                        ctl.drain(full0 + 8 * static_cast<int>(g % S), static_cast<uint32_t>((g / S) & 1),
+                                  10000000ull);
+                    }
+                } else {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 1000000ull) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================ MMA ==================================
+        if (lane == 0 && leader) {
+            constexpr uint32_t IDESC = make_idesc<KIND, CG>();
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int last_stage = -1;
+            uint32_t last_phase = 0;
+            for (int i = 0;; ++i) {
+                int w;
+                if (!ring_read(i, w) || w < 0) break;
+                if (!ctl.wait(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ctl.wait(full0 + 8 * stage, phase, WHERE_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sA + stage * SA);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * SB);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+                    umma_commit<CG>(empty0 + 8 * stage, 0x3);
+                    last_stage = stage;
+                    last_phase = phase;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit<CG>(acc_full0 + 8 * acc, 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // the last stage release is the last asynchronous arrival this
+            // thread caused; see it land before the CTA may exit
+            if (last_stage >= 0) ctl.drain(empty0 + 8 * last_stage, last_phase, 10000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ============================== epilogue ===============================
+        const uint32_t e = warp - 2;          // staging buffer owner index
+        const uint32_t q = warp & 3u;         // TMEM lane quarter this warp may access
+        const uint32_t stage_base = sEpi + e * (kEpiBufsPerWarp * kEpiBufBytes);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t nstore = 0;
+        for (int i = 0;; ++i) {
+            int w = 0;
+            int ok = 1;
+            if (lane == 0) ok = ring_read(i, w) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!ok || w < 0) break;
+            int tm, tn;
+            tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            if (lane == 0) ok = ctl.wait(acc_full0 + 8 * acc, acc_phase, WHERE_ACC_FULL) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (p.records != nullptr && e == 0 && lane == 0) {
+                TileRecord *r = p.records + (static_cast<long long>(tm) * p.tiles_n + tn);
+                atomicAdd(&r->visits, 1u);
+                if (leader) {
+                    r->work = static_cast<uint32_t>(w);
+                    r->owner = static_cast<uint32_t>(cluster_id);
+                    r->iter = static_cast<uint32_t>(i);
+                    r->smid = smid();
+                }
+            }
+            const int row0 = tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta
+                             + static_cast<int>(q) * kEpiRowsPerWarp;
+            const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * kTileN);
+#pragma unroll 1
+            for (int c = 0; c < kTileN / kEpiChunkCols; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
+                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols + 32, v1);
+                tmem_wait_ld();
+                if (c == kTileN / kEpiChunkCols - 1) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CG == 2 && !leader)
+                            mbar_arrive_cluster(mapa(acc_empty0 + 8 * acc, 0u));
+                        else
+                            mbar_arrive(acc_empty0 + 8 * acc);
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    pk[j] = pack2<KIND>(v0[2 * j], v0[2 * j + 1], p.out_scale);
+                    pk[16 + j] = pack2<KIND>(v1[2 * j], v1[2 * j + 1], p.out_scale);
+                }
+                const uint32_t buf = stage_base + (nstore & 1u) * kEpiBufBytes;
+                if (lane == 0) bulk_wait_read<1>();   // the store that used this buffer has read it
+                __syncwarp();
+                // row `lane`, 16-byte chunk j stored at chunk j ^ (row % 8): the
+                // layout the 128-byte-swizzled tensor map expects
+                const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col = tn * kTileN + c * kEpiChunkCols;
+                if (lane == 0) {
+                    if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
+                    bulk_commit();
+                }
+                ++nstore;
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---- teardown ------------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace pts

@@ -1,0 +1,25 @@
+// Launch entry points of the kernel instantiations (one translation unit per
+// cta_group, compiled in parallel).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_params.h"
+
+namespace pts {
+
+struct KernelOps {
+    // Raise the kernel's dynamic shared-memory limit to `smem` bytes.
+    cudaError_t (*set_smem)(int smem);
+    // Resident clusters the device can hold at once for this kernel.
+    cudaError_t (*max_active_clusters)(int smem, int *out);
+    cudaError_t (*launch)(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                          const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream);
+};
+
+// kind: 0 fp16, 1 bf16, 2 e4m3
+KernelOps kernel_ops_cg1(int kind);
+KernelOps kernel_ops_cg2(int kind);
+cudaError_t launch_zero_fill(void *c, long long bytes, cudaStream_t stream);
+
+}  // namespace pts

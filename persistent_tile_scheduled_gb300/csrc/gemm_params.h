@@ -1,0 +1,64 @@
+// Kernel parameters and compile-time tile geometry shared by the launcher
+// and the kernels (host and device).
+#pragma once
+#include <cstdint>
+
+namespace pts {
+
+// One CTA owns 128 rows of the output tile and its TMEM accumulator holds
+// 128 lanes x 256 fp32 columns.  A k-block is 128 bytes of K per row (64
+// fp16/bf16 or 128 e4m3 elements): one 128-byte swizzle atom row.
+constexpr int kRowsPerCta = 128;
+constexpr int kTileN = 256;
+constexpr int kKBlockBytes = 128;
+constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kEpiChunkCols = 64;       // columns per epilogue TMA store (128 bytes of fp16/bf16)
+constexpr int kEpiRowsPerWarp = 32;
+constexpr int kEpiBufBytes = kEpiRowsPerWarp * kEpiChunkCols * 2;   // 4 KB
+constexpr int kEpiBufsPerWarp = 2;
+constexpr int kRing = 4;                // depth of the tile-id broadcast ring
+constexpr int kTmemCols = 512;          // two 256-column accumulators
+constexpr int kMaxStages = 8;
+
+enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
+
+// Device status block: [0] first error code, [1] where, [2] block, [3] error count.
+enum : int32_t { DEV_ERR_TIMEOUT = 1 };
+enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u };
+
+struct TileRecord {
+    uint32_t visits, work, owner, iter, smid, reserved[3];
+};
+
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t num_kb;             // k-blocks per tile
+    int32_t tiles_m, tiles_n;   // output tiles (per cluster) along M and N
+    int32_t num_tiles;
+    int32_t group_m;            // GROUP_SIZE_M
+    int32_t sched;
+    int32_t stages;
+    float out_scale;            // 1, or 1/(scale_a*scale_b) for e4m3
+    uint32_t debug_flags;
+    int32_t fault_arg;
+    uint64_t timeout_ns;
+    int32_t *status;            // 4 ints
+    TileRecord *records;        // num_tiles entries, or null
+};
+
+__host__ __device__ constexpr int stage_bytes_a() { return kRowsPerCta * kKBlockBytes; }
+__host__ __device__ constexpr int stage_bytes_b(int cg) { return (kTileN / cg) * kKBlockBytes; }
+__host__ __device__ constexpr int epi_bytes() { return kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes; }
+
+// Dynamic shared memory needed for `stages` stages (plus 1 KB for aligning
+// the base to the 1024-byte swizzle period).
+__host__ __device__ constexpr int smem_bytes(int cg, int stages)
+{
+    return 1024 + stages * (stage_bytes_a() + stage_bytes_b(cg)) + epi_bytes()
+           + 8 * (2 * kMaxStages + 4 + 2 * kRing + 1)    // mbarriers
+           + 16                                          // CLC response
+           + 4 * kRing + 16;                             // ring payload, TMEM base, abort flag
+}
+
+}  // namespace pts

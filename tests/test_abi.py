@@ -1,0 +1,106 @@
+"""The C ABI on a machine without a GPU: the library builds, loads, exports
+every function include/pts_gemm.h declares, its structs match the Python
+binding byte for byte, and calls that need no device fail cleanly."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import persistent_tile_scheduled_gb300 as pts
+from persistent_tile_scheduled_gb300 import gemm as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pts_gemm.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared_functions() == sorted(g.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pts.load()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", pts._build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (gemm_\w+)", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_status_strings():
+    for s in range(6):
+        assert pts.gemm_status_string(s)
+    assert pts.gemm_status_string(99) == "unknown status"
+
+
+def test_calls_without_a_handle_are_rejected():
+    lib = pts.load()
+    assert lib.gemm_run(None, 8, 8, 8, None, None, None, 0, 0, 1.0, 1.0, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_create(None, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_destroy(None) == g.GEMM_OK
+    info = g.gemm_launch_info_t()
+    assert lib.gemm_query(None, 8, 8, 8, 0, 0, ctypes.byref(info)) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_bad_options_are_rejected_before_touching_a_device():
+    lib = pts.load()
+    h = ctypes.c_void_p()
+    for bad in (g.make_opts(cta_group=3), g.make_opts(stages=1), g.make_opts(stages=99),
+                g.make_opts(group_size_m=-1), g.make_opts(debug_flags=0x80)):
+        assert lib.gemm_create(ctypes.byref(h), 0, ctypes.byref(bad)) == g.GEMM_ERR_INVALID_ARG
+        assert h.value is None
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="a GPU is present")
+def test_create_without_a_gpu_fails_cleanly():
+    h = ctypes.c_void_p()
+    st = pts.load().gemm_create(ctypes.byref(h), 0, None)
+    assert st in (g.GEMM_ERR_CUDA, g.GEMM_ERR_UNSUPPORTED) and h.value is None
+
+
+def test_struct_layouts_match_the_header():
+    src = r"""
+    #include <stdio.h>
+    #include <stddef.h>
+    #include "pts_gemm.h"
+    int main(void) {
+      printf("%zu %zu %zu %zu\n", sizeof(gemm_opts_t), offsetof(gemm_opts_t, debug_flags),
+             offsetof(gemm_opts_t, fault_arg), offsetof(gemm_opts_t, timeout_ns));
+      printf("%zu %zu\n", sizeof(gemm_tile_record_t), offsetof(gemm_tile_record_t, smid));
+      printf("%zu %zu %zu %zu\n", sizeof(gemm_launch_info_t), offsetof(gemm_launch_info_t, tiles_m),
+             offsetof(gemm_launch_info_t, grid_ctas), offsetof(gemm_launch_info_t, threads));
+      return 0;
+    }
+    """
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
+    got = [int(v) for v in out]
+    want = [ctypes.sizeof(g.gemm_opts_t), g.gemm_opts_t.debug_flags.offset, g.gemm_opts_t.fault_arg.offset,
+            g.gemm_opts_t.timeout_ns.offset,
+            ctypes.sizeof(g.gemm_tile_record_t), g.gemm_tile_record_t.smid.offset,
+            ctypes.sizeof(g.gemm_launch_info_t), g.gemm_launch_info_t.tiles_m.offset,
+            g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset]
+    assert got == want
+
+
+def test_no_cpu_fallback_in_the_package():
+    """The product package never imports the oracle or multiplies matrices on the host."""
+    pkg = os.path.join(ROOT, "persistent_tile_scheduled_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                text = open(os.path.join(dirpath, f)).read()
+                for banned in ("oracle", "matmul", " @ ", "torch.mm", "einsum"):
+                    assert banned not in text, (f, banned)

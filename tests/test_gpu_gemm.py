@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Element by element on small and ragged shapes (several tiles plus partial
+tiles), on sampled outputs at the full workload sizes, bit-exact on closed
+forms, and tile coverage bit-exact against the scheduler model.
+Tolerance (max relative error normalised by s * sum_k |a||b|): 2e-3 for
+fp16/bf16, 3e-2 for e4m3 after per-tensor scaling.
+"""
+import numpy as np
+import pytest
+import torch
+
+import persistent_tile_scheduled_gb300 as pts
+import workloads as wl
+from oracle import gemm as og
+
+from helpers import (TOL, check_records, compare_full, compare_sampled, run_device)
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = [pts.GEMM_SCHED_NONPERSISTENT, pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC]
+
+
+@pytest.fixture(scope="module", params=[1, 2], ids=["cg1", "cg2"])
+def handle(request):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    h = pts.gemm_create(0, pts.make_opts(cta_group=request.param, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    yield h, request.param
+    pts.gemm_destroy(h)
+
+
+def _run_checked(h, x, sched, full=True):
+    p = x.problem
+    C = run_device(h, x, sched)
+    info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
+    st, recs, dev = pts.gemm_read_debug(h, int(info.tiles))
+    assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
+    check_records(recs, info, sched)
+    err = compare_full(x, C) if full else compare_sampled(x, C, info.tile_m, info.tile_n)
+    assert err <= TOL[p.dtype], f"rel err {err}"
+    return C, err
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_fp16_512_all_schedulers(handle, sched):
+    h, _ = handle
+    x = wl.make_inputs(wl.fp16_512()[0])
+    _run_checked(h, x, sched)
+
+
+RAGGED = [(1, 8, 16), (129, 264, 80), (300, 520, 208), (257, 8, 16), (640, 1000, 1040), (2000, 48, 64)]
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16, wl.E4M3])
+@pytest.mark.parametrize("shape", RAGGED, ids=[f"{m}x{n}x{k}" for m, n, k in RAGGED])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_ragged_shapes(handle, dtype, shape, sched):
+    h, _ = handle
+    M, N, K = shape
+    dist = "normal" if dtype == wl.E4M3 else "uniform"
+    x = wl.make_inputs(wl.Problem("ragged", M, N, K, dtype, dist, 17 + M + N + K))
+    _run_checked(h, x, sched)
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16, wl.E4M3])
+def test_identity_and_permutation_bit_exact(handle, dtype):
+    """One non-zero product per output: the result is exactly b (or permuted b)."""
+    h, _ = handle
+    M = K = 512
+    N = 264
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(K)
+    P = np.zeros((M, K), np.float32)
+    P[np.arange(M), perm] = 1.0
+    td = {wl.F16: torch.float16, wl.BF16: torch.bfloat16, wl.E4M3: torch.float8_e4m3fn}[dtype]
+    Bv = torch.from_numpy(rng.uniform(-2, 2, (N, K)).astype(np.float32)).to(td)
+    for mat in (np.eye(M, dtype=np.float32), P):
+        A = torch.from_numpy(mat).to(td)
+        x = wl.Inputs(wl.Problem("perm", M, N, K, dtype, "uniform", 0), A, Bv, 1.0, 1.0)
+        C = run_device(h, x, pts.GEMM_SCHED_CLC)
+        st, dev = pts.gemm_check(h)
+        assert st == 0
+        b = Bv.double().numpy().T                           # K x N
+        want = b[np.nonzero(mat)[1], :]
+        got = C.double().cpu().numpy()
+        assert np.array_equal(got, want)
+
+
+def test_k_zero_writes_zeros(handle):
+    h, _ = handle
+    C = torch.full((64, 48), 7.0, dtype=torch.float16, device="cuda")
+    pts.gemm_run(h, 64, 48, 0, None, None, C, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+    torch.cuda.synchronize()
+    assert not C.any()
+
+
+def test_empty_m_or_n_launches_nothing(handle):
+    h, _ = handle
+    pts.gemm_run(h, 0, 64, 64, None, None, None, pts.GEMM_BF16, pts.GEMM_SCHED_CLC)
+    pts.gemm_run(h, 64, 0, 64, None, None, None, pts.GEMM_BF16, pts.GEMM_SCHED_CLC)
+    assert pts.gemm_check(h)[0] == 0
+
+
+def test_invalid_arguments_are_rejected(handle):
+    h, _ = handle
+    A = torch.zeros(64, 72, dtype=torch.float16, device="cuda")
+    C = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(pts.GemmError):     # K not a multiple of 8
+        pts.gemm_run(h, 64, 64, 12, A, A, C, pts.GEMM_F16, 1)
+    with pytest.raises(pts.GemmError):     # misaligned pointer
+        pts.gemm_run(h, 64, 64, 64, A.data_ptr() + 2, A, C, pts.GEMM_F16, 1)
+    with pytest.raises(pts.GemmError):     # bad scheduler
+        pts.gemm_run(h, 64, 64, 64, A, A, C, pts.GEMM_F16, 7)
+    with pytest.raises(pts.GemmError):     # e4m3 scale must be positive
+        pts.gemm_run(h, 64, 64, 64, A, A, C, pts.GEMM_E4M3, 1, 0.0, 1.0)
+
+
+def test_run_host_matches_device_path(handle):
+    h, _ = handle
+    x = wl.custom(300, 264, 128, wl.BF16, "uniform", 3)
+    Cd = run_device(h, x, pts.GEMM_SCHED_STATIC)
+    Ch = torch.empty(300, 264, dtype=torch.bfloat16).pin_memory()
+    pts.gemm_run_host(h, 300, 264, 128, x.A.pin_memory(), x.B.pin_memory(), Ch, wl.BF16, pts.GEMM_SCHED_STATIC)
+    assert torch.equal(Cd.cpu().view(torch.int16), Ch.view(torch.int16))
+
+
+# ---------------------------------------------------------------- full sizes
+
+FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
+        + [("bf16_8192_ksweep", k) for k in (256, 8192)]
+        + [("e4m3_8192", None)]
+        + [("bf16_tail", i) for i in range(3)])
+
+
+def _full_problem(name, arg):
+    if name == "fp16_4096_ksweep":
+        return wl.fp16_4096_ksweep([arg])[0]
+    if name == "bf16_8192_ksweep":
+        return wl.bf16_8192_ksweep([arg])[0]
+    if name == "e4m3_8192":
+        return wl.e4m3_8192()[0]
+    return wl.bf16_tail()[arg]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,arg", FULL, ids=[f"{n}-{a}" for n, a in FULL])
+def test_full_size_sampled(handle, name, arg):
+    h, _ = handle
+    x = wl.make_inputs(_full_problem(name, arg))
+    for sched in SCHEDS:
+        _run_checked(h, x, sched, full=False)
+
+
+# ---------------------------------------------------------------- CLC extras
+
+@pytest.mark.parametrize("stop_at", [0, 1, 3])
+def test_clc_injected_request_failure_keeps_coverage(stop_at):
+    """Every CTA behaves as if its stop_at-th request had failed; the clusters
+    it would have cancelled launch and run their own tiles."""
+    h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS | pts.GEMM_DEBUG_CLC_STOP_AT,
+                                         fault_arg=stop_at))
+    try:
+        x = wl.custom(2048, 2048, 256, wl.BF16, "uniform", 11)
+        _run_checked(h, x, pts.GEMM_SCHED_CLC)
+    finally:
+        pts.gemm_destroy(h)
+
+
+def test_two_gemms_on_two_streams():
+    """Two CLC GEMMs in flight at once on one GPU: both exact in coverage and
+    within tolerance (the concurrency case CLC redistributes work for)."""
+    hs = [pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS)) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    try:
+        xs = [wl.make_inputs(wl.bf16_tail()[0]), wl.make_inputs(wl.bf16_tail()[2])]
+        dev_in = [(x.A.cuda(), x.B.cuda()) for x in xs]
+        Cs = [torch.empty(x.problem.M, x.problem.N, dtype=torch.bfloat16, device="cuda") for x in xs]
+        torch.cuda.synchronize()
+        for h, s, x, (A, B), C in zip(hs, streams, xs, dev_in, Cs):
+            p = x.problem
+            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, pts.GEMM_SCHED_CLC, 1.0, 1.0, s)
+        for h, s, x, C in zip(hs, streams, xs, Cs):
+            p = x.problem
+            info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, pts.GEMM_SCHED_CLC)
+            st, recs, dev = pts.gemm_read_debug(h, int(info.tiles), s)
+            assert st == 0
+            check_records(recs, info, pts.GEMM_SCHED_CLC)
+            assert compare_sampled(x, C, info.tile_m, info.tile_n) <= TOL[p.dtype]
+    finally:
+        for h in hs:
+            pts.gemm_destroy(h)
