@@ -1,0 +1,443 @@
+"""Benchmark: GEMM TFLOP/s and fraction of tensor peak vs K, per scheduler.
+
+Workload (the fp16 K sweep of "[Persistent] Performance on 09-persistent-matmul
+on A100 worse than non-persistent": M = N = 4096, K = 128..4096 step 128,
+128x256x64 tiles, GROUP_SIZE_M 8).  One step = the 32 GEMMs of the sweep, each
+on its own A, B, C buffers (2.1 GB together, far above the 129 MB L2, so no
+GEMM finds its operands in L2 from the step before).  The step runs once per
+scheduler (non-persistent, static, CLC); the headline value is the static
+persistent scheduler.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  Under torchrun every rank runs the same sweep on its own
+GPU (independent replicas, no collective on the data path); times are the max
+over ranks and value = all ranks' FLOPs / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "GEMM TFLOPS & % of tensor peak vs K, per scheduler (nonpersist/static/CLC)"
+UNIT = "TFLOP/s"
+WORKLOAD = ("fp16 GEMM M=N=4096, K=128..4096 step 128 (32 GEMMs per step), A,B ~ N(0,1)/sqrt(K), "
+            "fp32 accumulate, fp16 C, row-major A, column-major B")
+SCHED_NAMES = ["nonpersistent", "static", "clc"]
+HEADLINE = "static"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["persistent_tile_scheduled_gb300/csrc/gemm_kernel.cuh",
+                  "persistent_tile_scheduled_gb300/csrc/ptx.cuh",
+                  "persistent_tile_scheduled_gb300/csrc/gemm_params.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------- setup
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, *keys):
+    for k in keys:
+        v = peaks.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "tflops", "gbs"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """Per-launch DRAM traffic of the GEMM kernel from the committed ncu summary,
+    only if it was taken on the kernel sources as they are now."""
+    path = os.path.join(ROOT, "profiles", "gemm_kernel_fp16_4096_ksweep.json")
+    if not os.path.exists(path):
+        return None, None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_sources_sha256_16") != kernel_hash():
+        return None, "stale"
+    return d.get("dram_bytes_per_launch_k4096"), d.get("launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", delete=False, suffix=".csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start: float, t_end: float):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist):
+    """Warm-up, then `steps` timed passes over the sweep; per-K event timings."""
+    for _ in range(warmup):
+        for p, (A, B, C) in zip(problems, bufs):
+            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+    torch.cuda.synchronize()
+    st, dev = pts.gemm_check(h, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {dev:#x} after warm-up")
+    n = len(problems)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
+                ev[s][i].record(stream)
+                pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+            ev[s][n].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(dist)
+    st, dev = pts.gemm_check(h, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {dev:#x} in the timed region")
+    total_ms = ev[0][0].elapsed_time(ev[steps - 1][n])
+    per_k = [statistics.median(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(n)]
+    return total_ms, per_k, (t0, t1)
+
+
+def cpu_baseline_sample(problem, x, budget_s=10.0):
+    """The oracle as it stands on the host cores, on a bounded row sample."""
+    from oracle import gemm as og
+    p = problem
+    A, B = x.bits("A"), x.bits("B")
+    rows, spent, flops = 1, 0.0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        og.gemm(rows, p.N, p.K, A[: rows * p.K], B, p.dtype)
+        dt = time.perf_counter() - t0
+        spent, flops = dt, gemm_flops(rows, p.N, p.K)
+        if dt > budget_s / 4 or rows >= 512:
+            break
+        rows *= 4
+    return {"value": flops / spent / 1e12, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the M=N=4096, K={p.K} fp16 GEMM ({rows}x{p.N} outputs, "
+                      f"fp64 triple loop over all K), {spent:.1f} s"}
+
+
+def run_ours(args, dist, rank, world, local):
+    import persistent_tile_scheduled_gb300 as pts
+    torch.cuda.set_device(local)
+    pts.load(build_if_missing=False)
+    problems = wl.fp16_4096_ksweep(args.ks)
+    log(f"[rank {rank}] generating {len(problems)} inputs ...")
+    xs = [wl.make_inputs(p) for p in problems]
+    bufs = [(x.A.cuda(), x.B.cuda(), torch.empty(x.problem.M, x.problem.N, dtype=torch.float16, device="cuda"))
+            for x in xs]
+    stream = torch.cuda.Stream()
+    flops_step = sum(gemm_flops(p.M, p.N, p.K) for p in problems)
+
+    per_sched = {}
+    clocks = None
+    h = pts.gemm_create(local, pts.make_opts(cta_group=1))
+    try:
+        for si, name in enumerate(SCHED_NAMES):
+            if name not in args.scheds:
+                continue
+            sampler = ClockSampler(local) if name == HEADLINE else None
+            if sampler:
+                sampler.__enter__()
+            total_ms, per_k, (t0, t1) = time_sweep(pts, h, bufs, problems, si, args.steps, args.warmup, stream, dist)
+            if sampler:
+                sampler.__exit__(None, None, None)
+                clocks = sampler.summary(t0, t1)
+            total_ms = max_over_ranks(dist, total_ms)
+            ms_step = total_ms / args.steps
+            per_sched[name] = {
+                "value": world * flops_step / (ms_step * 1e-3) / 1e12,
+                "ms_per_step": ms_step,
+                "per_k_tflops": [round(gemm_flops(p.M, p.N, p.K) / (t * 1e-3) / 1e12, 1)
+                                 for p, t in zip(problems, per_k)],
+                "per_k_ms": per_k,
+            }
+            log(f"[rank {rank}] {name}: {per_sched[name]['value']:.1f} TFLOP/s, {ms_step:.3f} ms/step")
+
+        # end-to-end through the public host-buffer API (copies inside the timed region)
+        e2e = None
+        if args.e2e:
+            e2e = end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream)
+        extra = square_8192(pts, local, stream) if args.square and rank == 0 else None
+    finally:
+        pts.gemm_destroy(h)
+    return finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step)
+
+
+def end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream):
+    host = [(x.A.pin_memory(), x.B.pin_memory(),
+             torch.empty(x.problem.M, x.problem.N, dtype=torch.float16).pin_memory()) for x in xs]
+    e2e_steps = max(1, min(args.steps, 10))
+    for p, (A, B, C) in zip(problems, host):
+        pts.gemm_run_host(h, p.M, p.N, p.K, A, B, C, p.dtype, 1, 1.0, 1.0, stream)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for p, (A, B, C) in zip(problems, host):
+            pts.gemm_run_host(h, p.M, p.N, p.K, A, B, C, p.dtype, 1, 1.0, 1.0, stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, (time.perf_counter() - t0) / e2e_steps)
+    bi = sum(A.numel() * A.element_size() + B.numel() * B.element_size() for A, B, _ in host)
+    bo = sum(C.numel() * C.element_size() for _, _, C in host)
+    return {"value": world * flops_step / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "api": "gemm_run_host (pinned host A, B, C)", "steps": e2e_steps}
+
+
+def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step):
+    peaks, peaks_src = load_peaks()
+    tensor_peak = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
+    tensor_peak_sus = peak_value(peaks, "bf16_tflops_sustained")
+    hbm = peak_value(peaks, "hbm_gbs", "hbm_GBs")
+    head = per_sched.get(HEADLINE) or next(iter(per_sched.values()))
+    traffic, launch = profile_traffic()
+    achieved = head["value"] / world
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": UNIT,
+                "frac": round(achieved / tensor_peak, 4) if tensor_peak else None,
+                "traffic": traffic if isinstance(traffic, (int, float)) else None,
+                "peak_source": f"{peaks_src} bf16 dense (fp16 runs at the same tensor rate), burst",
+                "achieved_def": "sum of 2MNK over the 32 launches / sum of their CUDA-event durations"}
+    if traffic is not None and launch:
+        roofline["traffic_launch"] = launch
+    per_k_roof = []
+    for p, t in zip(problems, head["per_k_ms"]):
+        fl = gemm_flops(p.M, p.N, p.K)
+        q = 2.0 * (p.M * p.K + p.N * p.K) + 2.0 * p.M * p.N
+        attain = min(tensor_peak * 1e12, fl / q * hbm * 1e9) if tensor_peak and hbm else None
+        per_k_roof.append({"K": p.K, "tflops": round(fl / (t * 1e-3) / 1e12, 1),
+                           "bound": "tensor" if attain == (tensor_peak or 0) * 1e12 else "hbm",
+                           "attainable_tflops": round(attain / 1e12, 1) if attain else None,
+                           "frac": round(fl / (t * 1e-3) / attain, 3) if attain else None})
+
+    line = {
+        "metric": METRIC, "value": round(head["value"], 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1)/sqrt(K), rounded to fp16)",
+        "config": {"workload": WORKLOAD, "tile": "128x256x64", "group_size_m": 8, "cta_group": 1,
+                   "sched": HEADLINE, "stages": 4,
+                   "l2": "no flush: one step's 32 distinct A,B,C sets (2.1 GB) exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_tensor_peak": round(achieved / tensor_peak, 4) if tensor_peak else None,
+        "per_scheduler": {k: {kk: vv for kk, vv in v.items() if kk != "per_k_ms"} for k, v in per_sched.items()},
+        "per_k_roofline": per_k_roof,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(problems),
+        "clocks": clocks,
+        "peaks": {"tensor_tflops": tensor_peak, "tensor_tflops_sustained": tensor_peak_sus, "hbm_gbs": hbm,
+                  "source": peaks_src},
+    }
+    if extra is not None:
+        line["square_8192_bf16"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(problems[-1], xs[-1])
+    return line
+
+
+def square_8192(pts, dev, stream, reps=10):
+    """bf16 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
+    p = wl.bf16_8192_ksweep([8192])[0]
+    x = wl.make_inputs(p)
+    A, B = x.A.cuda(), x.B.cuda()
+    C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+    out = {}
+    for cg in (1, 2):
+        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
+        try:
+            for si, name in enumerate(SCHED_NAMES):
+                for _ in range(3):
+                    pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, 1.0, 1.0, stream)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                with torch.cuda.stream(stream):
+                    for r in range(reps):
+                        ev[r].record(stream)
+                        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, 1.0, 1.0, stream)
+                    ev[reps].record(stream)
+                torch.cuda.synchronize()
+                if pts.gemm_check(h, stream)[0] != 0:
+                    raise RuntimeError("device error in the 8192^3 run")
+                ms = statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+                out[f"cg{cg}_{name}"] = round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1)
+        finally:
+            pts.gemm_destroy(h)
+    out["note"] = "median of 10 back-to-back launches; A,B = 256 MB > L2"
+    return out
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, dist, rank, world):
+    """The oracle as it stands, on the host cores: every step computes rows
+    0..R-1 of all 32 GEMMs of the sweep (R x 4096 outputs each)."""
+    if rank != 0:
+        return None
+    from oracle import gemm as og
+    problems = wl.fp16_4096_ksweep()
+    xs = [wl.make_inputs(p) for p in problems]
+    rows = args.ref_rows
+    bits = [(x.bits("A")[: rows * x.problem.K], x.bits("B")) for x in xs]
+
+    def step():
+        for p, (A, B) in zip(problems, bits):
+            og.gemm(rows, p.N, p.K, A, B, p.dtype)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = sum(gemm_flops(rows, p.N, p.K) for p in problems)
+    v = flops / dt / 1e12
+    sample = f"rows 0..{rows - 1} of each of the 32 sweep GEMMs ({rows}x4096 outputs per K, fp64 triple loop)"
+    return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as our arm)",
+            "config": {"workload": WORKLOAD, "sample": sample}, "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-rows", type=int, default=2)
+    ap.add_argument("--no-square", dest="square", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
+    ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warm-up raised to 3 steps")
+        args.warmup = 3
+    dist, rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, dist, rank, world)
+    else:
+        line = run_ours(args, dist, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

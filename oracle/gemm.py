@@ -196,11 +196,17 @@ def gemm_loops(M, N, K, A_bits, B_bits, dtype, s=1.0):
 # comparison metric
 # ---------------------------------------------------------------------------
 
-def rel_err(C_test, C_ref, C_abs):
-    """max |C_test - C_ref| / (s * sum_k |a||b|) over the compared elements.
+OUT_UNIT_ROUNDOFF = {F16: 2.0 ** -11, BF16: 2.0 ** -8}   # RNE to the output format: |err| <= u |x|
 
-    Elements whose normaliser is 0 must be exactly 0 in C_test; any that are
-    not make the error infinite.
+
+def rel_err(C_test, C_ref, C_abs, out_u: float = 0.0):
+    """max (|C_test - C_ref| - out_u * |C_ref|)+ / (s * sum_k |a||b|).
+
+    ``out_u`` is the unit roundoff of the output format (2^-11 for fp16,
+    2^-8 for bf16): rounding the exact result to that format may move it by up
+    to out_u * |C_ref|, which no kernel can avoid, so that much is not charged.
+    ``out_u = 0`` gives the plain normalised error.  Elements whose normaliser
+    is 0 must be exactly 0 in C_test; any that are not make the error infinite.
     """
     C_test = np.asarray(C_test, np.float64)
     C_ref = np.asarray(C_ref, np.float64)
@@ -212,4 +218,5 @@ def rel_err(C_test, C_ref, C_abs):
         return float("inf")
     if not np.any(~zero):
         return 0.0
-    return float(np.max(np.abs(C_test[~zero] - C_ref[~zero]) / C_abs[~zero]))
+    d = np.abs(C_test[~zero] - C_ref[~zero]) - out_u * np.abs(C_ref[~zero])
+    return float(max(np.max(d / C_abs[~zero]), 0.0))

@@ -26,10 +26,15 @@ def dequant(x: wl.Inputs) -> float:
     return 1.0 / (float(x.scale_a) * float(x.scale_b)) if x.problem.dtype == wl.E4M3 else 1.0
 
 
+def out_u(dtype: int) -> float:
+    """Unit roundoff of the output format (fp16 C for fp16 in, bf16 C otherwise)."""
+    return og.OUT_UNIT_ROUNDOFF[og.F16 if dtype == wl.F16 else og.BF16]
+
+
 def compare_full(x: wl.Inputs, C: torch.Tensor):
     p = x.problem
     ref, ref_abs = og.gemm(p.M, p.N, p.K, x.bits("A"), x.bits("B"), p.dtype, dequant(x))
-    return og.rel_err(C.double().cpu().numpy(), ref, ref_abs)
+    return og.rel_err(C.double().cpu().numpy(), ref, ref_abs, out_u(p.dtype))
 
 
 def sample_positions(M, N, tile_m, tile_n, n_random=4096, seed=0):
@@ -53,7 +58,7 @@ def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, see
     ii, jj = sample_positions(p.M, p.N, tile_m, tile_n, seed=seed)
     ref, ref_abs = og.gemm_sampled(p.M, p.N, p.K, x.bits("A"), x.bits("B"), p.dtype, ii, jj, dequant(x))
     got = C.double().cpu().numpy()[ii, jj]
-    return og.rel_err(got, ref, ref_abs)
+    return og.rel_err(got, ref, ref_abs, out_u(p.dtype))
 
 
 def check_records(records, info, sched: int, group_m: int = 8):

@@ -239,9 +239,16 @@ def test_rel_err_planted_mistakes():
     B = _random_finite_bits(rng, N * K, og.BF16)
     C, Cabs = og.gemm(M, N, K, A, B, og.BF16)
     assert og.rel_err(C, C, Cabs) == 0.0
-    # bf16 output rounding alone stays inside the 2e-3 budget
+    # rounding to the output format moves a value by at most u |x| (RNE):
+    # not charged when out_u is given, charged (and possibly above 2e-3 for
+    # bf16, whose u = 2^-8) when it is not
+    for tdt, u in ((torch.bfloat16, 2.0 ** -8), (torch.float16, 2.0 ** -11)):
+        Cr = torch.from_numpy(C).to(tdt).double().numpy()
+        assert og.rel_err(Cr, C, Cabs, out_u=u) == 0.0
+        assert 0.0 < og.rel_err(Cr, C, Cabs) <= u
+    # one output-format ulp too many is charged
     Cr = torch.from_numpy(C).to(torch.bfloat16).double().numpy()
-    assert og.rel_err(Cr, C, Cabs) <= 2.0 ** -9
+    assert og.rel_err(Cr * (1 + 2.0 ** -6), C, Cabs, out_u=2.0 ** -8) > 0.0
     # a dropped k term, a sign flip and a transposed output all fail it
     a = og.decode_np(A, og.BF16).reshape(M, K)
     b = og.decode_np(B, og.BF16).reshape(N, K)
