@@ -65,6 +65,12 @@ typedef enum {
  * try_cancel request (0-based) had failed: it does not issue it and stops
  * after its current tile.  Clusters that were therefore not cancelled launch
  * and run their own tile, so coverage stays exact. */
+#define GEMM_DEBUG_FAULT_SKIP_TMA 0x4u
+/* test hook for the bounded waits: every producer announces its fault_arg-th
+ * stage load (0-based) but does not issue it, so the MMA warp's wait on that
+ * stage runs past timeout_ns.  The kernel records the time-out, stops every
+ * role, frees its resources and returns; gemm_check then reports
+ * GEMM_ERR_TIMEOUT and C is unspecified.  The context stays usable. */
 
 typedef struct gemm_opts {
     int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair); 0 = 1 */
@@ -72,7 +78,7 @@ typedef struct gemm_opts {
     int stages;                     /* shared-memory ring depth; 0 = the most that fits */
     int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */
     unsigned debug_flags;           /* GEMM_DEBUG_* */
-    int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT */
+    int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
 } gemm_opts_t;
 
@@ -83,7 +89,10 @@ typedef struct gemm_tile_record {
     uint32_t owner;    /* cluster index (blockIdx.x / cta_group) that ran it */
     uint32_t iter;     /* how many tiles that cluster had run before it */
     uint32_t smid;     /* SM of the (leader) CTA */
-    uint32_t reserved[3];
+    /* low 32 bits of the GPU global timer (ns) when: the MMA thread began the
+     * tile, the epilogue saw its accumulator complete, the epilogue issued the
+     * tile's last store (leader CTA) */
+    uint32_t t_mma_start, t_acc_full, t_stored;
 } gemm_tile_record_t;
 
 /* Launch shape chosen for a problem. */

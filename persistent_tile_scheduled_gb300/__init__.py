@@ -5,7 +5,7 @@ package only builds it and marshals arguments into its C ABI
 (include/pts_gemm.h).  Importing the package does not load the library; the
 first call does, and raises if it cannot.
 """
-from .gemm import (GEMM_BF16, GEMM_DEBUG_CLC_STOP_AT, GEMM_DEBUG_RECORDS, GEMM_E4M3, GEMM_F16,  # noqa: F401
+from .gemm import (GEMM_BF16, GEMM_DEBUG_CLC_STOP_AT, GEMM_DEBUG_FAULT_SKIP_TMA, GEMM_DEBUG_RECORDS, GEMM_E4M3, GEMM_F16,  # noqa: F401
                    GEMM_SCHED_CLC, GEMM_SCHED_NONPERSISTENT, GEMM_SCHED_STATIC, SCHEDS, GemmError,
                    gemm_check, gemm_create, gemm_destroy, gemm_query, gemm_read_debug, gemm_run,
                    gemm_run_host, gemm_status_string, load, make_opts)

@@ -263,7 +263,8 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT)) return GEMM_ERR_INVALID_ARG;
+    if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
+        return GEMM_ERR_INVALID_ARG;
 
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return cuda_fail(cudaErrorNoDevice);

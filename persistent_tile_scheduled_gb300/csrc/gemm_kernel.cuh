@@ -275,15 +275,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ctl.wait(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
                     const int x = kb * KELEMS;
                     const uint32_t fb = full0 + 8 * stage;
+                    // test hook: announce the stage's bytes but never load them,
+                    // so the MMA warp's bounded wait on this stage runs out
+                    const bool skip = (p.debug_flags & DBG_FAULT_SKIP_TMA) && issued == p.fault_arg;
                     if constexpr (CG == 1) {
                         mbar_arrive_expect_tx(fb, TX_BYTES);
-                        tma_load_2d(sA + stage * SA, &tmA, fb, x, ya);
-                        tma_load_2d(sB + stage * SB, &tmB, fb, x, yb);
+                        if (!skip) {
+                            tma_load_2d(sA + stage * SA, &tmA, fb, x, ya);
+                            tma_load_2d(sB + stage * SB, &tmB, fb, x, yb);
+                        }
                     } else {
                         if (leader) mbar_arrive_expect_tx(fb, TX_BYTES);
                         const uint32_t fbc = mapa(fb, 0u);
-                        tma_load_2d_pair(sA + stage * SA, &tmA, fbc, x, ya);
-                        tma_load_2d_pair(sB + stage * SB, &tmB, fbc, x, yb);
+                        if (!skip) {
+                            tma_load_2d_pair(sA + stage * SA, &tmA, fbc, x, ya);
+                            tma_load_2d_pair(sB + stage * SB, &tmB, fbc, x, yb);
+                        }
                     }
                     ++issued;
                     if (++stage == S) {
@@ -391,6 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ring_read(i, w) || w < 0) break;
                 if (!ctl.wait(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
+                if (p.records != nullptr) {
+                    int tm, tn;
+                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                    p.records[static_cast<long long>(tm) * p.tiles_n + tn].t_mma_start =
+                        static_cast<uint32_t>(globaltimer_ns());
+                }
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -445,14 +458,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            if (p.records != nullptr && e == 0 && lane == 0) {
-                TileRecord *r = p.records + (static_cast<long long>(tm) * p.tiles_n + tn);
-                atomicAdd(&r->visits, 1u);
+            TileRecord *rec = (p.records != nullptr && e == 0 && lane == 0)
+                                  ? p.records + (static_cast<long long>(tm) * p.tiles_n + tn)
+                                  : nullptr;
+            if (rec != nullptr) {
+                atomicAdd(&rec->visits, 1u);
                 if (leader) {
-                    r->work = static_cast<uint32_t>(w);
-                    r->owner = static_cast<uint32_t>(cluster_id);
-                    r->iter = static_cast<uint32_t>(i);
-                    r->smid = smid();
+                    rec->work = static_cast<uint32_t>(w);
+                    rec->owner = static_cast<uint32_t>(cluster_id);
+                    rec->iter = static_cast<uint32_t>(i);
+                    rec->smid = smid();
+                    rec->t_acc_full = static_cast<uint32_t>(globaltimer_ns());
                 }
             }
             const int row0 = tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta
@@ -500,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++nstore;
             }
+            if (rec != nullptr && leader) rec->t_stored = static_cast<uint32_t>(globaltimer_ns());
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;

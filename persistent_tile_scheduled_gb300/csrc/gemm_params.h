@@ -25,10 +25,13 @@ enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
 
 // Device status block: [0] first error code, [1] where, [2] block, [3] error count.
 enum : int32_t { DEV_ERR_TIMEOUT = 1 };
-enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u };
+enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u, DBG_FAULT_SKIP_TMA = 0x4u };
 
+// Per-tile debug record.  Times are the low 32 bits of %globaltimer (ns):
+// the MMA thread starting the tile, the epilogue seeing its accumulator
+// complete, the epilogue having issued the tile's last store.
 struct TileRecord {
-    uint32_t visits, work, owner, iter, smid, reserved[3];
+    uint32_t visits, work, owner, iter, smid, t_mma_start, t_acc_full, t_stored;
 };
 
 struct GemmParams {

@@ -19,6 +19,7 @@ SCHEDS = {"nonpersistent": 0, "static": 1, "clc": 2}
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_COVERAGE = range(6)
 GEMM_DEBUG_RECORDS = 0x1
 GEMM_DEBUG_CLC_STOP_AT = 0x2
+GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
             "gemm_read_debug", "gemm_destroy", "gemm_status_string")
@@ -32,7 +33,8 @@ class gemm_opts_t(ctypes.Structure):
 
 class gemm_tile_record_t(ctypes.Structure):
     _fields_ = [("visits", ctypes.c_uint32), ("work", ctypes.c_uint32), ("owner", ctypes.c_uint32),
-                ("iter", ctypes.c_uint32), ("smid", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 3)]
+                ("iter", ctypes.c_uint32), ("smid", ctypes.c_uint32), ("t_mma_start", ctypes.c_uint32),
+                ("t_acc_full", ctypes.c_uint32), ("t_stored", ctypes.c_uint32)]
 
 
 class gemm_launch_info_t(ctypes.Structure):

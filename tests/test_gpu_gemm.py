@@ -190,3 +190,32 @@ def test_two_gemms_on_two_streams():
     finally:
         for h in hs:
             pts.gemm_destroy(h)
+
+
+# ------------------------------------------------------------ bounded waits
+
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("sched", [pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC])
+def test_wait_time_out_is_reported_and_the_context_survives(cg, sched):
+    """A stage load that never arrives makes the MMA warp's bounded wait run
+    out: the launch reports GEMM_ERR_TIMEOUT (nothing traps, nothing hangs) and
+    the next GEMM on the same context is exact."""
+    x = wl.custom(512, 512, 1024, wl.BF16, "uniform", 2)
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, debug_flags=pts.GEMM_DEBUG_FAULT_SKIP_TMA,
+                                         fault_arg=5, timeout_ns=20_000_000))
+    try:
+        run_device(h, x, sched)
+        st, dev = pts.gemm_check(h)
+        assert st == pts.gemm.GEMM_ERR_TIMEOUT
+        assert dev >> 24 == 1                          # device error code: time-out
+        assert (dev >> 16) & 0xFF in (1, 2, 4)        # a stage, MMA or accumulator wait gave up
+        assert pts.gemm_check(h)[0] == 0              # the status block was cleared
+    finally:
+        pts.gemm_destroy(h)
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg))
+    try:
+        C = run_device(h, x, sched)
+        assert pts.gemm_check(h)[0] == 0
+        assert compare_full(x, C) <= TOL[wl.BF16]
+    finally:
+        pts.gemm_destroy(h)
