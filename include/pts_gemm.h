@@ -154,6 +154,46 @@ gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status);
 gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records,
                               int64_t n_tiles, int *device_status);
 
+/* ---- allocation-free entry point ---------------------------------------
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they need a GEMM: runtimes that reserve
+ * all device memory at start-up and refuse later allocations, and
+ * latency-critical loops that cannot accept the implicit synchronisation
+ * cudaMalloc / cudaFree may perform.  gemm_create allocates, so those callers
+ * cannot use the handle API.
+ *
+ * gemm_run_noalloc computes C = A . B exactly like gemm_run (same layouts,
+ * size and alignment rules, K == 0 writes zeros) on the CURRENT device, with
+ * the default options (group_size_m 8, deepest ring, 1 s wait limit) and the
+ * given cta_group (1 or 2).  It allocates nothing: no cudaMalloc, no cudaFree,
+ * no host heap.  The kernel's scratch -- a 4-word device status block and one
+ * gemm_tile_record_t per output tile (the coverage counters) -- lives in a
+ * file-scope __device__ array of 256 + 32 * GEMM_NOALLOC_MAX_TILES bytes
+ * (512.25 KiB) that every GPU which loads the library holds until the
+ * process exits.
+ *   - Problems with more than GEMM_NOALLOC_MAX_TILES output tiles (tile
+ *     128x256 for cta_group 1, 256x256 for cta_group 2) are rejected with
+ *     GEMM_ERR_INVALID_ARG before anything is launched.
+ *   - The first call on a device does a one-time set-up on that device (the
+ *     scratch array's device address via cudaGetSymbolAddress, kernel
+ *     attributes, occupancy); make that first call before any stream capture.
+ *   - Every call clears the status block and its tiles' records with a
+ *     cudaMemsetAsync on `stream`, then launches on `stream`.
+ *   - All calls share the one scratch array, which keeps the last call's
+ *     contents: calls whose kernels overlap on the GPU (different streams,
+ *     or different host threads) race on it.  Order them on one stream.
+ *   - device_status == NULL: asynchronous, returns after the launch (device
+ *     errors are then not reported).  Otherwise the call synchronises
+ *     `stream`, stores the raw first device error word (0 = none) and returns
+ *     GEMM_ERR_TIMEOUT on a device wait time-out, GEMM_ERR_COVERAGE if a tile
+ *     was not stored exactly once by its CTA (pair), else GEMM_OK. */
+#define GEMM_NOALLOC_MAX_TILES 16384
+gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                               const void *A, const void *B, void *C,
+                               gemm_dtype_t dtype, gemm_sched_t sched,
+                               float scale_a, float scale_b, int cta_group,
+                               void *stream, int *device_status);
+
 /* Free the handle and everything it owns.  NULL is accepted. */
 gemm_status_t gemm_destroy(gemm_handle_t h);
 

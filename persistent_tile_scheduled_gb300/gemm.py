@@ -22,7 +22,8 @@ GEMM_DEBUG_CLC_STOP_AT = 0x2
 GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
-            "gemm_read_debug", "gemm_destroy", "gemm_status_string")
+            "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc")
+GEMM_NOALLOC_MAX_TILES = 16384
 
 
 class gemm_opts_t(ctypes.Structure):
@@ -81,6 +82,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gemm_read_debug.restype = st
     lib.gemm_destroy.argtypes = [vp]
     lib.gemm_destroy.restype = st
+    lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int, f32, f32,
+                                     ctypes.c_int, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.gemm_run_noalloc.restype = st
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -154,6 +158,18 @@ def gemm_read_debug(h, n_tiles: int, stream=None):
     dev = ctypes.c_int(0)
     st = load().gemm_read_debug(h, _stream(stream), recs, int(n_tiles), ctypes.byref(dev))
     return st, recs, dev.value
+
+
+def gemm_run_noalloc(M, N, K, A, B, C, dtype, sched, scale_a=1.0, scale_b=1.0, cta_group=1, stream=None,
+                     check=False):
+    """The allocation-free entry point.  Returns (status, device status word);
+    never raises.  check=True makes the call synchronise and report device
+    errors and coverage (the C call's device_status argument)."""
+    dev = ctypes.c_int(0)
+    st = load().gemm_run_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), int(dtype), int(sched), float(scale_a),
+                                 float(scale_b), int(cta_group), _stream(stream),
+                                 ctypes.byref(dev) if check else None)
+    return st, dev.value
 
 
 def gemm_destroy(h) -> int:
