@@ -80,19 +80,32 @@ typedef struct gemm_opts {
     unsigned debug_flags;           /* GEMM_DEBUG_* */
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
+    int split;                      /* column slices per tile of the last partial wave: 0 = auto,
+                                       1 = never; 2 or 4 = slice EVERY tile (testing) */
 } gemm_opts_t;
 
-/* Per-tile record written when GEMM_DEBUG_RECORDS is set. */
+/* Work items.  Output tiles are visited in grouped order; a work item is one
+ * tile, except that the tiles of the last partial wave (the tiles left over
+ * when the tile count is not a multiple of the resident clusters) may be cut
+ * into `split` column slices of 256/split columns each, one work item per
+ * slice, so that the last wave ends early.  Work ids below full_work are
+ * whole tiles; work id full_work + split*j + h is slice h of the
+ * (full_work + j)-th tile in grouped order.
+ *
+ * Per-work-item record written when GEMM_DEBUG_RECORDS is set (work-id order). */
 typedef struct gemm_tile_record {
-    uint32_t visits;   /* CTAs that stored this tile; exactly cta_group when coverage is exact */
-    uint32_t work;     /* linear work id that mapped to this tile */
+    uint32_t visits;   /* CTAs that stored this item; exactly cta_group when coverage is exact */
+    uint32_t tile;     /* tile index tm * tiles_n + tn of the item */
+    uint32_t n_off;    /* first column of the item within its tile */
+    uint32_t n_len;    /* columns of the item (256, 128 or 64) */
     uint32_t owner;    /* cluster index (blockIdx.x / cta_group) that ran it */
-    uint32_t iter;     /* how many tiles that cluster had run before it */
+    uint32_t iter;     /* how many items that cluster had run before it */
     uint32_t smid;     /* SM of the (leader) CTA */
     /* low 32 bits of the GPU global timer (ns) when: the MMA thread began the
-     * tile, the epilogue saw its accumulator complete, the epilogue issued the
-     * tile's last store (leader CTA) */
+     * item, the epilogue saw its accumulator complete, the epilogue issued the
+     * item's last store (leader CTA) */
     uint32_t t_mma_start, t_acc_full, t_stored;
+    uint32_t reserved[2];
 } gemm_tile_record_t;
 
 /* Launch shape chosen for a problem. */
@@ -105,6 +118,9 @@ typedef struct gemm_launch_info {
     int max_active_clusters;        /* resident clusters the device holds for this kernel */
     int smem_bytes;                 /* dynamic shared memory per CTA */
     int threads;                    /* threads per CTA */
+    int split;                      /* column slices per tile of the last partial wave */
+    int64_t full_work;              /* work ids below this are whole tiles */
+    int64_t work_items;             /* work items in total */
 } gemm_launch_info_t;
 
 typedef struct gemm_ctx *gemm_handle_t;
@@ -147,12 +163,13 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * Returns GEMM_ERR_TIMEOUT if a device wait timed out since the last check. */
 gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status);
 
-/* After a run with GEMM_DEBUG_RECORDS: synchronise `stream`, copy n_tiles
- * records (tile-row-major order: index tm * tiles_n + tn) to host memory
- * `records`, and do what gemm_check does.  Returns GEMM_ERR_COVERAGE if any
- * visits count differs from the cta_group of the last run. */
+/* After a run with GEMM_DEBUG_RECORDS: synchronise `stream`, copy the
+ * n_work records of the last run (work-id order; n_work must equal its
+ * work_items) to host memory `records`, and do what gemm_check does.
+ * Returns GEMM_ERR_COVERAGE if any visits count differs from the cta_group of
+ * the last run. */
 gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records,
-                              int64_t n_tiles, int *device_status);
+                              int64_t n_work, int *device_status);
 
 /* ---- allocation-free entry point ---------------------------------------
  * The paper has no counterpart to this call; it exists for callers that
@@ -164,20 +181,21 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
  *
  * gemm_run_noalloc computes C = A . B exactly like gemm_run (same layouts,
  * size and alignment rules, K == 0 writes zeros) on the CURRENT device, with
- * the default options (group_size_m 8, deepest ring, 1 s wait limit) and the
- * given cta_group (1 or 2).  It allocates nothing: no cudaMalloc, no cudaFree,
- * no host heap.  The kernel's scratch -- a 4-word device status block and one
- * gemm_tile_record_t per output tile (the coverage counters) -- lives in a
- * file-scope __device__ array of 256 + 32 * GEMM_NOALLOC_MAX_TILES bytes
- * (512.25 KiB) that every GPU which loads the library holds until the
- * process exits.
- *   - Problems with more than GEMM_NOALLOC_MAX_TILES output tiles (tile
- *     128x256 for cta_group 1, 256x256 for cta_group 2) are rejected with
- *     GEMM_ERR_INVALID_ARG before anything is launched.
+ * the default options (group_size_m 8, deepest ring, automatic last-wave
+ * slicing, 1 s wait limit) and the given cta_group (1 or 2).  It allocates
+ * nothing: no cudaMalloc, no cudaFree, no host heap.  The kernel's scratch --
+ * a 4-word device status block and one gemm_tile_record_t per work item (the
+ * coverage counters) -- lives in a file-scope __device__ array of
+ * 256 + 48 * GEMM_NOALLOC_MAX_WORK_ITEMS bytes (768.25 KiB) that every GPU which
+ * loads the library holds until the process exits.
+ *   - Problems with more than GEMM_NOALLOC_MAX_WORK_ITEMS work items are
+ *     rejected with GEMM_ERR_INVALID_ARG before anything is launched (work
+ *     items = output tiles of 128x256 for cta_group 1 or 256x256 for
+ *     cta_group 2, plus up to 3 per tile of a sliced last wave).
  *   - The first call on a device does a one-time set-up on that device (the
  *     scratch array's device address via cudaGetSymbolAddress, kernel
  *     attributes, occupancy); make that first call before any stream capture.
- *   - Every call clears the status block and its tiles' records with a
+ *   - Every call clears the status block and its work items' records with a
  *     cudaMemsetAsync on `stream`, then launches on `stream`.
  *   - All calls share the one scratch array, which keeps the last call's
  *     contents: calls whose kernels overlap on the GPU (different streams,
@@ -185,9 +203,9 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
  *   - device_status == NULL: asynchronous, returns after the launch (device
  *     errors are then not reported).  Otherwise the call synchronises
  *     `stream`, stores the raw first device error word (0 = none) and returns
- *     GEMM_ERR_TIMEOUT on a device wait time-out, GEMM_ERR_COVERAGE if a tile
- *     was not stored exactly once by its CTA (pair), else GEMM_OK. */
-#define GEMM_NOALLOC_MAX_TILES 16384
+ *     GEMM_ERR_TIMEOUT on a device wait time-out, GEMM_ERR_COVERAGE if a work
+ *     item was not stored exactly once by its CTA (pair), else GEMM_OK. */
+#define GEMM_NOALLOC_MAX_WORK_ITEMS 16384
 gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
                                const void *A, const void *B, void *C,
                                gemm_dtype_t dtype, gemm_sched_t sched,

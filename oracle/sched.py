@@ -50,6 +50,26 @@ def swizzle(w: int, Tm: int, Tn: int, group_m: int) -> Tuple[int, int]:
     return first_m + r % rows_here, r // rows_here
 
 
+def work_items(T: int, full_work: int, split: int, tile_n: int = 256) -> List[Tuple[int, int, int, int]]:
+    """(work id, grouped-order tile index, first column, columns) of every work item.
+
+    Work ids below ``full_work`` are whole tiles.  The remaining tiles (the
+    last partial wave) are each cut into ``split`` column slices: work id
+    ``full_work + split*j + h`` is slice h of tile ``full_work + j``.  Cutting
+    the last wave's tiles does not change what is computed, only how the
+    output is partitioned among CTAs ("Neither mode creates additional
+    independent work at the tail of a grid": slicing is a separate device).
+    """
+    if not (0 <= full_work <= T and split in (1, 2, 4)):
+        raise ValueError((T, full_work, split))
+    out = [(w, w, 0, tile_n) for w in range(full_work)]
+    step = tile_n // split
+    for j in range(T - full_work):
+        for h in range(split):
+            out.append((full_work + split * j + h, full_work + j, h * step, step))
+    return out
+
+
 def static_grid(T: int, max_clusters: int) -> int:
     """Resident clusters launched by the static persistent scheduler."""
     return max(1, min(T, max_clusters)) if T > 0 else 0

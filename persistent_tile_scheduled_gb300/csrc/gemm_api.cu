@@ -37,8 +37,8 @@ struct gemm_ctx {
     gemm_opts_t opts{};
     int32_t *d_status = nullptr;              // 4 ints
     pts::TileRecord *d_records = nullptr;
-    int64_t records_cap = 0;
-    int64_t last_tiles = 0;
+    int64_t records_cap = 0;                  // in work items
+    int64_t last_work = 0;
     int last_cta_group = 1;
     void *d_host_bufs = nullptr;              // gemm_run_host staging (A | B | C)
     size_t host_bufs_cap = 0;
@@ -95,9 +95,13 @@ pts::KernelOps ops_for(int kind, int cg) { return cg == 2 ? pts::kernel_ops_cg2(
 struct Plan {
     int cg, stages, smem;
     int64_t tiles_m, tiles_n, tiles;
+    int split;               // column slices per tile of the last partial wave
+    int64_t full_work;       // work ids below this are whole tiles
+    int64_t work;            // work items in total
     int64_t grid_ctas;
     int max_active_clusters;
 };
+
 
 gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_sched_t sched)
 {
@@ -142,12 +146,14 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, gemm_dtype_t dtype, g
     }
     pl.max_active_clusters = h->occ_clusters[kind][ci];
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
-    int64_t clusters = pl.tiles;
-    if (sched == GEMM_SCHED_STATIC) {
-        int64_t cap = pl.max_active_clusters;
-        if (h->opts.max_clusters > 0 && h->opts.max_clusters < cap) cap = h->opts.max_clusters;
-        clusters = pl.tiles < cap ? pl.tiles : cap;
-    }
+    int64_t resident = pl.max_active_clusters;
+    if (h->opts.max_clusters > 0 && h->opts.max_clusters < resident) resident = h->opts.max_clusters;
+    pl.split = h->opts.split > 0 ? h->opts.split : pts::choose_split(pl.tiles, resident);
+    pl.full_work = pl.split == 1 ? pl.tiles : pl.tiles - pl.tiles % resident;
+    if (h->opts.split > 1) pl.full_work = 0;   // forced split: every tile is sliced
+    pl.work = pl.full_work + pl.split * (pl.tiles - pl.full_work);
+    int64_t clusters = pl.work;
+    if (sched == GEMM_SCHED_STATIC) clusters = pl.work < resident ? pl.work : resident;
     pl.grid_ctas = clusters * pl.cg;
     return GEMM_OK;
 }
@@ -177,11 +183,14 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
 
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
     const CUtensorMap *ma = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems);
-    const CUtensorMap *mb = get_map(h, B, uint64_t(N), uint64_t(K), dtype, pts::kTileN / pl.cg, kelems);
+    const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
+    const CUtensorMap *mb[3] = {get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows, kelems), nullptr, nullptr};
+    mb[1] = pl.split == 2 ? get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / 2, kelems) : mb[0];
+    mb[2] = pl.split == 4 ? get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / 4, kelems) : mb[0];
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
     const CUtensorMap *mc = get_map(h, C, uint64_t(M), uint64_t(N), cdt, pts::kEpiRowsPerWarp,
                                     pts::kEpiChunkCols);
-    if (!ma || !mb || !mc) return GEMM_ERR_CUDA;
+    if (!ma || !mb[0] || !mb[1] || !mb[2] || !mc) return GEMM_ERR_CUDA;
 
     pts::GemmParams p{};
     p.M = static_cast<int32_t>(M);
@@ -191,6 +200,9 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.tiles_m = static_cast<int32_t>(pl.tiles_m);
     p.tiles_n = static_cast<int32_t>(pl.tiles_n);
     p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.full_work = static_cast<int32_t>(pl.full_work);
+    p.split = pl.split;
+    p.num_work = static_cast<int32_t>(pl.work);
     p.group_m = h->opts.group_size_m;
     p.sched = static_cast<int32_t>(sched);
     p.stages = pl.stages;
@@ -201,22 +213,22 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.status = h->d_status;
     p.records = nullptr;
     if (h->opts.debug_flags & GEMM_DEBUG_RECORDS) {
-        if (h->records_cap < pl.tiles) {
+        if (h->records_cap < pl.work) {
             cudaFree(h->d_records);
             h->d_records = nullptr;
             h->records_cap = 0;
-            if (cudaMalloc(&h->d_records, size_t(pl.tiles) * sizeof(pts::TileRecord)) != cudaSuccess)
+            if (cudaMalloc(&h->d_records, size_t(pl.work) * sizeof(pts::TileRecord)) != cudaSuccess)
                 return cuda_fail(cudaErrorMemoryAllocation);
-            h->records_cap = pl.tiles;
+            h->records_cap = pl.work;
         }
-        if (cudaMemsetAsync(h->d_records, 0, size_t(pl.tiles) * sizeof(pts::TileRecord), stream) != cudaSuccess)
+        if (cudaMemsetAsync(h->d_records, 0, size_t(pl.work) * sizeof(pts::TileRecord), stream) != cudaSuccess)
             return cuda_fail(cudaErrorInvalidValue);
         p.records = h->d_records;
     }
-    h->last_tiles = pl.tiles;
+    h->last_work = pl.work;
     h->last_cta_group = pl.cg;
 
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(*ma, *mb, *mc, p, static_cast<int>(pl.grid_ctas),
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(*ma, mb, *mc, p, static_cast<int>(pl.grid_ctas),
                                                                    pl.smem, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return cuda_fail(cudaGetLastError());
@@ -263,6 +275,7 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
+    if (o.split != 0 && o.split != 1 && o.split != 2 && o.split != 4) return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
         return GEMM_ERR_INVALID_ARG;
 
@@ -366,6 +379,9 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     info->tiles_m = pl.tiles_m;
     info->tiles_n = pl.tiles_n;
     info->tiles = pl.tiles;
+    info->split = pl.split;
+    info->full_work = pl.full_work;
+    info->work_items = pl.work;
     info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;
     info->max_active_clusters = pl.max_active_clusters;
     info->smem_bytes = pl.smem;
@@ -379,19 +395,19 @@ gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status)
     return read_status(h, static_cast<cudaStream_t>(stream), device_status);
 }
 
-gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records, int64_t n_tiles,
+gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t *records, int64_t n_work,
                               int *device_status)
 {
-    if (h == nullptr || n_tiles < 0 || (n_tiles > 0 && records == nullptr)) return GEMM_ERR_INVALID_ARG;
-    if (!(h->opts.debug_flags & GEMM_DEBUG_RECORDS) || n_tiles > h->records_cap || n_tiles != h->last_tiles)
+    if (h == nullptr || n_work < 0 || (n_work > 0 && records == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (!(h->opts.debug_flags & GEMM_DEBUG_RECORDS) || n_work > h->records_cap || n_work != h->last_work)
         return GEMM_ERR_INVALID_ARG;
     static_assert(sizeof(gemm_tile_record_t) == sizeof(pts::TileRecord), "record layout");
     gemm_status_t st = read_status(h, static_cast<cudaStream_t>(stream), device_status);
-    if (n_tiles > 0 && cudaMemcpy(records, h->d_records, size_t(n_tiles) * sizeof(gemm_tile_record_t),
-                                  cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (n_work > 0 && cudaMemcpy(records, h->d_records, size_t(n_work) * sizeof(gemm_tile_record_t),
+                                 cudaMemcpyDeviceToHost) != cudaSuccess)
         return cuda_fail(cudaErrorUnknown);
     if (st != GEMM_OK) return st;
-    for (int64_t t = 0; t < n_tiles; ++t)
+    for (int64_t t = 0; t < n_work; ++t)
         if (records[t].visits != static_cast<uint32_t>(h->last_cta_group)) return GEMM_ERR_COVERAGE;
     return GEMM_OK;
 }

@@ -49,13 +49,13 @@ struct Inst {
         return cudaOccupancyMaxActiveClusters(out, gemm_kernel<KIND, CG>, &cfg);
     }
 
-    static cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+    static cudaError_t launch(const CUtensorMap &a, const CUtensorMap *const b[3], const CUtensorMap &c,
                               const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream)
     {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         fill_config(cfg, attr, grid_ctas, smem, stream);
-        return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, a, b, c, p);
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, a, *b[0], *b[1], *b[2], c, p);
     }
 
     static KernelOps ops() { return KernelOps{&set_smem, &max_active_clusters, &launch}; }

@@ -78,10 +78,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
 // 7-9 / 10-12 (kind::f16: fp16 0, bf16 1; kind::f8f6f4: e4m3 0), both
 // operands K-major (bits 15/16 = 0), N >> 3 at bits 17-22, M >> 4 at 24-28.
 template <int KIND, int CG>
-__host__ __device__ constexpr uint32_t make_idesc()
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t n)
 {
     constexpr uint32_t fmt = (KIND == 1) ? 1u : 0u;
-    constexpr uint32_t m = 128u * CG, n = static_cast<uint32_t>(kTileN);
+    constexpr uint32_t m = 128u * CG;
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
@@ -96,6 +96,30 @@ __device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int gro
     const int r = w - g * per_group;
     tm = first + r % rows;
     tn = r / rows;
+}
+
+// A work item: tile (tm, tn) and the column slice [n_off, n_off + n_len) of
+// it.  Work ids below full_work are whole tiles in grouped order; the tiles of
+// the last partial wave are cut into `split` slices each, so that wave ends
+// after 1/split of a tile's time instead of a whole one.
+struct WorkTile {
+    int tm, tn, n_off, n_len;
+};
+
+__device__ __forceinline__ WorkTile work_tile(int w, const GemmParams &p)
+{
+    WorkTile t;
+    int tile = w, sub = 0;
+    t.n_len = kTileN;
+    if (w >= p.full_work) {
+        const int q = w - p.full_work;
+        tile = p.full_work + q / p.split;
+        sub = q - (q / p.split) * p.split;
+        t.n_len = kTileN / p.split;
+    }
+    tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
+    t.n_off = sub * t.n_len;
+    return t;
 }
 
 struct WaitCtl {
@@ -164,12 +188,14 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits, fl
 template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB4,
                 const __grid_constant__ CUtensorMap tmC, const GemmParams p)
 {
+    // tmB / tmB2 / tmB4: B boxes of 256/CG, 128/CG and 64/CG rows, for whole
+    // tiles and for halves and quarters of the last wave's tiles
     constexpr int SA = stage_bytes_a();
     constexpr int SB = stage_bytes_b(CG);
     constexpr int KELEMS = (KIND == 2) ? kKBlockBytes : kKBlockBytes / 2;   // K elements per k-block
-    constexpr uint32_t TX_BYTES = static_cast<uint32_t>(CG * (SA + SB));   // per stage, whole pair
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -224,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (p.split == 2) prefetch_tmap(&tmB2);
+        if (p.split == 4) prefetch_tmap(&tmB4);
         prefetch_tmap(&tmC);
     }
     if (warp == 1) {
@@ -236,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
 
-    // ---- tile-id broadcast ring -------------------------------------------
-    // Slot r holds the id of tile i (i % kRing == r), or -1 = no more tiles.
+    // ---- work-id broadcast ring -------------------------------------------
+    // Slot r holds the id of work item i (i % kRing == r), or -1 = no more.
     auto publish = [&](int i, int w) -> bool {
         const int slot = i % kRing;
         if (i >= kRing && !ctl.wait(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
@@ -268,9 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            auto load_tile = [&](int tm, int tn) -> bool {
-                const int ya = tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
-                const int yb = tn * kTileN + static_cast<int>(rank) * (kTileN / CG);
+            auto load_tile = [&](const WorkTile &t) -> bool {
+                const int ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
+                const int yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
+                const CUtensorMap *mb = t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
+                const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!ctl.wait(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
                     const int x = kb * KELEMS;
@@ -279,17 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // so the MMA warp's bounded wait on this stage runs out
                     const bool skip = (p.debug_flags & DBG_FAULT_SKIP_TMA) && issued == p.fault_arg;
                     if constexpr (CG == 1) {
-                        mbar_arrive_expect_tx(fb, TX_BYTES);
+                        mbar_arrive_expect_tx(fb, tx);
                         if (!skip) {
                             tma_load_2d(sA + stage * SA, &tmA, fb, x, ya);
-                            tma_load_2d(sB + stage * SB, &tmB, fb, x, yb);
+                            tma_load_2d(sB + stage * SB, mb, fb, x, yb);
                         }
                     } else {
-                        if (leader) mbar_arrive_expect_tx(fb, TX_BYTES);
+                        if (leader) mbar_arrive_expect_tx(fb, tx);
                         const uint32_t fbc = mapa(fb, 0u);
                         if (!skip) {
                             tma_load_2d_pair(sA + stage * SA, &tmA, fbc, x, ya);
-                            tma_load_2d_pair(sB + stage * SB, &tmB, fbc, x, yb);
+                            tma_load_2d_pair(sB + stage * SB, mb, fbc, x, yb);
                         }
                     }
                     ++issued;
@@ -303,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             bool clc_pending = false;
             if (leader) {
-                int w = cluster_id < p.num_tiles ? cluster_id : -1;
+                int w = cluster_id < p.num_work ? cluster_id : -1;
                 bool may_request = p.sched == SCHED_CLC;
                 uint32_t clc_phase = 0;
                 ok = publish(0, w);
@@ -318,15 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             clc_pending = true;
                         }
                     }
-                    int tm, tn;
-                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                    if (!load_tile(tm, tn)) {
+                    if (!load_tile(work_tile(w, p))) {
                         ok = false;
                         break;
                     }
                     int next = -1;
                     if (p.sched == SCHED_STATIC) {
-                        next = (w + num_clusters < p.num_tiles) ? w + num_clusters : -1;
+                        next = (w + num_clusters < p.num_work) ? w + num_clusters : -1;
                     } else if (clc_pending) {
                         if (!ctl.wait(clc_bar, clc_phase, WHERE_CLC)) {
                             ok = false;
@@ -337,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t x;
                         if (clc_decode(clc_resp, x)) {
                             next = static_cast<int>(x / CG);
-                            if (next >= p.num_tiles) {   // cannot happen for a well-formed grid
+                            if (next >= p.num_work) {   // cannot happen for a well-formed grid
                                 ctl.fail(WHERE_BAD_TILE);
                                 next = -1;
                             }
@@ -357,9 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (w < 0) break;
-                    int tm, tn;
-                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                    if (!load_tile(tm, tn)) {
+                    if (!load_tile(work_tile(w, p))) {
                         ok = false;
                         break;
                     }
@@ -386,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================ MMA ==================================
         if (lane == 0 && leader) {
-            constexpr uint32_t IDESC = make_idesc<KIND, CG>();
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -398,12 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ring_read(i, w) || w < 0) break;
                 if (!ctl.wait(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
-                if (p.records != nullptr) {
-                    int tm, tn;
-                    tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                    p.records[static_cast<long long>(tm) * p.tiles_n + tn].t_mma_start =
-                        static_cast<uint32_t>(globaltimer_ns());
-                }
+                if (p.records != nullptr) p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
+                const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(work_tile(w, p).n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -416,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = smem_desc_sw128(sB + stage * SB);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit<CG>(empty0 + 8 * stage, 0x3);
                     last_stage = stage;
                     last_phase = phase;
@@ -452,35 +473,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             w = __shfl_sync(0xffffffffu, w, 0);
             if (!ok || w < 0) break;
-            int tm, tn;
-            tile_of(w, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const WorkTile t = work_tile(w, p);
             if (lane == 0) ok = ctl.wait(acc_full0 + 8 * acc, acc_phase, WHERE_ACC_FULL) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            TileRecord *rec = (p.records != nullptr && e == 0 && lane == 0)
-                                  ? p.records + (static_cast<long long>(tm) * p.tiles_n + tn)
-                                  : nullptr;
+            TileRecord *rec = (p.records != nullptr && e == 0 && lane == 0) ? p.records + w : nullptr;
             if (rec != nullptr) {
                 atomicAdd(&rec->visits, 1u);
                 if (leader) {
-                    rec->work = static_cast<uint32_t>(w);
+                    rec->tile = static_cast<uint32_t>(t.tm * p.tiles_n + t.tn);
+                    rec->n_off = static_cast<uint32_t>(t.n_off);
+                    rec->n_len = static_cast<uint32_t>(t.n_len);
                     rec->owner = static_cast<uint32_t>(cluster_id);
                     rec->iter = static_cast<uint32_t>(i);
                     rec->smid = smid();
                     rec->t_acc_full = static_cast<uint32_t>(globaltimer_ns());
                 }
             }
-            const int row0 = tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta
+            const int row0 = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta
                              + static_cast<int>(q) * kEpiRowsPerWarp;
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * kTileN);
+            const int chunks = t.n_len / kEpiChunkCols;
 #pragma unroll 1
-            for (int c = 0; c < kTileN / kEpiChunkCols; ++c) {
+            for (int c = 0; c < chunks; ++c) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
                 tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols + 32, v1);
                 tmem_wait_ld();
-                if (c == kTileN / kEpiChunkCols - 1) {
+                if (c == chunks - 1) {
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
@@ -509,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int col = tn * kTileN + c * kEpiChunkCols;
+                const int col = t.tn * kTileN + t.n_off + c * kEpiChunkCols;
                 if (lane == 0) {
                     if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
                     bulk_commit();

@@ -13,7 +13,8 @@ struct KernelOps {
     cudaError_t (*set_smem)(int smem);
     // Resident clusters the device can hold at once for this kernel.
     cudaError_t (*max_active_clusters)(int smem, int *out);
-    cudaError_t (*launch)(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+    // b[0..2]: B maps with boxes of 256/CG, 128/CG and 64/CG rows
+    cudaError_t (*launch)(const CUtensorMap &a, const CUtensorMap *const b[3], const CUtensorMap &c,
                           const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream);
 };
 

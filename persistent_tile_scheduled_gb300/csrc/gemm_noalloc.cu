@@ -5,7 +5,7 @@
 // latency-critical loops that cannot accept the implicit synchronisation
 // cudaMalloc / cudaFree may perform.  gemm_create allocates a status block, so
 // those callers cannot use the handle API.  This entry point keeps the kernel's
-// scratch -- the device status block and one tile record per output tile (the
+// scratch -- the device status block and one record per work item (the
 // coverage counters) -- in a file-scope __device__ array instead.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -23,12 +23,12 @@ namespace {
 
 constexpr size_t kStatusBytes = 256;   // 4 status words, padded to the array's alignment
 constexpr size_t kScratchBytes =
-    kStatusBytes + static_cast<size_t>(GEMM_NOALLOC_MAX_TILES) * sizeof(pts::TileRecord);
+    kStatusBytes + static_cast<size_t>(GEMM_NOALLOC_MAX_WORK_ITEMS) * sizeof(pts::TileRecord);
 
 }  // namespace
 
-// Scratch of every call: [0, 256) status block, then one record per tile.
-// Every GPU that loads this library holds it (kScratchBytes = 512.25 KiB)
+// Scratch of every call: [0, 256) status block, then one record per work item.
+// Every GPU that loads this library holds it (kScratchBytes = 768.25 KiB)
 // until the process exits.  Calls share it; calls that overlap on the GPU race.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -153,26 +153,32 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     const int64_t tiles_m = (M + tile_m - 1) / tile_m;
     const int64_t tiles_n = (N + pts::kTileN - 1) / pts::kTileN;
     const int64_t tiles = tiles_m * tiles_n;
-    if (tiles > GEMM_NOALLOC_MAX_TILES) return GEMM_ERR_INVALID_ARG;   // scratch holds one record per tile
-
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(cudaErrorInvalidDevice);
     const DeviceSetup *s = setup_device(dev);
     if (s->error != GEMM_OK) return s->error;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int ci = cta_group - 1;
+    const int64_t resident = s->clusters[dtype][ci];
+    const int split = pts::choose_split(tiles, resident);
+    const int64_t full_work = split == 1 ? tiles : tiles - tiles % resident;
+    const int64_t work = full_work + split * (tiles - full_work);
+    if (work > GEMM_NOALLOC_MAX_WORK_ITEMS) return GEMM_ERR_INVALID_ARG;   // one scratch record per item
 
-    // status words and the records of this problem's tiles must start at zero
-    const size_t used = kStatusBytes + static_cast<size_t>(tiles) * sizeof(pts::TileRecord);
+    // status words and the records of this problem's work items must start at zero
+    const size_t used = kStatusBytes + static_cast<size_t>(work) * sizeof(pts::TileRecord);
     if (cudaMemsetAsync(s->scratch, 0, used, st) != cudaSuccess) return fail(cudaErrorInvalidValue);
 
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
-    CUtensorMap ma, mb, mc;
+    CUtensorMap ma, mb, mb_slice, mc;
+    const uint32_t brows = uint32_t(pts::kTileN / cta_group);
     if (!encode_2d(s, &ma, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems)
-        || !encode_2d(s, &mb, B, uint64_t(N), uint64_t(K), dtype, pts::kTileN / cta_group, kelems)
+        || !encode_2d(s, &mb, B, uint64_t(N), uint64_t(K), dtype, brows, kelems)
+        || !encode_2d(s, &mb_slice, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(split), kelems)
         || !encode_2d(s, &mc, C, uint64_t(M), uint64_t(N), dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16,
                       pts::kEpiRowsPerWarp, pts::kEpiChunkCols))
         return GEMM_ERR_CUDA;
+    const CUtensorMap *mbs[3] = {&mb, split == 2 ? &mb_slice : &mb, split == 4 ? &mb_slice : &mb};
 
     pts::GemmParams p{};
     p.M = static_cast<int32_t>(M);
@@ -182,6 +188,9 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.num_tiles = static_cast<int32_t>(tiles);
+    p.full_work = static_cast<int32_t>(full_work);
+    p.split = split;
+    p.num_work = static_cast<int32_t>(work);
     p.group_m = 8;
     p.sched = static_cast<int32_t>(sched);
     p.stages = s->stages[ci];
@@ -192,10 +201,10 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.status = reinterpret_cast<int32_t *>(s->scratch);
     p.records = reinterpret_cast<pts::TileRecord *>(s->scratch + kStatusBytes);
 
-    int64_t clusters = tiles;
-    if (sched == GEMM_SCHED_STATIC && clusters > s->clusters[dtype][ci]) clusters = s->clusters[dtype][ci];
+    int64_t clusters = work;
+    if (sched == GEMM_SCHED_STATIC && clusters > resident) clusters = resident;
     pts::KernelOps ops = cta_group == 2 ? pts::kernel_ops_cg2(dtype) : pts::kernel_ops_cg1(dtype);
-    cudaError_t e = ops.launch(ma, mb, mc, p, static_cast<int>(clusters * cta_group), s->smem[ci], st);
+    cudaError_t e = ops.launch(ma, mbs, mc, p, static_cast<int>(clusters * cta_group), s->smem[ci], st);
     if (e != cudaSuccess) return fail(e);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
     if (device_status == nullptr) return GEMM_OK;
@@ -211,8 +220,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
         return words[0] == pts::DEV_ERR_TIMEOUT ? GEMM_ERR_TIMEOUT : GEMM_ERR_CUDA;
     }
     pts::TileRecord chunk[128];
-    for (int64_t t0 = 0; t0 < tiles; t0 += 128) {
-        const int64_t n = tiles - t0 < 128 ? tiles - t0 : 128;
+    for (int64_t t0 = 0; t0 < work; t0 += 128) {
+        const int64_t n = work - t0 < 128 ? work - t0 : 128;
         if (cudaMemcpy(chunk, s->scratch + kStatusBytes + size_t(t0) * sizeof(pts::TileRecord),
                        size_t(n) * sizeof(pts::TileRecord), cudaMemcpyDeviceToHost) != cudaSuccess)
             return fail(cudaErrorUnknown);

@@ -27,11 +27,12 @@ enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
 enum : int32_t { DEV_ERR_TIMEOUT = 1 };
 enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u, DBG_FAULT_SKIP_TMA = 0x4u };
 
-// Per-tile debug record.  Times are the low 32 bits of %globaltimer (ns):
-// the MMA thread starting the tile, the epilogue seeing its accumulator
-// complete, the epilogue having issued the tile's last store.
+// Debug record of one work item (a tile, or a column slice of a tile of the
+// last partial wave).  Times are the low 32 bits of %globaltimer (ns): the
+// MMA thread starting the item, the epilogue seeing its accumulator complete,
+// the epilogue having issued the item's last store.
 struct TileRecord {
-    uint32_t visits, work, owner, iter, smid, t_mma_start, t_acc_full, t_stored;
+    uint32_t visits, tile, n_off, n_len, owner, iter, smid, t_mma_start, t_acc_full, t_stored, pad[2];
 };
 
 struct GemmParams {
@@ -39,6 +40,9 @@ struct GemmParams {
     int32_t num_kb;             // k-blocks per tile
     int32_t tiles_m, tiles_n;   // output tiles (per cluster) along M and N
     int32_t num_tiles;
+    int32_t full_work;          // work ids below this are whole tiles
+    int32_t split;              // each later tile is cut into `split` column slices (1, 2, 4)
+    int32_t num_work;           // full_work + split * (num_tiles - full_work)
     int32_t group_m;            // GROUP_SIZE_M
     int32_t sched;
     int32_t stages;
@@ -47,8 +51,20 @@ struct GemmParams {
     int32_t fault_arg;
     uint64_t timeout_ns;
     int32_t *status;            // 4 ints
-    TileRecord *records;        // num_tiles entries, or null
+    TileRecord *records;        // num_work entries, or null
 };
+
+// Column slices per tile for the last partial wave of `tiles` tiles on
+// `resident` clusters: quarters when the whole problem fits in a quarter wave,
+// halves when the leftover tiles fit in half a wave, otherwise none.
+inline int choose_split(int64_t tiles, int64_t resident)
+{
+    const int64_t r = tiles % resident;
+    if (r == 0) return 1;
+    if (tiles < resident && 4 * r <= resident) return 4;
+    if (2 * r <= resident) return 2;
+    return 1;
+}
 
 __host__ __device__ constexpr int stage_bytes_a() { return kRowsPerCta * kKBlockBytes; }
 __host__ __device__ constexpr int stage_bytes_b(int cg) { return (kTileN / cg) * kKBlockBytes; }

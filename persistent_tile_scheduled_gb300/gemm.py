@@ -23,26 +23,28 @@ GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
             "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc")
-GEMM_NOALLOC_MAX_TILES = 16384
+GEMM_NOALLOC_MAX_WORK_ITEMS = 16384
 
 
 class gemm_opts_t(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int), ("group_size_m", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("debug_flags", ctypes.c_uint), ("fault_arg", ctypes.c_int),
-                ("timeout_ns", ctypes.c_ulonglong)]
+                ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int)]
 
 
 class gemm_tile_record_t(ctypes.Structure):
-    _fields_ = [("visits", ctypes.c_uint32), ("work", ctypes.c_uint32), ("owner", ctypes.c_uint32),
-                ("iter", ctypes.c_uint32), ("smid", ctypes.c_uint32), ("t_mma_start", ctypes.c_uint32),
-                ("t_acc_full", ctypes.c_uint32), ("t_stored", ctypes.c_uint32)]
+    _fields_ = [("visits", ctypes.c_uint32), ("tile", ctypes.c_uint32), ("n_off", ctypes.c_uint32),
+                ("n_len", ctypes.c_uint32), ("owner", ctypes.c_uint32), ("iter", ctypes.c_uint32),
+                ("smid", ctypes.c_uint32), ("t_mma_start", ctypes.c_uint32), ("t_acc_full", ctypes.c_uint32),
+                ("t_stored", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("cta_group", ctypes.c_int), ("stages", ctypes.c_int), ("tiles_m", ctypes.c_int64),
                 ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64),
-                ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int)]
+                ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
+                ("split", ctypes.c_int), ("full_work", ctypes.c_int64), ("work_items", ctypes.c_int64)]
 
 
 class GemmError(RuntimeError):
@@ -118,8 +120,8 @@ def gemm_status_string(status: int) -> str:
 
 
 def make_opts(cta_group=1, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
-              timeout_ns=0) -> gemm_opts_t:
-    return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns)
+              timeout_ns=0, split=0) -> gemm_opts_t:
+    return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split)
 
 
 def gemm_create(device: int = 0, opts: Optional[gemm_opts_t] = None) -> int:
@@ -152,11 +154,11 @@ def gemm_check(h, stream=None):
     return st, dev.value
 
 
-def gemm_read_debug(h, n_tiles: int, stream=None):
+def gemm_read_debug(h, n_work: int, stream=None):
     """Returns (status, records, raw device status word); never raises."""
-    recs = (gemm_tile_record_t * max(int(n_tiles), 1))()
+    recs = (gemm_tile_record_t * max(int(n_work), 1))()
     dev = ctypes.c_int(0)
-    st = load().gemm_read_debug(h, _stream(stream), recs, int(n_tiles), ctypes.byref(dev))
+    st = load().gemm_read_debug(h, _stream(stream), recs, int(n_work), ctypes.byref(dev))
     return st, recs, dev.value
 
 

@@ -62,24 +62,34 @@ def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, see
 
 
 def check_records(records, info, sched: int, group_m: int = 8):
-    """Tile records against what the scheduler must do (bit-exact)."""
+    """Per-work-item records against what the schedulers must do (bit-exact)."""
     T, Tm, Tn, cg = int(info.tiles), int(info.tiles_m), int(info.tiles_n), int(info.cta_group)
+    W, F, split = int(info.work_items), int(info.full_work), int(info.split)
     G = int(info.grid_ctas) // cg
-    rec = [(r.visits, r.work, r.owner, r.iter) for r in records[:T]]
-    assert all(v == cg for v, _, _, _ in rec), "a tile was not stored exactly once by its CTA pair"
-    # the work id recorded for tile (tm, tn) must map back to it
-    for t, (_, w, _, _) in enumerate(rec):
-        assert osched.swizzle(w, Tm, Tn, group_m) == (t // Tn, t % Tn)
-    by_work = {w: (owner, it) for _, w, owner, it in rec}
-    assert sorted(by_work) == list(range(T))
+    items = osched.work_items(T, F, split)
+    assert len(items) == W
+    cover = {}
+    for w, t_order, n_off, n_len in items:
+        r = records[w]
+        assert r.visits == cg, f"work item {w} stored {r.visits} times"
+        tm, tn = osched.swizzle(t_order, Tm, Tn, group_m)
+        assert (r.tile, r.n_off, r.n_len) == (tm * Tn + tn, n_off, n_len), w
+        cover.setdefault(r.tile, []).append((r.n_off, r.n_len))
+    # the items partition every tile's 256 columns exactly once
+    assert sorted(cover) == list(range(T))
+    for t, parts in cover.items():
+        parts.sort()
+        assert parts[0][0] == 0 and sum(n for _, n in parts) == 256
+        assert all(a + n == b for (a, n), (b, _) in zip(parts, parts[1:])), t
+    by_work = {w: (records[w].owner, records[w].iter) for w in range(W)}
     if sched == pts.GEMM_SCHED_STATIC:
-        want = {w: (c, it) for w, c, it in osched.static_assignment(T, G)}
+        want = {w: (c, it) for w, c, it in osched.static_assignment(W, G)}
         assert by_work == want
     elif sched == pts.GEMM_SCHED_NONPERSISTENT:
-        want = {w: (c, it) for w, c, it in osched.nonpersistent_assignment(T)}
+        want = {w: (c, it) for w, c, it in osched.nonpersistent_assignment(W)}
         assert by_work == want
     else:
-        # CLC: a cluster's first tile is its own id; its later tiles were
+        # CLC: a cluster's first item is its own id; its later items were
         # cancelled clusters, each run exactly once; iterations are 0..n-1
         per_owner = {}
         for w, (owner, it) in by_work.items():

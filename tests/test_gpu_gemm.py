@@ -34,7 +34,7 @@ def _run_checked(h, x, sched, full=True):
     p = x.problem
     C = run_device(h, x, sched)
     info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
-    st, recs, dev = pts.gemm_read_debug(h, int(info.tiles))
+    st, recs, dev = pts.gemm_read_debug(h, int(info.work_items))
     assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
     check_records(recs, info, sched)
     err = compare_full(x, C) if full else compare_sampled(x, C, info.tile_m, info.tile_n)
@@ -125,6 +125,36 @@ def test_run_host_matches_device_path(handle):
     assert torch.equal(Cd.cpu().view(torch.int16), Ch.view(torch.int16))
 
 
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_forced_column_slices(cg, split, sched):
+    """Every tile cut into 2 or 4 column slices (MMA N = 128 or 64), ragged shapes."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, split=split, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 96, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("slices", M, N, K, dt, dist, M + N + K + split))
+            _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
+def test_automatic_last_wave_slicing():
+    """The launch plan slices the leftover tiles when they fit in half a wave."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=1))
+    try:
+        info = pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        G = int(info.max_active_clusters)
+        r = 512 % G
+        if r and 2 * r <= G:
+            assert info.split == 2 and info.full_work == 512 - r and info.work_items == 512 + r
+        info = pts.gemm_query(h, 512, 512, 512, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        assert info.tiles == 8 and info.split == 4 and info.full_work == 0 and info.work_items == 32
+    finally:
+        pts.gemm_destroy(h)
+
+
 # ---------------------------------------------------------------- full sizes
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
@@ -183,7 +213,7 @@ def test_two_gemms_on_two_streams():
         for h, s, x, C in zip(hs, streams, xs, Cs):
             p = x.problem
             info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, pts.GEMM_SCHED_CLC)
-            st, recs, dev = pts.gemm_read_debug(h, int(info.tiles), s)
+            st, recs, dev = pts.gemm_read_debug(h, int(info.work_items), s)
             assert st == 0
             check_records(recs, info, pts.GEMM_SCHED_CLC)
             assert compare_sampled(x, C, info.tile_m, info.tile_n) <= TOL[p.dtype]

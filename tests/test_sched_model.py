@@ -102,3 +102,21 @@ def test_clc_replay_uneven_costs_cover_exactly_once():
     T, resident = 200, 20
     ev, _, _ = sm.clc_replay(T, resident, cost=lambda w: 5.0 if w % 2 == 0 else 1.0)
     assert sm.coverage(ev, T) == [1] * T
+
+
+def test_work_items_hand_worked():
+    # 5 tiles, 4 whole, the fifth cut in two: columns 0-127 and 128-255
+    assert sm.work_items(5, 4, 2) == [(0, 0, 0, 256), (1, 1, 0, 256), (2, 2, 0, 256), (3, 3, 0, 256),
+                                      (4, 4, 0, 128), (5, 4, 128, 128)]
+    assert sm.work_items(2, 0, 4)[:4] == [(0, 0, 0, 64), (1, 0, 64, 64), (2, 0, 128, 64), (3, 0, 192, 64)]
+
+
+@pytest.mark.parametrize("T,F,s", [(512, 456, 2), (8, 0, 4), (528, 456, 2), (150, 150, 1), (800, 760, 2)])
+def test_work_items_partition_every_tile(T, F, s):
+    items = sm.work_items(T, F, s)
+    assert [w for w, _, _, _ in items] == list(range(F + s * (T - F)))
+    cols = {}
+    for _, t, off, n in items:
+        cols.setdefault(t, set()).update(range(off, off + n))
+    assert all(cols[t] == set(range(256)) for t in range(T))
+    assert sum(n for *_, n in items) == 256 * T        # no column computed twice

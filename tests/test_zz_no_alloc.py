@@ -81,7 +81,7 @@ def test_noalloc_asynchronous_call_matches():
 def test_noalloc_rejects_problems_beyond_its_scratch():
     """More output tiles than the static scratch holds: rejected before any launch."""
     M, N, K = 128 * 129, 256 * 128, 8          # 16 512 tiles of 128 x 256 > 16 384
-    assert (M // 128) * (N // 256) > pts.gemm.GEMM_NOALLOC_MAX_TILES
+    assert (M // 128) * (N // 256) > pts.gemm.GEMM_NOALLOC_MAX_WORK_ITEMS
     A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
     B = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
     C = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
