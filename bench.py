@@ -38,6 +38,8 @@ UNIT = "TFLOP/s"
 WORKLOAD = ("fp16 GEMM M=N=4096, K=128..4096 step 128 (32 GEMMs per step), A,B ~ N(0,1)/sqrt(K), "
             "fp32 accumulate, fp16 C, row-major A, column-major B")
 SCHED_NAMES = ["nonpersistent", "static", "clc"]
+TILE_DESC = {1: "128x256x64 per CTA (tcgen05 cta_group::1)",
+             2: "128x256x64 per CTA; CTA pairs run one 256x256 tcgen05 cta_group::2 MMA and share B"}
 HEADLINE = "static"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["persistent_tile_scheduled_gb300/csrc/gemm_kernel.cuh",
@@ -181,33 +183,46 @@ def gemm_flops(M, N, K):
 
 
 def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist):
-    """Warm-up, then `steps` timed passes over the sweep; per-K event timings."""
-    for _ in range(warmup):
+    """Warm-up, then `steps` timed passes over the sweep (events only at step
+    boundaries, so consecutive GEMMs may overlap their launches), then one
+    extra pass with an event between GEMMs for the per-K breakdown."""
+    def one_pass():
         for p, (A, B, C) in zip(problems, bufs):
             pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one_pass()
     torch.cuda.synchronize()
     st, dev = pts.gemm_check(h, stream)
     if st != 0:
         raise RuntimeError(f"device status {dev:#x} after warm-up")
-    n = len(problems)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.time()
     with torch.cuda.stream(stream):
+        ev[0].record(stream)
         for s in range(steps):
-            for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
-                ev[s][i].record(stream)
-                pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
-            ev[s][n].record(stream)
+            one_pass()
+            ev[s + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(dist)
     st, dev = pts.gemm_check(h, stream)
     if st != 0:
         raise RuntimeError(f"device status {dev:#x} in the timed region")
-    total_ms = ev[0][0].elapsed_time(ev[steps - 1][n])
-    per_k = [statistics.median(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(n)]
+    total_ms = ev[0].elapsed_time(ev[steps])
+    # per-K breakdown (outside the timed region): an event around every GEMM
+    n = len(problems)
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
+            kev[i].record(stream)
+            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+        kev[n].record(stream)
+    torch.cuda.synchronize()
+    per_k = [kev[i].elapsed_time(kev[i + 1]) for i in range(n)]
     return total_ms, per_k, (t0, t1)
 
 
@@ -244,7 +259,7 @@ def run_ours(args, dist, rank, world, local):
 
     per_sched = {}
     clocks = None
-    h = pts.gemm_create(local, pts.make_opts(cta_group=1))
+    h = pts.gemm_create(local, pts.make_opts(cta_group=args.cta_group))
     try:
         for si, name in enumerate(SCHED_NAMES):
             if name not in args.scheds:
@@ -261,8 +276,8 @@ def run_ours(args, dist, rank, world, local):
             per_sched[name] = {
                 "value": world * flops_step / (ms_step * 1e-3) / 1e12,
                 "ms_per_step": ms_step,
-                "per_k_tflops": [round(gemm_flops(p.M, p.N, p.K) / (t * 1e-3) / 1e12, 1)
-                                 for p, t in zip(problems, per_k)],
+                "per_k_tflops_isolated": [round(gemm_flops(p.M, p.N, p.K) / (t * 1e-3) / 1e12, 1)
+                                          for p, t in zip(problems, per_k)],
                 "per_k_ms": per_k,
             }
             log(f"[rank {rank}] {name}: {per_sched[name]['value']:.1f} TFLOP/s, {ms_step:.3f} ms/step")
@@ -309,7 +324,7 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
                 "frac": round(achieved / tensor_peak, 4) if tensor_peak else None,
                 "traffic": traffic if isinstance(traffic, (int, float)) else None,
                 "peak_source": f"{peaks_src} bf16 dense (fp16 runs at the same tensor rate), burst",
-                "achieved_def": "sum of 2MNK over the 32 launches / sum of their CUDA-event durations"}
+                "achieved_def": "sum of 2MNK over the 32 launches of a step / the step's CUDA-event time"}
     if traffic is not None and launch:
         roofline["traffic_launch"] = launch
     per_k_roof = []
@@ -327,8 +342,8 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded N(0,1)/sqrt(K), rounded to fp16)",
-        "config": {"workload": WORKLOAD, "tile": "128x256x64", "group_size_m": 8, "cta_group": 1,
-                   "sched": HEADLINE, "stages": 4,
+        "config": {"workload": WORKLOAD, "tile": TILE_DESC[args.cta_group], "group_size_m": 8,
+                   "cta_group": args.cta_group, "sched": HEADLINE,
                    "l2": "no flush: one step's 32 distinct A,B,C sets (2.1 GB) exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_tensor_peak": round(achieved / tensor_peak, 4) if tensor_peak else None,
@@ -427,6 +442,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
+    ap.add_argument("--cta-group", type=int, default=2, choices=[1, 2])
     args = ap.parse_args()
     if args.warmup < 3:
         log("warm-up raised to 3 steps")

@@ -12,6 +12,10 @@ struct Inst {
         return cudaFuncSetAttribute(gemm_kernel<KIND, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     }
 
+    // Launch attributes: a (2,1,1) cluster for CTA pairs, and programmatic
+    // stream serialization so that this grid may start while the previous
+    // grid in the stream finishes (the kernel waits for it before touching
+    // global memory).
     static void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid_ctas, int smem,
                             cudaStream_t stream)
     {
@@ -20,21 +24,25 @@ struct Inst {
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = static_cast<size_t>(smem);
         cfg.stream = stream;
-        cfg.numAttrs = 0;
         cfg.attrs = attr;
+        int n = 0;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
         if (CG == 2) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.numAttrs = 1;
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = 2;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
         }
+        cfg.numAttrs = static_cast<unsigned>(n);
     }
 
     static cudaError_t max_active_clusters(int smem, int *out)
     {
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         fill_config(cfg, attr, 2 * CG, smem, nullptr);
         if (CG == 1) {
             int per_sm = 0, dev = 0, sms = 0;
@@ -53,7 +61,7 @@ struct Inst {
                               const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream)
     {
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         fill_config(cfg, attr, grid_ctas, smem, stream);
         return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, a, *b[0], *b[1], *b[2], c, p);
     }

@@ -263,6 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CG == 2) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    // Back-to-back launches: the set-up above may overlap the end of the
+    // previous grid in the stream; nothing touches global memory before it
+    // has completed (A and B may be its outputs, C its inputs).
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- work-id broadcast ring -------------------------------------------
     // Slot r holds the id of work item i (i % kRing == r), or -1 = no more.

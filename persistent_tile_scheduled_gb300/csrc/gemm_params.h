@@ -54,15 +54,17 @@ struct GemmParams {
     TileRecord *records;        // num_work entries, or null
 };
 
-// Column slices per tile for the last partial wave of `tiles` tiles on
-// `resident` clusters: quarters when the whole problem fits in a quarter wave,
-// halves when the leftover tiles fit in half a wave, otherwise none.
+// Column slices per tile for a problem of `tiles` tiles on `resident`
+// clusters.  Only a problem smaller than one wave is sliced (quarters when it
+// fits in a quarter wave, halves when it fits in half): there slicing puts
+// idle SMs to work.  Past one wave the slices' smaller stages leave the
+// latency-bound load pipeline with fewer bytes in flight, and a slice takes
+// nearly as long as a whole tile, so later waves are not sliced.
 inline int choose_split(int64_t tiles, int64_t resident)
 {
-    const int64_t r = tiles % resident;
-    if (r == 0) return 1;
-    if (tiles < resident && 4 * r <= resident) return 4;
-    if (2 * r <= resident) return 2;
+    if (tiles >= resident) return 1;
+    if (4 * tiles <= resident) return 4;
+    if (2 * tiles <= resident) return 2;
     return 1;
 }
 

@@ -243,6 +243,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Let the next grid in the stream (launched with programmatic stream
+// serialization) be scheduled once every CTA of this grid has called this or
+// exited.  It does not release any data: the next grid still waits below.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Block until the grids this one depends on have completed and their memory
+// is visible; returns at once when there is no such dependency.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------- Cluster Launch Control
 
 // Ask the hardware to cancel a cluster of this grid that has not launched

@@ -140,15 +140,12 @@ def test_forced_column_slices(cg, split, sched):
         pts.gemm_destroy(h)
 
 
-def test_automatic_last_wave_slicing():
-    """The launch plan slices the leftover tiles when they fit in half a wave."""
+def test_automatic_slicing_of_sub_wave_problems():
+    """Problems smaller than a wave are sliced so that more SMs take part."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=1))
     try:
         info = pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        G = int(info.max_active_clusters)
-        r = 512 % G
-        if r and 2 * r <= G:
-            assert info.split == 2 and info.full_work == 512 - r and info.work_items == 512 + r
+        assert info.split == 1 and info.work_items == info.tiles == 512
         info = pts.gemm_query(h, 512, 512, 512, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
         assert info.tiles == 8 and info.split == 4 and info.full_work == 0 and info.work_items == 32
     finally:
