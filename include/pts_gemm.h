@@ -30,7 +30,10 @@
  *   - Errors are reported only through the returned status; nothing aborts
  *     the process and no call falls back to the CPU.
  *   - Calls are asynchronous on the given stream unless stated otherwise.
- *   - A handle is not thread-safe; use one handle per host thread.
+ *   - A handle is not thread-safe; use one handle per host thread.  GEMMs
+ *     that run at the same time on different streams need one handle each:
+ *     a handle's workspace (K-split partials, debug records) serves one
+ *     launch at a time.
  */
 #ifndef PTS_GEMM_H
 #define PTS_GEMM_H
@@ -80,17 +83,25 @@ typedef struct gemm_opts {
     unsigned debug_flags;           /* GEMM_DEBUG_* */
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
-    int split;                      /* column slices per tile of the last partial wave: 0 = auto,
-                                       1 = never; 2 or 4 = slice EVERY tile (testing) */
+    int split;                      /* 0 = automatic; 1 = never cut tiles; 2..4 = cut EVERY
+                                       tile into that many parts (testing) */
+    int split_k;                    /* with split >= 2: 0 = column slices (2 or 4),
+                                       1 = K ranges with a fixup (2, 3 or 4) */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are visited in grouped order; a work item is one
- * tile, except that the tiles of the last partial wave (the tiles left over
- * when the tile count is not a multiple of the resident clusters) may be cut
- * into `split` column slices of 256/split columns each, one work item per
- * slice, so that the last wave ends early.  Work ids below full_work are
- * whole tiles; work id full_work + split*j + h is slice h of the
- * (full_work + j)-th tile in grouped order.
+ * tile, except that some tiles are cut into `split` parts, one work item per
+ * part: work ids below full_work are whole tiles, work id
+ * full_work + split*j + h is part h of the (full_work + j)-th tile.
+ *   - A problem smaller than one wave of resident clusters is cut into
+ *     column slices of 256/split columns (split 2 or 4), so more SMs work.
+ *   - Otherwise the tiles of the last partial wave may be cut into K ranges
+ *     (split 2..4, k-block range h*kb/split .. (h+1)*kb/split): every part
+ *     accumulates its range; each part but the last to finish writes its fp32
+ *     partial to a workspace the handle owns, and the last adds them and
+ *     stores C.  The last wave then ends after about 1/split of a tile.
+ * Cutting tiles changes which CTA computes what, never the result beyond the
+ * fp32 summation order.
  *
  * Per-work-item record written when GEMM_DEBUG_RECORDS is set (work-id order). */
 typedef struct gemm_tile_record {
@@ -105,7 +116,7 @@ typedef struct gemm_tile_record {
      * item, the epilogue saw its accumulator complete, the epilogue issued the
      * item's last store (leader CTA) */
     uint32_t t_mma_start, t_acc_full, t_stored;
-    uint32_t reserved[2];
+    uint32_t kb_begin, kb_end;  /* k-block range of the item */
 } gemm_tile_record_t;
 
 /* Launch shape chosen for a problem. */
@@ -118,7 +129,8 @@ typedef struct gemm_launch_info {
     int max_active_clusters;        /* resident clusters the device holds for this kernel */
     int smem_bytes;                 /* dynamic shared memory per CTA */
     int threads;                    /* threads per CTA */
-    int split;                      /* column slices per tile of the last partial wave */
+    int split;                      /* parts per tile past full_work (1 = none) */
+    int split_k;                    /* parts are K ranges (1) or column slices (0) */
     int64_t full_work;              /* work ids below this are whole tiles */
     int64_t work_items;             /* work items in total */
 } gemm_launch_info_t;

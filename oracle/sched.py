@@ -50,23 +50,33 @@ def swizzle(w: int, Tm: int, Tn: int, group_m: int) -> Tuple[int, int]:
     return first_m + r % rows_here, r // rows_here
 
 
-def work_items(T: int, full_work: int, split: int, tile_n: int = 256) -> List[Tuple[int, int, int, int]]:
-    """(work id, grouped-order tile index, first column, columns) of every work item.
+def work_items(T: int, full_work: int, split: int, tile_n: int = 256, split_k: bool = False,
+               num_kb: int = 1) -> List[Tuple[int, int, int, int, int, int]]:
+    """(work id, grouped-order tile index, first column, columns, first k-block,
+    end k-block) of every work item.
 
-    Work ids below ``full_work`` are whole tiles.  The remaining tiles (the
-    last partial wave) are each cut into ``split`` column slices: work id
-    ``full_work + split*j + h`` is slice h of tile ``full_work + j``.  Cutting
-    the last wave's tiles does not change what is computed, only how the
-    output is partitioned among CTAs ("Neither mode creates additional
-    independent work at the tail of a grid": slicing is a separate device).
+    Work ids below ``full_work`` are whole tiles.  Each remaining tile is cut
+    into ``split`` parts: work id ``full_work + split*j + h`` is part h of
+    tile ``full_work + j``.  Parts are column slices of ``tile_n / split``
+    columns, or (``split_k``) k-block ranges ``[h*num_kb//split,
+    (h+1)*num_kb//split)`` whose partial sums add up to the tile.  Cutting
+    tiles changes how the output is partitioned among CTAs, never what is
+    computed ("Neither mode creates additional independent work at the tail
+    of a grid": cutting is a separate device for the last wave).
     """
-    if not (0 <= full_work <= T and split in (1, 2, 4)):
+    if not (0 <= full_work <= T and 1 <= split <= 4):
         raise ValueError((T, full_work, split))
-    out = [(w, w, 0, tile_n) for w in range(full_work)]
-    step = tile_n // split
+    if not split_k and split not in (1, 2, 4):
+        raise ValueError(split)
+    out = [(w, w, 0, tile_n, 0, num_kb) for w in range(full_work)]
     for j in range(T - full_work):
         for h in range(split):
-            out.append((full_work + split * j + h, full_work + j, h * step, step))
+            w = full_work + split * j + h
+            if split_k:
+                out.append((w, full_work + j, 0, tile_n, h * num_kb // split, (h + 1) * num_kb // split))
+            else:
+                step = tile_n // split
+                out.append((w, full_work + j, h * step, step, 0, num_kb))
     return out
 
 

@@ -42,6 +42,11 @@ struct gemm_ctx {
     int last_cta_group = 1;
     void *d_host_bufs = nullptr;              // gemm_run_host staging (A | B | C)
     size_t host_bufs_cap = 0;
+    float *d_ws_partial = nullptr;            // K-split fixup workspace
+    size_t ws_partial_cap = 0;                // bytes
+    uint32_t *d_ws_sync = nullptr;            // K-split claim counters / ready flags
+    size_t ws_sync_cap = 0;                   // bytes
+    uint32_t epoch = 0;                       // launch number for the fixup counters (1 .. 2^29 - 1)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool smem_set[3][2] = {};
     int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
@@ -95,7 +100,9 @@ pts::KernelOps ops_for(int kind, int cg) { return cg == 2 ? pts::kernel_ops_cg2(
 struct Plan {
     int cg, stages, smem;
     int64_t tiles_m, tiles_n, tiles;
-    int split;               // column slices per tile of the last partial wave
+    int split;               // parts per tile past full_work
+    int split_k;             // parts are K ranges (1) or column slices (0)
+    int64_t num_kb;          // k-blocks per whole tile
     int64_t full_work;       // work ids below this are whole tiles
     int64_t work;            // work items in total
     int64_t grid_ctas;
@@ -114,8 +121,11 @@ gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, g
     return GEMM_OK;
 }
 
-gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, gemm_dtype_t dtype, gemm_sched_t sched, Plan &pl)
+gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_sched_t sched,
+                        Plan &pl)
 {
+    const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
+    pl.num_kb = (K + kelems - 1) / kelems;
     pl.cg = h->opts.cta_group;
     int stages = h->opts.stages;
     if (stages == 0) {   // the deepest ring that fits
@@ -148,9 +158,22 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, gemm_dtype_t dtype, g
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
     int64_t resident = pl.max_active_clusters;
     if (h->opts.max_clusters > 0 && h->opts.max_clusters < resident) resident = h->opts.max_clusters;
-    pl.split = h->opts.split > 0 ? h->opts.split : pts::choose_split(pl.tiles, resident);
-    pl.full_work = pl.split == 1 ? pl.tiles : pl.tiles - pl.tiles % resident;
-    if (h->opts.split > 1) pl.full_work = 0;   // forced split: every tile is sliced
+    if (h->opts.split > 0) {   // forced (testing): every tile is cut the same way
+        pl.split = h->opts.split;
+        pl.split_k = h->opts.split_k;
+        if (pl.split_k && pl.split > pl.num_kb) pl.split = static_cast<int>(pl.num_kb < 1 ? 1 : pl.num_kb);
+        if (pl.split == 1) pl.split_k = 0;
+        pl.full_work = pl.split == 1 ? pl.tiles : 0;
+    } else if ((pl.split = pts::choose_split(pl.tiles, resident)) > 1) {
+        pl.split_k = 0;                                   // a sub-wave problem: column slices
+        pl.full_work = 0;
+    } else if ((pl.split = pts::choose_split_k(pl.tiles, resident, pl.num_kb)) > 1) {
+        pl.split_k = 1;                                   // the last partial wave: K ranges + fixup
+        pl.full_work = pl.tiles - pl.tiles % resident;
+    } else {
+        pl.split_k = 0;
+        pl.full_work = pl.tiles;
+    }
     pl.work = pl.full_work + pl.split * (pl.tiles - pl.full_work);
     int64_t clusters = pl.work;
     if (sched == GEMM_SCHED_STATIC) clusters = pl.work < resident ? pl.work : resident;
@@ -178,8 +201,29 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
 
     Plan pl;
-    gemm_status_t st = make_plan(h, M, N, dtype, sched, pl);
+    gemm_status_t st = make_plan(h, M, N, K, dtype, sched, pl);
     if (st != GEMM_OK) return st;
+    if (pl.split_k) {   // fixup workspace: partials of all parts but the last, and the sync words
+        const size_t split_tiles = size_t(pl.tiles - pl.full_work);
+        const size_t need_p = split_tiles * size_t(pl.split - 1) * pl.cg * pts::kPartialFloats * sizeof(float);
+        const size_t need_s = split_tiles * pl.cg * pts::kEpiWarps * 4 * sizeof(uint32_t);
+        if (h->ws_partial_cap < need_p) {
+            cudaFree(h->d_ws_partial);
+            h->d_ws_partial = nullptr;
+            h->ws_partial_cap = 0;
+            if (cudaMalloc(&h->d_ws_partial, need_p) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
+            h->ws_partial_cap = need_p;
+        }
+        if (h->ws_sync_cap < need_s) {
+            cudaFree(h->d_ws_sync);
+            h->d_ws_sync = nullptr;
+            h->ws_sync_cap = 0;
+            if (cudaMalloc(&h->d_ws_sync, need_s) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
+            if (cudaMemset(h->d_ws_sync, 0, need_s) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
+            h->ws_sync_cap = need_s;
+        }
+    }
+    h->epoch = h->epoch % 0x1FFFFFFFu + 1u;
 
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
     const CUtensorMap *ma = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems);
@@ -196,12 +240,16 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.num_kb = static_cast<int32_t>((K + kelems - 1) / kelems);
+    p.num_kb = static_cast<int32_t>(pl.num_kb);
     p.tiles_m = static_cast<int32_t>(pl.tiles_m);
     p.tiles_n = static_cast<int32_t>(pl.tiles_n);
     p.num_tiles = static_cast<int32_t>(pl.tiles);
     p.full_work = static_cast<int32_t>(pl.full_work);
     p.split = pl.split;
+    p.split_k = pl.split_k;
+    p.epoch = h->epoch;
+    p.ws_partial = pl.split_k ? h->d_ws_partial : nullptr;
+    p.ws_sync = pl.split_k ? h->d_ws_sync : nullptr;
     p.num_work = static_cast<int32_t>(pl.work);
     p.group_m = h->opts.group_size_m;
     p.sched = static_cast<int32_t>(sched);
@@ -275,7 +323,8 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (o.split != 0 && o.split != 1 && o.split != 2 && o.split != 4) return GEMM_ERR_INVALID_ARG;
+    if (o.split < 0 || o.split > 4 || (!o.split_k && o.split == 3) || (o.split_k != 0 && o.split_k != 1))
+        return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
         return GEMM_ERR_INVALID_ARG;
 
@@ -368,7 +417,7 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     if (st != GEMM_OK) return st;
     if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
     Plan pl;
-    st = make_plan(h, M, N, dtype, sched, pl);
+    st = make_plan(h, M, N, K, dtype, sched, pl);
     if (st != GEMM_OK) return st;
     std::memset(info, 0, sizeof(*info));
     info->tile_m = pts::kRowsPerCta * pl.cg;
@@ -380,6 +429,7 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     info->tiles_n = pl.tiles_n;
     info->tiles = pl.tiles;
     info->split = pl.split;
+    info->split_k = pl.split_k;
     info->full_work = pl.full_work;
     info->work_items = pl.work;
     info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;
@@ -419,6 +469,8 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
     cudaFree(h->d_status);
     cudaFree(h->d_records);
     cudaFree(h->d_host_bufs);
+    cudaFree(h->d_ws_partial);
+    cudaFree(h->d_ws_sync);
     delete h;
     return GEMM_OK;
 }

@@ -44,6 +44,7 @@ enum : int32_t {
     WHERE_RING_FULL = 6,    // a role waiting for the next tile id
     WHERE_CLC = 7,          // scheduler waiting for a CLC response
     WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
+    WHERE_FIXUP = 9,        // the last part of a K-split tile waiting for the other parts
 };
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
@@ -98,28 +99,66 @@ __device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int gro
     tn = r / rows;
 }
 
-// A work item: tile (tm, tn) and the column slice [n_off, n_off + n_len) of
-// it.  Work ids below full_work are whole tiles in grouped order; the tiles of
-// the last partial wave are cut into `split` slices each, so that wave ends
-// after 1/split of a tile's time instead of a whole one.
+// A work item: tile (tm, tn), its column slice [n_off, n_off + n_len) and its
+// k-block range [kb_begin, kb_end).  Work ids below full_work are whole tiles
+// in grouped order.  Each later tile (the last partial wave) is cut into
+// `split` parts: column slices (split_k == 0), or K ranges (split_k == 1)
+// whose fp32 partials are summed by the part that finishes last; `ks` is then
+// the index of the split tile among them (else -1).
 struct WorkTile {
-    int tm, tn, n_off, n_len;
+    int tm, tn, n_off, n_len, kb_begin, kb_end, ks;
 };
 
 __device__ __forceinline__ WorkTile work_tile(int w, const GemmParams &p)
 {
     WorkTile t;
-    int tile = w, sub = 0;
+    int tile = w;
+    t.n_off = 0;
     t.n_len = kTileN;
+    t.kb_begin = 0;
+    t.kb_end = p.num_kb;
+    t.ks = -1;
     if (w >= p.full_work) {
         const int q = w - p.full_work;
-        tile = p.full_work + q / p.split;
-        sub = q - (q / p.split) * p.split;
-        t.n_len = kTileN / p.split;
+        const int j = q / p.split;
+        const int h = q - j * p.split;
+        tile = p.full_work + j;
+        if (p.split_k) {
+            t.kb_begin = (h * p.num_kb) / p.split;
+            t.kb_end = ((h + 1) * p.num_kb) / p.split;
+            t.ks = j;
+        } else {
+            t.n_len = kTileN / p.split;
+            t.n_off = h * t.n_len;
+        }
     }
     tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
-    t.n_off = sub * t.n_len;
     return t;
+}
+
+// K-split fixup, per (split tile, CTA of the pair, epilogue warp): the warp's
+// 32 rows of the tile are reduced independently of the other warps, so no
+// warp ever waits for another warp of its CTA.  Sync words: [0] claim counter
+// (epoch << 3 | parts claimed), [1..3] ready flags of partial slots 0..2
+// (each holds the epoch of the launch that filled the slot).  A unit has
+// split - 1 partial slots.
+// Partial slot layout: float4 index (chunk * 16 + g) * 32 + lane, so every
+// warp-wide access is 512 contiguous bytes.
+constexpr int kPartialFloat4PerWarp = kEpiRowsPerWarp * kTileN / 4;
+
+// Claim the next part number of this launch (epoch); 0 when the counter still
+// holds an earlier launch's value.
+__device__ __forceinline__ uint32_t fixup_claim(uint32_t *cnt, uint32_t epoch)
+{
+    uint32_t old = atomicAdd(cnt, 0u);
+    for (;;) {
+        const bool fresh = (old >> 3) != epoch;
+        const uint32_t mine = fresh ? 0u : (old & 7u);
+        const uint32_t next = fresh ? ((epoch << 3) | 1u) : old + 1u;
+        const uint32_t prev = atomicCAS(cnt, old, next);
+        if (prev == old) return mine;
+        old = prev;
+    }
 }
 
 struct WaitCtl {
@@ -250,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (p.split == 2) prefetch_tmap(&tmB2);
-        if (p.split == 4) prefetch_tmap(&tmB4);
+        if (!p.split_k && p.split == 2) prefetch_tmap(&tmB2);
+        if (!p.split_k && p.split == 4) prefetch_tmap(&tmB4);
         prefetch_tmap(&tmC);
     }
     if (warp == 1) {
@@ -306,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
                 const CUtensorMap *mb = t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
                 const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                     if (!ctl.wait(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
                     const int x = kb * KELEMS;
                     const uint32_t fb = full0 + 8 * stage;
@@ -429,10 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ctl.wait(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
                 if (p.records != nullptr) p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
-                const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(work_tile(w, p).n_len));
+                const WorkTile t = work_tile(w, p);
+                const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                     if (!ctl.wait(full0 + 8 * stage, phase, WHERE_FULL)) {
                         ok = false;
                         break;
@@ -442,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = smem_desc_sw128(sB + stage * SB);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, idesc, (kb != t.kb_begin || k != 0) ? 1u : 0u);
                     umma_commit<CG>(empty0 + 8 * stage, 0x3);
                     last_stage = stage;
                     last_phase = phase;
@@ -490,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rec->tile = static_cast<uint32_t>(t.tm * p.tiles_n + t.tn);
                     rec->n_off = static_cast<uint32_t>(t.n_off);
                     rec->n_len = static_cast<uint32_t>(t.n_len);
+                    rec->kb_begin = static_cast<uint32_t>(t.kb_begin);
+                    rec->kb_end = static_cast<uint32_t>(t.kb_end);
                     rec->owner = static_cast<uint32_t>(cluster_id);
                     rec->iter = static_cast<uint32_t>(i);
                     rec->smid = smid();
@@ -500,6 +542,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                              + static_cast<int>(q) * kEpiRowsPerWarp;
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * kTileN);
             const int chunks = t.n_len / kEpiChunkCols;
+
+            // K-split tile: claim a part number for this warp's rows.  Parts
+            // other than the last claimed write their fp32 partial and raise a
+            // flag; the last claimed waits for those flags (every such part has
+            // already claimed, so it is running and never waits itself) and
+            // adds the partials before storing C.
+            int part = -1;
+            uint32_t *sync = nullptr;
+            const float4 *partials = nullptr;
+            if (t.ks >= 0) {
+                const long long unit = (static_cast<long long>(t.ks) * CG + rank) * kEpiWarps + q;
+                sync = p.ws_sync + unit * 4;
+                partials = reinterpret_cast<const float4 *>(p.ws_partial)
+                           + unit * (p.split - 1) * kPartialFloat4PerWarp;
+                uint32_t mine = 0;
+                if (lane == 0) mine = fixup_claim(sync, p.epoch);
+                part = static_cast<int>(__shfl_sync(0xffffffffu, mine, 0));
+                if (part == p.split - 1) {
+                    if (lane == 0) {
+                        for (int sl = 0; sl < p.split - 1; ++sl) {
+                            const uint64_t t0 = globaltimer_ns();
+                            while (ld_acquire_gpu(sync + 1 + sl) != p.epoch) {
+                                if (ld_shared_u32(abort_flag)) break;
+                                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                                    ctl.fail(WHERE_FIXUP);
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    for (int sl = 0; sl < p.split - 1; ++sl) (void)ld_acquire_gpu(sync + 1 + sl);
+                }
+            }
+            const bool write_partial = part >= 0 && part < p.split - 1;
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t v0[32], v1[32];
@@ -515,6 +592,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_cluster(mapa(acc_empty0 + 8 * acc, 0u));
                         else
                             mbar_arrive(acc_empty0 + 8 * acc);
+                    }
+                }
+                if (write_partial) {
+                    float4 *dst = const_cast<float4 *>(partials) + part * kPartialFloat4PerWarp
+                                  + c * 16 * 32 + lane;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        st_cg_f4(dst + g * 32, __uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
+                                 __uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3]));
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        st_cg_f4(dst + (8 + g) * 32, __uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]),
+                                 __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]));
+                    continue;
+                }
+                if (part > 0) {   // the last part of a K-split tile: add the others' partials
+                    for (int sl = 0; sl < part; ++sl) {
+                        const float4 *src = partials + sl * kPartialFloat4PerWarp + c * 16 * 32 + lane;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const float4 a = ld_cg_f4(src + g * 32);
+                            v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + a.x);
+                            v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + a.y);
+                            v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + a.z);
+                            v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + a.w);
+                            const float4 b = ld_cg_f4(src + (8 + g) * 32);
+                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + b.x);
+                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + b.y);
+                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + b.z);
+                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + b.w);
+                        }
                     }
                 }
                 uint32_t pk[32];
@@ -541,6 +649,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
                 ++nstore;
+            }
+            if (write_partial) {
+                // publish this part: every lane's stores, then the flag (release)
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(sync + 1 + part, p.epoch);
             }
             if (rec != nullptr && leader) rec->t_stored = static_cast<uint32_t>(globaltimer_ns());
             if (++acc == 2) {

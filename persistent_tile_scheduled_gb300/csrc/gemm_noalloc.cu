@@ -190,6 +190,10 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.num_tiles = static_cast<int32_t>(tiles);
     p.full_work = static_cast<int32_t>(full_work);
     p.split = split;
+    p.split_k = 0;   // no K-split fixup: its workspace would not fit a modest static array
+    p.epoch = 1;
+    p.ws_partial = nullptr;
+    p.ws_sync = nullptr;
     p.num_work = static_cast<int32_t>(work);
     p.group_m = 8;
     p.sched = static_cast<int32_t>(sched);

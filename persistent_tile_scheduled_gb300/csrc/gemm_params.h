@@ -32,7 +32,7 @@ enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u, DBG_FAULT_SKIP_TMA
 // MMA thread starting the item, the epilogue seeing its accumulator complete,
 // the epilogue having issued the item's last store.
 struct TileRecord {
-    uint32_t visits, tile, n_off, n_len, owner, iter, smid, t_mma_start, t_acc_full, t_stored, pad[2];
+    uint32_t visits, tile, n_off, n_len, owner, iter, smid, t_mma_start, t_acc_full, t_stored, kb_begin, kb_end;
 };
 
 struct GemmParams {
@@ -41,7 +41,9 @@ struct GemmParams {
     int32_t tiles_m, tiles_n;   // output tiles (per cluster) along M and N
     int32_t num_tiles;
     int32_t full_work;          // work ids below this are whole tiles
-    int32_t split;              // each later tile is cut into `split` column slices (1, 2, 4)
+    int32_t split;              // each later tile is cut into `split` parts (1..4)
+    int32_t split_k;            // 0: parts are column slices; 1: parts are K ranges, reduced in a fixup
+    uint32_t epoch;             // launch number (29 bits, never 0) tagging the fixup counters and flags
     int32_t num_work;           // full_work + split * (num_tiles - full_work)
     int32_t group_m;            // GROUP_SIZE_M
     int32_t sched;
@@ -51,8 +53,34 @@ struct GemmParams {
     int32_t fault_arg;
     uint64_t timeout_ns;
     int32_t *status;            // 4 ints
+    float *ws_partial;          // K-split partial accumulators (fixup workspace), or null
+    uint32_t *ws_sync;          // K-split claim counters and ready flags, 4 words per (tile, CTA)
     TileRecord *records;        // num_work entries, or null
 };
+
+// Floats of one K-split partial: a CTA's 128 x 256 fp32 accumulator.
+constexpr int kPartialFloats = kRowsPerCta * kTileN;
+
+// K parts per leftover tile of the last partial wave, or 1.  Splitting K cuts
+// the wave's length to 1/parts of a tile's mainloop but costs a fixup (the
+// other parts' fp32 partials written and read back, about 3 k-blocks' time
+// each); parts must fit the idle clusters of that wave.
+inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
+{
+    const int64_t r = tiles % resident;
+    if (tiles < resident || r == 0) return 1;
+    int best = 1;
+    int64_t best_gain = 4;   // in k-block times; smaller gains are not worth a fixup
+    for (int s = 2; s <= 4; ++s) {
+        if (s * r > resident || s > num_kb) break;
+        const int64_t gain = num_kb - num_kb / s - 3 * (s - 1);
+        if (gain > best_gain) {
+            best_gain = gain;
+            best = s;
+        }
+    }
+    return best;
+}
 
 // Column slices per tile for a problem of `tiles` tiles on `resident`
 // clusters.  Only a problem smaller than one wave is sliced (quarters when it

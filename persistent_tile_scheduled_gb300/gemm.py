@@ -29,14 +29,14 @@ GEMM_NOALLOC_MAX_WORK_ITEMS = 16384
 class gemm_opts_t(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int), ("group_size_m", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("debug_flags", ctypes.c_uint), ("fault_arg", ctypes.c_int),
-                ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int), ("split_k", ctypes.c_int)]
 
 
 class gemm_tile_record_t(ctypes.Structure):
     _fields_ = [("visits", ctypes.c_uint32), ("tile", ctypes.c_uint32), ("n_off", ctypes.c_uint32),
                 ("n_len", ctypes.c_uint32), ("owner", ctypes.c_uint32), ("iter", ctypes.c_uint32),
                 ("smid", ctypes.c_uint32), ("t_mma_start", ctypes.c_uint32), ("t_acc_full", ctypes.c_uint32),
-                ("t_stored", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
+                ("t_stored", ctypes.c_uint32), ("kb_begin", ctypes.c_uint32), ("kb_end", ctypes.c_uint32)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
@@ -44,7 +44,8 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("cta_group", ctypes.c_int), ("stages", ctypes.c_int), ("tiles_m", ctypes.c_int64),
                 ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64),
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
-                ("split", ctypes.c_int), ("full_work", ctypes.c_int64), ("work_items", ctypes.c_int64)]
+                ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("full_work", ctypes.c_int64),
+                ("work_items", ctypes.c_int64)]
 
 
 class GemmError(RuntimeError):
@@ -120,8 +121,9 @@ def gemm_status_string(status: int) -> str:
 
 
 def make_opts(cta_group=1, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
-              timeout_ns=0, split=0) -> gemm_opts_t:
-    return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split)
+              timeout_ns=0, split=0, split_k=0) -> gemm_opts_t:
+    return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split,
+                       split_k)
 
 
 def gemm_create(device: int = 0, opts: Optional[gemm_opts_t] = None) -> int:

@@ -61,26 +61,28 @@ def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, see
     return og.rel_err(got, ref, ref_abs, out_u(p.dtype))
 
 
-def check_records(records, info, sched: int, group_m: int = 8):
+def check_records(records, info, sched: int, K: int, group_m: int = 8):
     """Per-work-item records against what the schedulers must do (bit-exact)."""
     T, Tm, Tn, cg = int(info.tiles), int(info.tiles_m), int(info.tiles_n), int(info.cta_group)
     W, F, split = int(info.work_items), int(info.full_work), int(info.split)
     G = int(info.grid_ctas) // cg
-    items = osched.work_items(T, F, split)
+    num_kb = -(-int(K) // int(info.tile_k))
+    items = osched.work_items(T, F, split, split_k=bool(info.split_k), num_kb=num_kb)
     assert len(items) == W
     cover = {}
-    for w, t_order, n_off, n_len in items:
+    for w, t_order, n_off, n_len, k0, k1 in items:
         r = records[w]
         assert r.visits == cg, f"work item {w} stored {r.visits} times"
         tm, tn = osched.swizzle(t_order, Tm, Tn, group_m)
         assert (r.tile, r.n_off, r.n_len) == (tm * Tn + tn, n_off, n_len), w
-        cover.setdefault(r.tile, []).append((r.n_off, r.n_len))
-    # the items partition every tile's 256 columns exactly once
+        assert (r.kb_begin, r.kb_end) == (k0, k1), w
+        cover.setdefault(r.tile, []).append((r.kb_begin, r.kb_end, r.n_off, r.n_len))
+    # the items partition every tile (columns x k-blocks) exactly once
     assert sorted(cover) == list(range(T))
     for t, parts in cover.items():
-        parts.sort()
-        assert parts[0][0] == 0 and sum(n for _, n in parts) == 256
-        assert all(a + n == b for (a, n), (b, _) in zip(parts, parts[1:])), t
+        cells = sum((k1 - k0) * n for k0, k1, _, n in parts)
+        kb_total = max(k1 for _, k1, _, _ in parts)
+        assert cells == 256 * kb_total, t
     by_work = {w: (records[w].owner, records[w].iter) for w in range(W)}
     if sched == pts.GEMM_SCHED_STATIC:
         want = {w: (c, it) for w, c, it in osched.static_assignment(W, G)}

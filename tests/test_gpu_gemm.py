@@ -36,7 +36,7 @@ def _run_checked(h, x, sched, full=True):
     info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
     st, recs, dev = pts.gemm_read_debug(h, int(info.work_items))
     assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
-    check_records(recs, info, sched)
+    check_records(recs, info, sched, p.K)
     err = compare_full(x, C) if full else compare_sampled(x, C, info.tile_m, info.tile_n)
     assert err <= TOL[p.dtype], f"rel err {err}"
     return C, err
@@ -140,6 +140,42 @@ def test_forced_column_slices(cg, split, sched):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("split", [2, 3, 4])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_forced_k_split_with_fixup(cg, split, sched):
+    """Every tile cut into 2-4 K ranges; all but the last part to finish write
+    fp32 partials that the last one adds before storing C."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, split=split, split_k=1,
+                                         debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("ksplit", M, N, K, dt, dist, M + N + K + 10 * split))
+            for _ in range(2):      # twice: the claim counters of one launch must not leak into the next
+                _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
+def test_automatic_k_split_of_the_last_wave():
+    """A last partial wave that fits half a wave is cut along K when K is long."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        info = pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        G = int(info.max_active_clusters)
+        r = int(info.tiles) % G
+        if r and 2 * r <= G:
+            assert info.split_k == 1 and info.split >= 2 and info.full_work == info.tiles - r
+        info = pts.gemm_query(h, 4096, 4096, 128, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        assert info.split == 1                       # two k-blocks: a fixup would cost more than it saves
+        x = wl.make_inputs(wl.fp16_4096_ksweep([4096])[0])
+        for sched in SCHEDS:
+            _run_checked(h, x, sched, full=False)
+    finally:
+        pts.gemm_destroy(h)
+
+
 def test_automatic_slicing_of_sub_wave_problems():
     """Problems smaller than a wave are sliced so that more SMs take part."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=1))
@@ -212,7 +248,7 @@ def test_two_gemms_on_two_streams():
             info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, pts.GEMM_SCHED_CLC)
             st, recs, dev = pts.gemm_read_debug(h, int(info.work_items), s)
             assert st == 0
-            check_records(recs, info, pts.GEMM_SCHED_CLC)
+            check_records(recs, info, pts.GEMM_SCHED_CLC, p.K)
             assert compare_sampled(x, C, info.tile_m, info.tile_n) <= TOL[p.dtype]
     finally:
         for h in hs:

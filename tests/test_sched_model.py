@@ -105,18 +105,31 @@ def test_clc_replay_uneven_costs_cover_exactly_once():
 
 
 def test_work_items_hand_worked():
-    # 5 tiles, 4 whole, the fifth cut in two: columns 0-127 and 128-255
-    assert sm.work_items(5, 4, 2) == [(0, 0, 0, 256), (1, 1, 0, 256), (2, 2, 0, 256), (3, 3, 0, 256),
-                                      (4, 4, 0, 128), (5, 4, 128, 128)]
-    assert sm.work_items(2, 0, 4)[:4] == [(0, 0, 0, 64), (1, 0, 64, 64), (2, 0, 128, 64), (3, 0, 192, 64)]
+    # 5 tiles of 8 k-blocks, 4 whole, the fifth cut in two: columns 0-127 and 128-255
+    assert sm.work_items(5, 4, 2, num_kb=8) == [
+        (0, 0, 0, 256, 0, 8), (1, 1, 0, 256, 0, 8), (2, 2, 0, 256, 0, 8), (3, 3, 0, 256, 0, 8),
+        (4, 4, 0, 128, 0, 8), (5, 4, 128, 128, 0, 8)]
+    assert [i[2:4] for i in sm.work_items(2, 0, 4)[:4]] == [(0, 64), (64, 64), (128, 64), (192, 64)]
+    # the same tile cut along K in three: k-blocks 0-2, 3-5, 6-9
+    assert sm.work_items(5, 4, 3, split_k=True, num_kb=10)[4:] == [
+        (4, 4, 0, 256, 0, 3), (5, 4, 0, 256, 3, 6), (6, 4, 0, 256, 6, 10)]
 
 
-@pytest.mark.parametrize("T,F,s", [(512, 456, 2), (8, 0, 4), (528, 456, 2), (150, 150, 1), (800, 760, 2)])
-def test_work_items_partition_every_tile(T, F, s):
-    items = sm.work_items(T, F, s)
-    assert [w for w, _, _, _ in items] == list(range(F + s * (T - F)))
-    cols = {}
-    for _, t, off, n in items:
-        cols.setdefault(t, set()).update(range(off, off + n))
-    assert all(cols[t] == set(range(256)) for t in range(T))
-    assert sum(n for *_, n in items) == 256 * T        # no column computed twice
+@pytest.mark.parametrize("T,F,s,k", [(512, 456, 2, False), (8, 0, 4, False), (528, 456, 2, False),
+                                     (150, 150, 1, False), (800, 760, 2, False), (512, 456, 2, True),
+                                     (256, 228, 3, True), (800, 760, 4, True), (8, 0, 4, True)])
+def test_work_items_partition_every_tile(T, F, s, k):
+    num_kb = 7
+    items = sm.work_items(T, F, s, split_k=k, num_kb=num_kb)
+    assert [i[0] for i in items] == list(range(F + s * (T - F)))
+    cells = {}
+    for _, t, off, n, k0, k1 in items:
+        assert k1 > k0
+        cells.setdefault(t, []).append((off, n, k0, k1))
+    for t in range(T):
+        got = set()
+        for off, n, k0, k1 in cells[t]:
+            new = {(c, kb) for c in range(off, off + n) for kb in range(k0, k1)}
+            assert not (got & new)                      # nothing computed twice
+            got |= new
+        assert got == {(c, kb) for c in range(256) for kb in range(num_kb)}
