@@ -599,29 +599,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   + c * 16 * 32 + lane;
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
-                        st_cg_f4(dst + g * 32, __uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
-                                 __uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3]));
+                        __stcg(dst + g * 32, make_float4(__uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
+                                                         __uint_as_float(v0[4 * g + 2]),
+                                                         __uint_as_float(v0[4 * g + 3])));
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
-                        st_cg_f4(dst + (8 + g) * 32, __uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]),
-                                 __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]));
+                        __stcg(dst + (8 + g) * 32,
+                               make_float4(__uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]),
+                                           __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3])));
                     continue;
                 }
                 if (part > 0) {   // the last part of a K-split tile: add the others' partials
                     for (int sl = 0; sl < part; ++sl) {
+                        // issue the chunk's 16 loads before using any, so their
+                        // latencies overlap
                         const float4 *src = partials + sl * kPartialFloat4PerWarp + c * 16 * 32 + lane;
+                        float4 a[16];
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) a[g] = __ldcg(src + g * 32);
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
-                            const float4 a = ld_cg_f4(src + g * 32);
-                            v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + a.x);
-                            v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + a.y);
-                            v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + a.z);
-                            v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + a.w);
-                            const float4 b = ld_cg_f4(src + (8 + g) * 32);
-                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + b.x);
-                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + b.y);
-                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + b.z);
-                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + b.w);
+                            v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + a[g].x);
+                            v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + a[g].y);
+                            v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + a[g].z);
+                            v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + a[g].w);
+                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + a[8 + g].x);
+                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + a[8 + g].y);
+                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + a[8 + g].z);
+                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + a[8 + g].w);
                         }
                     }
                 }

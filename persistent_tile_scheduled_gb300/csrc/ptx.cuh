@@ -257,23 +257,6 @@ __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// 16-byte load that is cached in L2 only (data another SM wrote).
-__device__ __forceinline__ float4 ld_cg_f4(const float4 *p)
-{
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_cg_f4(float4 *p, float a, float b, float c, float d)
-{
-    asm volatile("st.global.cg.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 // ------------------------------------------ programmatic dependent launch
 
 // Let the next grid in the stream (launched with programmatic stream
