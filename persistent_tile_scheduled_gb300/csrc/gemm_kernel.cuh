@@ -366,6 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d_pair(sB + stage * SB, mb, fbc, x, yb);
                         }
                     }
+                    // keep the k-block prefetch_kb ahead of this one on its way into
+                    // L2, so that a stage rarely waits on an HBM miss
+                    const int kp = kb + p.prefetch_kb;
+                    if (p.prefetch_kb > 0 && kp < t.kb_end) {
+                        tma_prefetch_2d(&tmA, kp * KELEMS, ya);
+                        tma_prefetch_2d(mb, kp * KELEMS, yb);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;

@@ -20,6 +20,7 @@ constexpr int kEpiBufsPerWarp = 2;
 constexpr int kRing = 4;                // depth of the tile-id broadcast ring
 constexpr int kTmemCols = 512;          // two 256-column accumulators
 constexpr int kMaxStages = 8;
+constexpr int kDefaultPrefetchKb = 8;   // L2 prefetch distance of the operand loads (k-blocks)
 
 enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
 
@@ -48,6 +49,7 @@ struct GemmParams {
     int32_t group_m;            // GROUP_SIZE_M
     int32_t sched;
     int32_t stages;
+    int32_t prefetch_kb;        // L2 prefetch distance ahead of the operand loads, in k-blocks (0 = none)
     float out_scale;            // 1, or 1/(scale_a*scale_b) for e4m3
     uint32_t debug_flags;
     int32_t fault_arg;
@@ -62,18 +64,19 @@ struct GemmParams {
 constexpr int kPartialFloats = kRowsPerCta * kTileN;
 
 // K parts per leftover tile of the last partial wave, or 1.  Splitting K cuts
-// the wave's length to 1/parts of a tile's mainloop but costs a fixup (the
-// other parts' fp32 partials written and read back, about 3 k-blocks' time
-// each); parts must fit the idle clusters of that wave.
+// the wave's length to 1/parts of a tile's mainloop but costs a fixup: the
+// first parts write their fp32 partials, fence and flag, the last reads and
+// adds them.  Measured on GB300 that is ~8 us, about 25 k-blocks' mainloop
+// time, per extra part; parts must fit the idle clusters of that wave.
 inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
 {
     const int64_t r = tiles % resident;
     if (tiles < resident || r == 0) return 1;
     int best = 1;
-    int64_t best_gain = 4;   // in k-block times; smaller gains are not worth a fixup
+    int64_t best_gain = 8;   // in k-block times; smaller gains are not worth a fixup
     for (int s = 2; s <= 4; ++s) {
         if (s * r > resident || s > num_kb) break;
-        const int64_t gain = num_kb - num_kb / s - 3 * (s - 1);
+        const int64_t gain = num_kb - num_kb / s - 25 * (s - 1);
         if (gain > best_gain) {
             best_gain = gain;
             best = s;

@@ -126,6 +126,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
                  : "memory");
 }
 
+// Bring a 2-D box of the tensor into L2 (no shared-memory destination, no
+// completion); out-of-bounds parts are ignored.
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"

@@ -162,14 +162,14 @@ def test_automatic_k_split_of_the_last_wave():
     """A last partial wave that fits half a wave is cut along K when K is long."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
-        info = pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        info = pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
         G = int(info.max_active_clusters)
         r = int(info.tiles) % G
         if r and 2 * r <= G:
             assert info.split_k == 1 and info.split >= 2 and info.full_work == info.tiles - r
-        info = pts.gemm_query(h, 4096, 4096, 128, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.split == 1                       # two k-blocks: a fixup would cost more than it saves
-        x = wl.make_inputs(wl.fp16_4096_ksweep([4096])[0])
+        info = pts.gemm_query(h, 4096, 4096, 1024, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        assert info.split == 1                       # 16 k-blocks: a fixup would cost more than it saves
+        x = wl.make_inputs(wl.Problem("k8192", 4096, 4096, 8192, wl.F16, "normal_sqrtk", 77))
         for sched in SCHEDS:
             _run_checked(h, x, sched, full=False)
     finally:
