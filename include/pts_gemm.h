@@ -88,7 +88,7 @@ typedef struct gemm_opts {
     int split_k;                    /* with split >= 2: 0 = column slices (2 or 4),
                                        1 = K ranges with a fixup (2, 3 or 4) */
     int prefetch;                   /* L2 prefetch of the operands, in k-blocks ahead of the
-                                       loads (<= 64); 0 = default (8), -1 = none */
+                                       loads (<= 64); 0 = default (none), -1 = none */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are visited in grouped order; a work item is one

@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kMapCache = 16;
+constexpr int kMapCache = 1024;   // direct-mapped; a K sweep's A, B, C maps rarely collide
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per wait
 
 struct MapEntry {
@@ -52,7 +52,6 @@ struct gemm_ctx {
     int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
     int occ_clusters[3][2] = {};
     MapEntry maps[kMapCache];
-    int map_next = 0;
 };
 
 namespace {
@@ -67,12 +66,16 @@ gemm_status_t cuda_fail(cudaError_t e)
 const CUtensorMap *get_map(gemm_ctx *h, const void *ptr, uint64_t rows, uint64_t cols, int dtype,
                            uint32_t box_rows, uint32_t box_cols)
 {
-    for (auto &m : h->maps)
-        if (m.ptr == ptr && m.rows == rows && m.cols == cols && m.dtype == dtype && m.box_rows == box_rows
-            && m.box_cols == box_cols)
-            return &m.map;
-    MapEntry &m = h->maps[h->map_next];
-    h->map_next = (h->map_next + 1) % kMapCache;
+    // direct-mapped cache keyed by every field of the map
+    uint64_t key = reinterpret_cast<uintptr_t>(ptr) ^ (rows * 0x9E3779B97F4A7C15ull) ^ (cols * 0xC2B2AE3D27D4EB4Full)
+                   ^ (uint64_t(dtype) << 7) ^ (uint64_t(box_rows) << 17) ^ (uint64_t(box_cols) << 29);
+    key ^= key >> 31;
+    key *= 0x94D049BB133111EBull;
+    key ^= key >> 29;
+    MapEntry &m = h->maps[key % kMapCache];
+    if (m.ptr == ptr && m.rows == rows && m.cols == cols && m.dtype == dtype && m.box_rows == box_rows
+        && m.box_cols == box_cols)
+        return &m.map;
     m.ptr = nullptr;
     CUtensorMapDataType t = dtype == GEMM_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                             : dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16

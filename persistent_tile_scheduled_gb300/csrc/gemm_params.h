@@ -20,7 +20,8 @@ constexpr int kEpiBufsPerWarp = 2;
 constexpr int kRing = 4;                // depth of the tile-id broadcast ring
 constexpr int kTmemCols = 512;          // two 256-column accumulators
 constexpr int kMaxStages = 8;
-constexpr int kDefaultPrefetchKb = 8;   // L2 prefetch distance of the operand loads (k-blocks)
+constexpr int kDefaultPrefetchKb = 0;   // L2 prefetch of the operand loads: off (it costs more L2
+                                        // traffic than it saves in miss latency on GB300)
 
 enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
 
