@@ -168,6 +168,27 @@ gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             gemm_dtype_t dtype, gemm_sched_t sched,
                             float scale_a, float scale_b, void *stream);
 
+/* One GEMM of a host-buffer batch (see gemm_run_host_batch). */
+typedef struct gemm_host_problem {
+    int64_t M, N, K;
+    const void *A;          /* host, M x K */
+    const void *B;          /* host, N x K */
+    void *C;                /* host, M x N */
+    gemm_dtype_t dtype;
+    float scale_a, scale_b; /* e4m3 only */
+} gemm_host_problem_t;
+
+/* Run n GEMMs on HOST buffers with the transfers overlapped: while GEMM i
+ * computes on `stream`, the inputs of GEMM i+1 are copied in and the result of
+ * GEMM i-1 is copied out, on two copy streams the handle owns, through two
+ * device staging slots the handle owns (grown as needed).  Work already
+ * queued on `stream` completes before the first copy starts.  Returns after
+ * every result is in host memory (the call synchronises), with the device
+ * status like gemm_check.  Pinned host memory is needed for the copies to
+ * overlap.  Same size rules per problem as gemm_run; n == 0 does nothing. */
+gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *problems, int64_t n,
+                                  gemm_sched_t sched, void *stream);
+
 /* Launch shape gemm_run would use (no GPU work).  Same argument rules. */
 gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                          gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info);

@@ -47,6 +47,12 @@ struct gemm_ctx {
     uint32_t *d_ws_sync = nullptr;            // K-split claim counters / ready flags
     size_t ws_sync_cap = 0;                   // bytes
     uint32_t epoch = 0;                       // launch number for the fixup counters (1 .. 2^29 - 1)
+    // gemm_run_host_batch: two staging slots (A | B | C each), copy streams and events
+    void *d_slot[2] = {nullptr, nullptr};
+    size_t slot_cap = 0;
+    cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
+    cudaEvent_t ev_entry = nullptr, ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr},
+                ev_free[2] = {nullptr, nullptr};
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool smem_set[3][2] = {};
     int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
@@ -414,6 +420,82 @@ gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     return read_status(h, s, nullptr);
 }
 
+gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *probs, int64_t n,
+                                  gemm_sched_t sched, void *stream)
+{
+    if (h == nullptr || n < 0 || (n > 0 && probs == nullptr)) return GEMM_ERR_INVALID_ARG;
+    auto round_up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    size_t need = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const gemm_host_problem_t &q = probs[i];
+        gemm_status_t st = check_sizes(q.M, q.N, q.K, q.dtype, sched);
+        if (st != GEMM_OK) return st;
+        if (q.M == 0 || q.N == 0) continue;
+        if (q.C == nullptr || (q.K > 0 && (q.A == nullptr || q.B == nullptr))) return GEMM_ERR_INVALID_ARG;
+        const size_t es = size_t(elem_bytes(q.dtype));
+        const size_t slot = round_up(size_t(q.M) * size_t(q.K) * es) + round_up(size_t(q.N) * size_t(q.K) * es)
+                            + round_up(size_t(q.M) * size_t(q.N) * 2);
+        if (slot > need) need = slot;
+    }
+    if (n == 0 || need == 0) return GEMM_OK;
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (h->s_h2d == nullptr) {   // copy streams and events, created once
+        if (cudaStreamCreateWithFlags(&h->s_h2d, cudaStreamNonBlocking) != cudaSuccess
+            || cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking) != cudaSuccess
+            || cudaEventCreateWithFlags(&h->ev_entry, cudaEventDisableTiming) != cudaSuccess)
+            return cuda_fail(cudaErrorUnknown);
+        for (int b = 0; b < 2; ++b)
+            if (cudaEventCreateWithFlags(&h->ev_in[b], cudaEventDisableTiming) != cudaSuccess
+                || cudaEventCreateWithFlags(&h->ev_comp[b], cudaEventDisableTiming) != cudaSuccess
+                || cudaEventCreateWithFlags(&h->ev_free[b], cudaEventDisableTiming) != cudaSuccess)
+                return cuda_fail(cudaErrorUnknown);
+    }
+    if (h->slot_cap < need) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+        for (int b = 0; b < 2; ++b) {
+            cudaFree(h->d_slot[b]);
+            h->d_slot[b] = nullptr;
+        }
+        h->slot_cap = 0;
+        for (int b = 0; b < 2; ++b)
+            if (cudaMalloc(&h->d_slot[b], need) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
+        h->slot_cap = need;
+    }
+    // everything already queued on the caller's stream comes first
+    if (cudaEventRecord(h->ev_entry, cs) != cudaSuccess || cudaStreamWaitEvent(h->s_h2d, h->ev_entry, 0) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    gemm_status_t first_error = GEMM_OK;
+    for (int64_t i = 0; i < n; ++i) {
+        const gemm_host_problem_t &q = probs[i];
+        if (q.M == 0 || q.N == 0) continue;
+        const int b = int(i & 1);
+        const size_t es = size_t(elem_bytes(q.dtype));
+        const size_t a_bytes = size_t(q.M) * size_t(q.K) * es, b_bytes = size_t(q.N) * size_t(q.K) * es;
+        const size_t c_bytes = size_t(q.M) * size_t(q.N) * 2;
+        char *dA = static_cast<char *>(h->d_slot[b]);
+        char *dB = dA + round_up(a_bytes);
+        char *dC = dB + round_up(b_bytes);
+        // slot b is free once the copy-out of the GEMM that used it two steps ago is done
+        if (i >= 2 && cudaStreamWaitEvent(h->s_h2d, h->ev_free[b], 0) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+        if ((a_bytes && cudaMemcpyAsync(dA, q.A, a_bytes, cudaMemcpyHostToDevice, h->s_h2d) != cudaSuccess)
+            || (b_bytes && cudaMemcpyAsync(dB, q.B, b_bytes, cudaMemcpyHostToDevice, h->s_h2d) != cudaSuccess)
+            || cudaEventRecord(h->ev_in[b], h->s_h2d) != cudaSuccess || cudaStreamWaitEvent(cs, h->ev_in[b], 0) != cudaSuccess)
+            return cuda_fail(cudaErrorUnknown);
+        gemm_status_t st = launch(h, q.M, q.N, q.K, dA, dB, dC, q.dtype, sched, q.scale_a, q.scale_b, cs);
+        if (st != GEMM_OK && first_error == GEMM_OK) first_error = st;
+        if (cudaEventRecord(h->ev_comp[b], cs) != cudaSuccess || cudaStreamWaitEvent(h->s_d2h, h->ev_comp[b], 0) != cudaSuccess
+            || cudaMemcpyAsync(q.C, dC, c_bytes, cudaMemcpyDeviceToHost, h->s_d2h) != cudaSuccess
+            || cudaEventRecord(h->ev_free[b], h->s_d2h) != cudaSuccess)
+            return cuda_fail(cudaErrorUnknown);
+    }
+    // the caller's stream continues after the last copy-out
+    for (int b = 0; b < 2; ++b)
+        if (cudaStreamWaitEvent(cs, h->ev_free[b], 0) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    gemm_status_t st = read_status(h, cs, nullptr);
+    return first_error != GEMM_OK ? first_error : st;
+}
+
 gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                          gemm_sched_t sched, gemm_launch_info_t *info)
 {
@@ -476,6 +558,15 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
     cudaFree(h->d_host_bufs);
     cudaFree(h->d_ws_partial);
     cudaFree(h->d_ws_sync);
+    for (int b = 0; b < 2; ++b) {
+        cudaFree(h->d_slot[b]);
+        if (h->ev_in[b]) cudaEventDestroy(h->ev_in[b]);
+        if (h->ev_comp[b]) cudaEventDestroy(h->ev_comp[b]);
+        if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
+    }
+    if (h->ev_entry) cudaEventDestroy(h->ev_entry);
+    if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
+    if (h->s_d2h) cudaStreamDestroy(h->s_d2h);
     delete h;
     return GEMM_OK;
 }

@@ -22,7 +22,8 @@ GEMM_DEBUG_CLC_STOP_AT = 0x2
 GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
-            "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc")
+            "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc",
+            "gemm_run_host_batch")
 GEMM_NOALLOC_MAX_WORK_ITEMS = 16384
 
 
@@ -47,6 +48,12 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
                 ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("full_work", ctypes.c_int64),
                 ("work_items", ctypes.c_int64)]
+
+
+class gemm_host_problem_t(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("A", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("dtype", ctypes.c_int), ("scale_a", ctypes.c_float),
+                ("scale_b", ctypes.c_float)]
 
 
 class GemmError(RuntimeError):
@@ -78,6 +85,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gemm_run.restype = st
     lib.gemm_run_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int, f32, f32, vp]
     lib.gemm_run_host.restype = st
+    lib.gemm_run_host_batch.argtypes = [vp, ctypes.POINTER(gemm_host_problem_t), i64, ctypes.c_int, vp]
+    lib.gemm_run_host_batch.restype = st
     lib.gemm_query.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(gemm_launch_info_t)]
     lib.gemm_query.restype = st
     lib.gemm_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
@@ -142,6 +151,18 @@ def gemm_run(h, M, N, K, A, B, C, dtype, sched, scale_a=1.0, scale_b=1.0, stream
 def gemm_run_host(h, M, N, K, A, B, C, dtype, sched, scale_a=1.0, scale_b=1.0, stream=None) -> int:
     return _check(load().gemm_run_host(h, M, N, K, _ptr(A), _ptr(B), _ptr(C), int(dtype), int(sched),
                                        float(scale_a), float(scale_b), _stream(stream)), "gemm_run_host")
+
+
+def gemm_run_host_batch(h, problems, sched, stream=None) -> int:
+    """problems: sequence of (M, N, K, A, B, C, dtype[, scale_a, scale_b]) with
+    host tensors (pinned for overlap) or raw addresses."""
+    arr = (gemm_host_problem_t * max(len(problems), 1))()
+    for i, q in enumerate(problems):
+        M, N, K, A, B, C, dt = q[:7]
+        sa, sb = (q[7], q[8]) if len(q) > 7 else (1.0, 1.0)
+        arr[i] = gemm_host_problem_t(M, N, K, _ptr(A), _ptr(B), _ptr(C), int(dt), float(sa), float(sb))
+    return _check(load().gemm_run_host_batch(h, arr, len(problems), int(sched), _stream(stream)),
+                  "gemm_run_host_batch")
 
 
 def gemm_query(h, M, N, K, dtype, sched) -> gemm_launch_info_t:

@@ -188,6 +188,23 @@ def test_automatic_slicing_of_sub_wave_problems():
         pts.gemm_destroy(h)
 
 
+def test_run_host_batch_matches_device_path(handle):
+    """Overlapped host-buffer batch: every result equals the device-path result."""
+    h, _ = handle
+    xs = [wl.custom(300, 264, 128, wl.BF16, "uniform", 31), wl.custom(1000, 520, 1024, wl.F16, "uniform", 32),
+          wl.custom(640, 1000, 256, wl.E4M3, "normal", 33), wl.custom(8, 8, 16, wl.BF16, "uniform", 34),
+          wl.custom(513, 256, 64, wl.F16, "uniform", 35)]
+    want, batch = [], []
+    for x in xs:
+        p = x.problem
+        want.append(run_device(h, x, pts.GEMM_SCHED_CLC).cpu())
+        C = torch.empty(p.M, p.N, dtype=wl.output_torch_dtype(p.dtype)).pin_memory()
+        batch.append((p.M, p.N, p.K, x.A.pin_memory(), x.B.pin_memory(), C, p.dtype, x.scale_a, x.scale_b))
+    pts.gemm_run_host_batch(h, batch, pts.GEMM_SCHED_CLC)
+    for w, q in zip(want, batch):
+        assert torch.equal(w.view(torch.int16), q[5].view(torch.int16))
+
+
 # ---------------------------------------------------------------- full sizes
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
