@@ -584,13 +584,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const bool write_partial = part >= 0 && part < p.split - 1;
-#pragma unroll 1
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
-                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols + 32, v1);
+            // Chunks of 64 columns, software-pipelined: the TMEM loads of
+            // chunk c+1 are in flight while chunk c is converted and stored.
+            uint32_t ra0[32], ra1[32], rb0[32], rb1[32];
+            tmem_ld_32x32b_x32(tbase, ra0);
+            tmem_ld_32x32b_x32(tbase + 32, ra1);
+#pragma unroll
+            for (int c = 0; c < kTileN / kEpiChunkCols; ++c) {
+                if (c >= chunks) break;
+                uint32_t(&v0)[32] = (c & 1) ? rb0 : ra0;
+                uint32_t(&v1)[32] = (c & 1) ? rb1 : ra1;
                 tmem_wait_ld();
-                if (c == chunks - 1) {
+                if (c + 1 < chunks) {
+                    tmem_ld_32x32b_x32(tbase + (c + 1) * kEpiChunkCols, (c & 1) ? ra0 : rb0);
+                    tmem_ld_32x32b_x32(tbase + (c + 1) * kEpiChunkCols + 32, (c & 1) ? ra1 : rb1);
+                } else {
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
@@ -618,22 +626,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (part > 0) {   // the last part of a K-split tile: add the others' partials
                     for (int sl = 0; sl < part; ++sl) {
-                        // issue the chunk's 16 loads before using any, so their
-                        // latencies overlap
+                        // issue 8 loads before using any, so their latencies overlap
                         const float4 *src = partials + sl * kPartialFloat4PerWarp + c * 16 * 32 + lane;
-                        float4 a[16];
+                        float4 a[8];
 #pragma unroll
-                        for (int g = 0; g < 16; ++g) a[g] = __ldcg(src + g * 32);
+                        for (int g = 0; g < 8; ++g) a[g] = __ldcg(src + g * 32);
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
                             v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + a[g].x);
                             v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + a[g].y);
                             v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + a[g].z);
                             v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + a[g].w);
-                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + a[8 + g].x);
-                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + a[8 + g].y);
-                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + a[8 + g].z);
-                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + a[8 + g].w);
+                        }
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) a[g] = __ldcg(src + (8 + g) * 32);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + a[g].x);
+                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + a[g].y);
+                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + a[g].z);
+                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + a[g].w);
                         }
                     }
                 }
