@@ -98,10 +98,12 @@ typedef struct gemm_opts {
  *   - A problem smaller than one wave of resident clusters is cut into
  *     column slices of 256/split columns (split 2 or 4), so more SMs work.
  *   - Otherwise the tiles of the last partial wave may be cut into K ranges
- *     (split 2..4, k-block range h*kb/split .. (h+1)*kb/split): every part
+ *     (split 2..4): parts 0..split-2 get part_kb k-blocks each (part h covers
+ *     h*part_kb .. (h+1)*part_kb), the last part the rest.  Every part
  *     accumulates its range; each part but the last to finish writes its fp32
  *     partial to a workspace the handle owns, and the last adds them and
- *     stores C.  The last wave then ends after about 1/split of a tile.
+ *     stores C.  The shorter first parts publish their partials while the last
+ *     part still computes, and the wave ends well before a whole tile would.
  * Cutting tiles changes which CTA computes what, never the result beyond the
  * fp32 summation order.
  *
@@ -134,6 +136,7 @@ typedef struct gemm_launch_info {
     int split;                      /* parts per tile past full_work (1 = none) */
     int split_k;                    /* parts are K ranges (1) or column slices (0) */
     int64_t full_work;              /* work ids below this are whole tiles */
+    int64_t part_kb;                /* K ranges: k-blocks of every part but the last */
     int64_t work_items;             /* work items in total */
 } gemm_launch_info_t;
 

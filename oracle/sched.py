@@ -51,15 +51,17 @@ def swizzle(w: int, Tm: int, Tn: int, group_m: int) -> Tuple[int, int]:
 
 
 def work_items(T: int, full_work: int, split: int, tile_n: int = 256, split_k: bool = False,
-               num_kb: int = 1) -> List[Tuple[int, int, int, int, int, int]]:
+               num_kb: int = 1, part_kb: Optional[int] = None) -> List[Tuple[int, int, int, int, int, int]]:
     """(work id, grouped-order tile index, first column, columns, first k-block,
     end k-block) of every work item.
 
     Work ids below ``full_work`` are whole tiles.  Each remaining tile is cut
     into ``split`` parts: work id ``full_work + split*j + h`` is part h of
     tile ``full_work + j``.  Parts are column slices of ``tile_n / split``
-    columns, or (``split_k``) k-block ranges ``[h*num_kb//split,
-    (h+1)*num_kb//split)`` whose partial sums add up to the tile.  Cutting
+    columns, or (``split_k``) k-block ranges whose partial sums add up to the
+    tile: parts 0..split-2 take ``part_kb`` k-blocks each (default
+    ``num_kb // split``), part h covering ``[h*part_kb, (h+1)*part_kb)``, and
+    the last part takes the rest, up to ``num_kb``.  Cutting
     tiles changes how the output is partitioned among CTAs, never what is
     computed ("Neither mode creates additional independent work at the tail
     of a grid": cutting is a separate device for the last wave).
@@ -68,12 +70,15 @@ def work_items(T: int, full_work: int, split: int, tile_n: int = 256, split_k: b
         raise ValueError((T, full_work, split))
     if not split_k and split not in (1, 2, 4):
         raise ValueError(split)
+    a = (num_kb // split) if part_kb is None else part_kb
+    if split_k and not (1 <= a and (split - 1) * a < num_kb):
+        raise ValueError((num_kb, split, a))
     out = [(w, w, 0, tile_n, 0, num_kb) for w in range(full_work)]
     for j in range(T - full_work):
         for h in range(split):
             w = full_work + split * j + h
             if split_k:
-                out.append((w, full_work + j, 0, tile_n, h * num_kb // split, (h + 1) * num_kb // split))
+                out.append((w, full_work + j, 0, tile_n, h * a, num_kb if h == split - 1 else (h + 1) * a))
             else:
                 step = tile_n // split
                 out.append((w, full_work + j, h * step, step, 0, num_kb))

@@ -111,6 +111,7 @@ struct Plan {
     int64_t tiles_m, tiles_n, tiles;
     int split;               // parts per tile past full_work
     int split_k;             // parts are K ranges (1) or column slices (0)
+    int64_t part_kb;         // K ranges: k-blocks of every part but the last
     int64_t num_kb;          // k-blocks per whole tile
     int64_t full_work;       // work ids below this are whole tiles
     int64_t work;            // work items in total
@@ -136,6 +137,7 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
     pl.num_kb = (K + kelems - 1) / kelems;
     pl.cg = h->opts.cta_group;
+    pl.part_kb = 0;
     int stages = h->opts.stages;
     if (stages == 0) {   // the deepest ring that fits
         stages = pts::kMaxStages;
@@ -173,12 +175,14 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
         if (pl.split_k && pl.split > pl.num_kb) pl.split = static_cast<int>(pl.num_kb < 1 ? 1 : pl.num_kb);
         if (pl.split == 1) pl.split_k = 0;
         pl.full_work = pl.split == 1 ? pl.tiles : 0;
+        pl.part_kb = pl.split_k ? pl.num_kb / pl.split : 0;   // even parts, the last takes the remainder
     } else if ((pl.split = pts::choose_split(pl.tiles, resident)) > 1) {
         pl.split_k = 0;                                   // a sub-wave problem: column slices
         pl.full_work = 0;
     } else if ((pl.split = pts::choose_split_k(pl.tiles, resident, pl.num_kb)) > 1) {
         pl.split_k = 1;                                   // the last partial wave: K ranges + fixup
         pl.full_work = pl.tiles - pl.tiles % resident;
+        pl.part_kb = pts::split_part_kb(pl.num_kb, pl.split);
     } else {
         pl.split_k = 0;
         pl.full_work = pl.tiles;
@@ -256,6 +260,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.full_work = static_cast<int32_t>(pl.full_work);
     p.split = pl.split;
     p.split_k = pl.split_k;
+    p.part_kb = static_cast<int32_t>(pl.part_kb);
     p.epoch = h->epoch;
     p.ws_partial = pl.split_k ? h->d_ws_partial : nullptr;
     p.ws_sync = pl.split_k ? h->d_ws_sync : nullptr;
@@ -517,6 +522,7 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     info->tiles = pl.tiles;
     info->split = pl.split;
     info->split_k = pl.split_k;
+    info->part_kb = pl.part_kb;
     info->full_work = pl.full_work;
     info->work_items = pl.work;
     info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;

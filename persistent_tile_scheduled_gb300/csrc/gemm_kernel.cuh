@@ -101,10 +101,11 @@ __device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int gro
 
 // A work item: tile (tm, tn), its column slice [n_off, n_off + n_len) and its
 // k-block range [kb_begin, kb_end).  Work ids below full_work are whole tiles
-// in grouped order.  Each later tile (the last partial wave) is cut into
-// `split` parts: column slices (split_k == 0), or K ranges (split_k == 1)
-// whose fp32 partials are summed by the part that finishes last; `ks` is then
-// the index of the split tile among them (else -1).
+// in grouped order.  Each later tile is cut into `split` parts: column slices
+// (split_k == 0), or K ranges (split_k == 1: part_kb k-blocks for each part
+// but the last, which takes the rest) whose fp32 partials are summed by the
+// part that finishes last; `ks` is then the index of the split tile among
+// them (else -1).
 struct WorkTile {
     int tm, tn, n_off, n_len, kb_begin, kb_end, ks;
 };
@@ -124,8 +125,8 @@ __device__ __forceinline__ WorkTile work_tile(int w, const GemmParams &p)
         const int h = q - j * p.split;
         tile = p.full_work + j;
         if (p.split_k) {
-            t.kb_begin = (h * p.num_kb) / p.split;
-            t.kb_end = ((h + 1) * p.num_kb) / p.split;
+            t.kb_begin = h * p.part_kb;
+            t.kb_end = h == p.split - 1 ? p.num_kb : (h + 1) * p.part_kb;
             t.ks = j;
         } else {
             t.n_len = kTileN / p.split;

@@ -45,6 +45,7 @@ struct GemmParams {
     int32_t full_work;          // work ids below this are whole tiles
     int32_t split;              // each later tile is cut into `split` parts (1..4)
     int32_t split_k;            // 0: parts are column slices; 1: parts are K ranges, reduced in a fixup
+    int32_t part_kb;            // K ranges: k-blocks of each part but the last (the last gets the rest)
     uint32_t epoch;             // launch number (29 bits, never 0) tagging the fixup counters and flags
     int32_t num_work;           // full_work + split * (num_tiles - full_work)
     int32_t group_m;            // GROUP_SIZE_M
@@ -64,22 +65,38 @@ struct GemmParams {
 // Floats of one K-split partial: a CTA's 128 x 256 fp32 accumulator.
 constexpr int kPartialFloats = kRowsPerCta * kTileN;
 
-// K parts per leftover tile of the last partial wave, or 1.  Splitting K cuts
-// the wave's length to 1/parts of a tile's mainloop but costs a fixup: the
-// first parts write their fp32 partials, fence and flag, the last reads and
-// adds them.  Measured on GB300 that is ~8 us, about 25 k-blocks' mainloop
-// time, per extra part; parts must fit the idle clusters of that wave.
+// K-split of the last partial wave.  The first split-1 parts get `part_kb`
+// k-blocks each and the last part the rest, which is longer: the first parts
+// finish early and write their fp32 partials while the last one still
+// computes, so it finds them ready.  Measured on GB300 a writer needs about
+// kFixupWriteKb k-blocks' time to publish its partial and the last part about
+// kFixupReadKb per partial it adds.
+constexpr int kFixupWriteKb = 13;
+constexpr int kFixupReadKb = 5;
+
+inline int64_t split_part_kb(int64_t num_kb, int split)
+{
+    const int64_t a = (num_kb - kFixupWriteKb) / split;
+    return a < 1 ? 1 : a;
+}
+
+// K parts per leftover tile of the last partial wave (1 = no split): the
+// count that shortens the wave most, if it saves more than 8 k-blocks' time;
+// parts must fit the idle clusters of that wave.
 inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
 {
     const int64_t r = tiles % resident;
     if (tiles < resident || r == 0) return 1;
     int best = 1;
-    int64_t best_gain = 8;   // in k-block times; smaller gains are not worth a fixup
+    int64_t best_tail = num_kb - 8;
     for (int s = 2; s <= 4; ++s) {
         if (s * r > resident || s > num_kb) break;
-        const int64_t gain = num_kb - num_kb / s - 25 * (s - 1);
-        if (gain > best_gain) {
-            best_gain = gain;
+        const int64_t a = split_part_kb(num_kb, s);
+        const int64_t last = num_kb - (s - 1) * a;
+        const int64_t writers_done = a + kFixupWriteKb;
+        const int64_t tail = (last > writers_done ? last : writers_done) + kFixupReadKb * (s - 1);
+        if (tail < best_tail) {
+            best_tail = tail;
             best = s;
         }
     }

@@ -47,7 +47,7 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64),
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
                 ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("full_work", ctypes.c_int64),
-                ("work_items", ctypes.c_int64)]
+                ("part_kb", ctypes.c_int64), ("work_items", ctypes.c_int64)]
 
 
 class gemm_host_problem_t(ctypes.Structure):

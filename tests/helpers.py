@@ -67,7 +67,8 @@ def check_records(records, info, sched: int, K: int, group_m: int = 8):
     W, F, split = int(info.work_items), int(info.full_work), int(info.split)
     G = int(info.grid_ctas) // cg
     num_kb = -(-int(K) // int(info.tile_k))
-    items = osched.work_items(T, F, split, split_k=bool(info.split_k), num_kb=num_kb)
+    items = osched.work_items(T, F, split, split_k=bool(info.split_k), num_kb=num_kb,
+                              part_kb=int(info.part_kb) if info.split_k else None)
     assert len(items) == W
     cover = {}
     for w, t_order, n_off, n_len, k0, k1 in items:

@@ -113,14 +113,21 @@ def test_work_items_hand_worked():
     # the same tile cut along K in three: k-blocks 0-2, 3-5, 6-9
     assert sm.work_items(5, 4, 3, split_k=True, num_kb=10)[4:] == [
         (4, 4, 0, 256, 0, 3), (5, 4, 0, 256, 3, 6), (6, 4, 0, 256, 6, 10)]
+    # uneven K parts: a short first part (25 k-blocks) and a long last one (39)
+    assert sm.work_items(5, 4, 2, split_k=True, num_kb=64, part_kb=25)[4:] == [
+        (4, 4, 0, 256, 0, 25), (5, 4, 0, 256, 25, 64)]
+    with pytest.raises(ValueError):      # parts must leave the last one at least a k-block
+        sm.work_items(5, 4, 3, split_k=True, num_kb=10, part_kb=5)
 
 
-@pytest.mark.parametrize("T,F,s,k", [(512, 456, 2, False), (8, 0, 4, False), (528, 456, 2, False),
-                                     (150, 150, 1, False), (800, 760, 2, False), (512, 456, 2, True),
-                                     (256, 228, 3, True), (800, 760, 4, True), (8, 0, 4, True)])
-def test_work_items_partition_every_tile(T, F, s, k):
+@pytest.mark.parametrize("T,F,s,k,a", [(512, 456, 2, False, None), (8, 0, 4, False, None),
+                                       (528, 456, 2, False, None), (150, 150, 1, False, None),
+                                       (800, 760, 2, False, None), (512, 456, 2, True, None),
+                                       (256, 228, 3, True, None), (800, 760, 4, True, None), (8, 0, 4, True, None),
+                                       (512, 456, 2, True, 2), (256, 228, 3, True, 1)])
+def test_work_items_partition_every_tile(T, F, s, k, a):
     num_kb = 7
-    items = sm.work_items(T, F, s, split_k=k, num_kb=num_kb)
+    items = sm.work_items(T, F, s, split_k=k, num_kb=num_kb, part_kb=a)
     assert [i[0] for i in items] == list(range(F + s * (T - F)))
     cells = {}
     for _, t, off, n, k0, k1 in items:
