@@ -89,6 +89,10 @@ typedef struct gemm_opts {
                                        1 = K ranges with a fixup (2, 3 or 4) */
     int prefetch;                   /* L2 prefetch of the operands, in k-blocks ahead of the
                                        loads (<= 64); 0 = default (none), -1 = none */
+    int overlap_launch;             /* 0 = default (on): a launch may start while the previous
+                                       kernel in the stream finishes (programmatic dependent
+                                       launch; it waits for that kernel before touching memory);
+                                       -1 = off */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are visited in grouped order; a work item is one

@@ -292,7 +292,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     h->last_cta_group = pl.cg;
 
     cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(*ma, mb, *mc, p, static_cast<int>(pl.grid_ctas),
-                                                                   pl.smem, stream);
+                                                                   pl.smem, stream, h->opts.overlap_launch >= 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return cuda_fail(cudaGetLastError());
 }
@@ -338,7 +338,7 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (o.prefetch > 64) return GEMM_ERR_INVALID_ARG;
+    if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0) return GEMM_ERR_INVALID_ARG;
     if (o.split < 0 || o.split > 4 || (!o.split_k && o.split == 3) || (o.split_k != 0 && o.split_k != 1))
         return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))

@@ -17,7 +17,7 @@ struct Inst {
     // grid in the stream finishes (the kernel waits for it before touching
     // global memory).
     static void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid_ctas, int smem,
-                            cudaStream_t stream)
+                            cudaStream_t stream, bool overlap = true)
     {
         cfg = cudaLaunchConfig_t{};
         cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
@@ -26,9 +26,11 @@ struct Inst {
         cfg.stream = stream;
         cfg.attrs = attr;
         int n = 0;
-        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n].val.programmaticStreamSerializationAllowed = 1;
-        ++n;
+        if (overlap) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
         if (CG == 2) {
             attr[n].id = cudaLaunchAttributeClusterDimension;
             attr[n].val.clusterDim.x = 2;
@@ -58,11 +60,11 @@ struct Inst {
     }
 
     static cudaError_t launch(const CUtensorMap &a, const CUtensorMap *const b[3], const CUtensorMap &c,
-                              const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream)
+                              const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream, bool overlap)
     {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[2];
-        fill_config(cfg, attr, grid_ctas, smem, stream);
+        fill_config(cfg, attr, grid_ctas, smem, stream, overlap);
         return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG>, a, *b[0], *b[1], *b[2], c, p);
     }
 

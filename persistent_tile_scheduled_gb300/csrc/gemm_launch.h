@@ -15,7 +15,7 @@ struct KernelOps {
     cudaError_t (*max_active_clusters)(int smem, int *out);
     // b[0..2]: B maps with boxes of 256/CG, 128/CG and 64/CG rows
     cudaError_t (*launch)(const CUtensorMap &a, const CUtensorMap *const b[3], const CUtensorMap &c,
-                          const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream);
+                          const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream, bool overlap);
 };
 
 // kind: 0 fp16, 1 bf16, 2 e4m3

@@ -209,7 +209,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     int64_t clusters = work;
     if (sched == GEMM_SCHED_STATIC && clusters > resident) clusters = resident;
     pts::KernelOps ops = cta_group == 2 ? pts::kernel_ops_cg2(dtype) : pts::kernel_ops_cg1(dtype);
-    cudaError_t e = ops.launch(ma, mbs, mc, p, static_cast<int>(clusters * cta_group), s->smem[ci], st);
+    cudaError_t e = ops.launch(ma, mbs, mc, p, static_cast<int>(clusters * cta_group), s->smem[ci], st, true);
     if (e != cudaSuccess) return fail(e);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
     if (device_status == nullptr) return GEMM_OK;
