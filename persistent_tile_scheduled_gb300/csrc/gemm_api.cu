@@ -238,16 +238,29 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     }
     h->epoch = h->epoch % 0x1FFFFFFFu + 1u;
 
+    // Each map is copied out of the cache at once: a later lookup in this same
+    // call may reuse the cache slot an earlier map came from.
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
-    const CUtensorMap *ma = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems);
     const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
-    const CUtensorMap *mb[3] = {get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows, kelems), nullptr, nullptr};
-    mb[1] = pl.split == 2 ? get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / 2, kelems) : mb[0];
-    mb[2] = pl.split == 4 ? get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / 4, kelems) : mb[0];
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
-    const CUtensorMap *mc = get_map(h, C, uint64_t(M), uint64_t(N), cdt, pts::kEpiRowsPerWarp,
-                                    pts::kEpiChunkCols);
-    if (!ma || !mb[0] || !mb[1] || !mb[2] || !mc) return GEMM_ERR_CUDA;
+    const bool slices = pl.split > 1 && !pl.split_k;
+    CUtensorMap ma, mb0, mb_slice, mc;
+    const CUtensorMap *m;
+    if (!(m = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems))) return GEMM_ERR_CUDA;
+    ma = *m;
+    if (!(m = get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows, kelems))) return GEMM_ERR_CUDA;
+    mb0 = *m;
+    mb_slice = mb0;
+    if (slices) {
+        if (!(m = get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(pl.split), kelems)))
+            return GEMM_ERR_CUDA;
+        mb_slice = *m;
+    }
+    if (!(m = get_map(h, C, uint64_t(M), uint64_t(N), cdt, pts::kEpiRowsPerWarp, pts::kEpiChunkCols)))
+        return GEMM_ERR_CUDA;
+    mc = *m;
+    const CUtensorMap *mb[3] = {&mb0, (slices && pl.split == 2) ? &mb_slice : &mb0,
+                                (slices && pl.split == 4) ? &mb_slice : &mb0};
 
     pts::GemmParams p{};
     p.M = static_cast<int32_t>(M);
@@ -291,7 +304,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     h->last_work = pl.work;
     h->last_cta_group = pl.cg;
 
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(*ma, mb, *mc, p, static_cast<int>(pl.grid_ctas),
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(ma, mb, mc, p, static_cast<int>(pl.grid_ctas),
                                                                    pl.smem, stream, h->opts.overlap_launch >= 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return cuda_fail(cudaGetLastError());

@@ -188,6 +188,26 @@ def test_automatic_slicing_of_sub_wave_problems():
         pts.gemm_destroy(h)
 
 
+def test_many_buffer_sets_on_one_handle():
+    """More distinct A, B, C buffers than the tensor-map cache has slots, with
+    every cut of the tiles in play: maps evicted from the cache, even within
+    one call, never leak into a launch."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=2, timeout_ns=200_000_000))
+    try:
+        shapes = [(4096, 4096, k) for k in range(2816, 4097, 128)] + [(512, 512, 512), (384, 264, 1024)]
+        outs = []
+        for i, (M, N, K) in enumerate(shapes * 2):
+            x = wl.custom(M, N, K, wl.F16, "normal_sqrtk", 900 + i)
+            outs.append((x, run_device(h, x, pts.GEMM_SCHED_STATIC)))
+        st, dev = pts.gemm_check(h)
+        assert st == 0, f"device word {dev:#x}"
+        for x, C in outs[-4:]:
+            p = x.problem
+            assert compare_sampled(x, C, 256, 256) <= TOL[wl.F16]
+    finally:
+        pts.gemm_destroy(h)
+
+
 def test_run_host_batch_matches_device_path(handle):
     """Overlapped host-buffer batch: every result equals the device-path result."""
     h, _ = handle
