@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -300,9 +301,13 @@ def run_ours(args, dist, rank, world, local):
         if args.e2e:
             e2e = end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream)
         extra = square_8192(pts, local, stream) if args.square and rank == 0 else None
+        extras = extra_configs(pts, local, stream) if args.extras and rank == 0 else None
     finally:
         pts.gemm_destroy(h)
-    return finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step)
+    line = finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step)
+    if extras is not None:
+        line["other_configs"] = extras
+    return line
 
 
 def end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream):
@@ -380,6 +385,94 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
     return line
 
 
+def device_inputs(p, seed):
+    """Seeded inputs of problem p generated on the GPU (timing-only extras;
+    the tests check parity on these shapes with CPU-generated inputs)."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    if p.dtype == wl.E4M3:
+        a = torch.randn(p.M, p.K, device="cuda", generator=g)
+        b = torch.randn(p.N, p.K, device="cuda", generator=g)
+        sa, sb = 448.0 / float(a.abs().max()), 448.0 / float(b.abs().max())
+        return ((a * sa).clamp(-448, 448).to(torch.float8_e4m3fn), (b * sb).clamp(-448, 448).to(torch.float8_e4m3fn),
+                sa, sb)
+    td = torch.float16 if p.dtype == wl.F16 else torch.bfloat16
+    s = 1.0 / math.sqrt(p.K)
+    return ((torch.randn(p.M, p.K, device="cuda", generator=g) * s).to(td),
+            (torch.randn(p.N, p.K, device="cuda", generator=g) * s).to(td), 1.0, 1.0)
+
+
+def time_one(pts, h, p, A, B, C, sa, sb, sched, stream, reps):
+    for _ in range(2):
+        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, sa, sb, stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for r in range(reps):
+            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, sa, sb, stream)
+            ev[r + 1].record(stream)
+    torch.cuda.synchronize()
+    if pts.gemm_check(h, stream)[0] != 0:
+        raise RuntimeError(f"device error in {p.name}")
+    return statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+
+
+def extra_configs(pts, dev, stream):
+    """The other workloads, TFLOP/s per scheduler (CTA pairs): bf16 8192 sweep
+    points, e4m3 8192^3, the tail shapes, and two GEMMs at once on two streams."""
+    out = {}
+    h = pts.gemm_create(dev, pts.make_opts(cta_group=2))
+    try:
+        probs = (wl.bf16_8192_ksweep([256, 1024, 2048, 4096, 6144, 8192]) + wl.e4m3_8192() + wl.bf16_tail())
+        for i, p in enumerate(probs):
+            A, B, sa, sb = device_inputs(p, 7000 + i)
+            C = torch.empty(p.M, p.N, dtype=wl.output_torch_dtype(p.dtype), device="cuda")
+            reps = 5 if p.M * p.N * p.K > 2 ** 38 else 10
+            row = {}
+            for si, name in enumerate(SCHED_NAMES):
+                ms = time_one(pts, h, p, A, B, C, sa, sb, si, stream, reps)
+                row[name] = round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1)
+            out[p.name] = row
+            del A, B, C
+        # two GEMMs in flight at once on two streams: the case CLC redistributes work for
+        pa, pb = wl.bf16_tail()[0], wl.bf16_tail()[2]
+        ins = [device_inputs(pa, 7100), device_inputs(pb, 7101)]
+        Cs = [torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda") for p in (pa, pb)]
+        hs = [h, pts.gemm_create(dev, pts.make_opts(cta_group=2))]
+        streams = [stream, torch.cuda.Stream()]
+        conc = {}
+        try:
+            for si, name in enumerate(SCHED_NAMES):
+                times = []
+                for rep in range(6):
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(streams[0])
+                    streams[1].wait_event(e0)
+                    for hh, s_, p, (A, B, sa, sb), C in zip(hs, streams, (pa, pb), ins, Cs):
+                        pts.gemm_run(hh, p.M, p.N, p.K, A, B, C, p.dtype, si, sa, sb, s_)
+                    end1 = torch.cuda.Event()
+                    end1.record(streams[1])
+                    streams[0].wait_event(end1)
+                    e1.record(streams[0])
+                    torch.cuda.synchronize()
+                    if rep >= 2:
+                        times.append(e0.elapsed_time(e1))
+                for hh, s_ in zip(hs, streams):
+                    if pts.gemm_check(hh, s_)[0] != 0:
+                        raise RuntimeError("device error in the concurrent pair")
+                ms = statistics.median(times)
+                conc[name] = {"ms": round(ms, 4), "tflops": round(
+                    (gemm_flops(pa.M, pa.N, pa.K) + gemm_flops(pb.M, pb.N, pb.K)) / (ms * 1e-3) / 1e12, 1)}
+        finally:
+            pts.gemm_destroy(hs[1])
+        out["concurrent_" + pa.name + "+" + pb.name] = conc
+    finally:
+        pts.gemm_destroy(h)
+    out["note"] = ("CTA pairs; median of back-to-back launches; inputs generated on the GPU from seeded "
+                   "generators (parity for these shapes is in the tests)")
+    return out
+
+
 def square_8192(pts, dev, stream, reps=10):
     """bf16 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
     p = wl.bf16_8192_ksweep([8192])[0]
@@ -455,6 +548,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-square", dest="square", action="store_false")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the other workloads (bf16 8192 sweep points, e4m3, tail shapes, concurrent pair)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
