@@ -272,7 +272,7 @@ def run_ours(args, dist, rank, world, local):
 
     per_sched = {}
     clocks = None
-    h = pts.gemm_create(local, pts.make_opts(cta_group=args.cta_group))
+    h = pts.gemm_create(local, pts.make_opts(cta_group=args.cta_group, epilogue=args.epilogue))
     try:
         for si, name in enumerate(SCHED_NAMES):
             if name not in args.scheds:
@@ -555,6 +555,8 @@ def main():
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
     ap.add_argument("--cta-group", type=int, default=2, choices=[1, 2])
+    ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],
+                    help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the 32 GEMMs of a step one by one instead of replaying a CUDA graph")
     args = ap.parse_args()

@@ -93,6 +93,9 @@ typedef struct gemm_opts {
                                        kernel in the stream finishes (programmatic dependent
                                        launch; it waits for that kernel before touching memory);
                                        -1 = off */
+    int epilogue;                   /* 0 = default (1); 1 = TMA stores from a swizzled shared-
+                                       memory staging buffer; 2 = every lane stores its row's
+                                       outputs straight from registers */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are visited in grouped order; a work item is one

@@ -282,6 +282,8 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.sched = static_cast<int32_t>(sched);
     p.stages = pl.stages;
     p.prefetch_kb = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
+    p.epi_direct = h->opts.epilogue == 2 ? 1 : 0;
+    p.c_ptr = C;
     p.out_scale = out_scale;
     p.debug_flags = h->opts.debug_flags;
     p.fault_arg = h->opts.fault_arg;
@@ -351,7 +353,8 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0) return GEMM_ERR_INVALID_ARG;
+    if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)
+        return GEMM_ERR_INVALID_ARG;
     if (o.split < 0 || o.split > 4 || (!o.split_k && o.split == 3) || (o.split_k != 0 && o.split_k != 1))
         return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))

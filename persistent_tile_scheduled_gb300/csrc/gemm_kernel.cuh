@@ -656,6 +656,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[j] = pack2<KIND>(v0[2 * j], v0[2 * j + 1], p.out_scale);
                     pk[16 + j] = pack2<KIND>(v1[2 * j], v1[2 * j + 1], p.out_scale);
                 }
+                const int col = t.tn * kTileN + t.n_off + c * kEpiChunkCols;
+                if (p.epi_direct) {
+                    // this lane's row: 64 outputs = 8 x 16 bytes, straight to global
+                    const int row = row0 + static_cast<int>(lane);
+                    if (row < p.M) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c_ptr)
+                                                               + static_cast<long long>(row) * p.N + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (col + 8 * j < p.N)
+                                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                    continue;
+                }
                 const uint32_t buf = stage_base + (nstore & 1u) * kEpiBufBytes;
                 if (lane == 0) bulk_wait_read<1>();   // the store that used this buffer has read it
                 __syncwarp();
@@ -668,7 +682,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int col = t.tn * kTileN + t.n_off + c * kEpiChunkCols;
                 if (lane == 0) {
                     if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
                     bulk_commit();

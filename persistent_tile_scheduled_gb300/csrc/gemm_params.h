@@ -52,6 +52,8 @@ struct GemmParams {
     int32_t sched;
     int32_t stages;
     int32_t prefetch_kb;        // L2 prefetch distance ahead of the operand loads, in k-blocks (0 = none)
+    int32_t epi_direct;         // 1: the epilogue stores C rows straight from registers (no TMA store)
+    void *c_ptr;                // C (for the direct-store epilogue)
     float out_scale;            // 1, or 1/(scale_a*scale_b) for e4m3
     uint32_t debug_flags;
     int32_t fault_arg;

@@ -31,7 +31,7 @@ class gemm_opts_t(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int), ("group_size_m", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("debug_flags", ctypes.c_uint), ("fault_arg", ctypes.c_int),
                 ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int), ("split_k", ctypes.c_int),
-                ("prefetch", ctypes.c_int), ("overlap_launch", ctypes.c_int)]
+                ("prefetch", ctypes.c_int), ("overlap_launch", ctypes.c_int), ("epilogue", ctypes.c_int)]
 
 
 class gemm_tile_record_t(ctypes.Structure):
@@ -131,9 +131,9 @@ def gemm_status_string(status: int) -> str:
 
 
 def make_opts(cta_group=1, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
-              timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0) -> gemm_opts_t:
+              timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0, epilogue=0) -> gemm_opts_t:
     return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split,
-                       split_k, prefetch, overlap_launch)
+                       split_k, prefetch, overlap_launch, epilogue)
 
 
 def gemm_create(device: int = 0, opts: Optional[gemm_opts_t] = None) -> int:

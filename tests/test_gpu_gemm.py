@@ -158,6 +158,22 @@ def test_forced_k_split_with_fixup(cg, split, sched):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("split,split_k", [(1, 0), (2, 0), (2, 1)])
+def test_direct_store_epilogue(cg, split, split_k):
+    """The epilogue that stores C rows straight from registers (no TMA store)."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, epilogue=2, split=split, split_k=split_k,
+                                         debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("direct", M, N, K, dt, dist, M + N + K + 3))
+            for sched in SCHEDS:
+                _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
 def test_automatic_k_split_of_the_last_wave():
     """A last partial wave that fits half a wave is cut along K when K is long."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
