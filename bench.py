@@ -39,7 +39,9 @@ UNIT = "TFLOP/s"
 WORKLOAD = ("fp16 GEMM M=N=4096, K=128..4096 step 128 (32 GEMMs per step), A,B ~ N(0,1)/sqrt(K), "
             "fp32 accumulate, fp16 C, row-major A, column-major B")
 SCHED_NAMES = ["nonpersistent", "static", "clc"]
-TILE_DESC = {1: "128x256x64 per CTA (tcgen05 cta_group::1)",
+TILE_DESC = {0: "128x256x64 per CTA; single CTAs (tcgen05 cta_group::1) for every GEMM of this sweep "
+                "(the library pairs CTAs only from 128 k-blocks per tile)",
+             1: "128x256x64 per CTA (tcgen05 cta_group::1)",
              2: "128x256x64 per CTA; CTA pairs run one 256x256 tcgen05 cta_group::2 MMA and share B"}
 HEADLINE = "static"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -417,10 +419,10 @@ def time_one(pts, h, p, A, B, C, sa, sb, sched, stream, reps):
 
 
 def extra_configs(pts, dev, stream):
-    """The other workloads, TFLOP/s per scheduler (CTA pairs): bf16 8192 sweep
+    """The other workloads, TFLOP/s per scheduler: bf16 8192 sweep
     points, e4m3 8192^3, the tail shapes, and two GEMMs at once on two streams."""
     out = {}
-    h = pts.gemm_create(dev, pts.make_opts(cta_group=2))
+    h = pts.gemm_create(dev, pts.make_opts(cta_group=0))
     try:
         probs = (wl.bf16_8192_ksweep([256, 1024, 2048, 4096, 6144, 8192]) + wl.e4m3_8192() + wl.bf16_tail())
         for i, p in enumerate(probs):
@@ -437,7 +439,7 @@ def extra_configs(pts, dev, stream):
         pa, pb = wl.bf16_tail()[0], wl.bf16_tail()[2]
         ins = [device_inputs(pa, 7100), device_inputs(pb, 7101)]
         Cs = [torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda") for p in (pa, pb)]
-        hs = [h, pts.gemm_create(dev, pts.make_opts(cta_group=2))]
+        hs = [h, pts.gemm_create(dev, pts.make_opts(cta_group=0))]
         streams = [stream, torch.cuda.Stream()]
         conc = {}
         try:
@@ -468,8 +470,9 @@ def extra_configs(pts, dev, stream):
         out["concurrent_" + pa.name + "+" + pb.name] = conc
     finally:
         pts.gemm_destroy(h)
-    out["note"] = ("CTA pairs; median of back-to-back launches; inputs generated on the GPU from seeded "
-                   "generators (parity for these shapes is in the tests)")
+    out["note"] = ("library's CTA group per GEMM (pairs from 128 k-blocks per tile); median of back-to-back "
+                   "launches; inputs generated on the GPU from seeded generators (parity for these shapes is in "
+                   "the tests)")
     return out
 
 
@@ -554,7 +557,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
-    ap.add_argument("--cta-group", type=int, default=2, choices=[1, 2])
+    ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
+                    help="0 = the library's choice per GEMM (single CTAs below 128 k-blocks per tile)")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],
                     help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

@@ -76,7 +76,8 @@ typedef enum {
  * GEMM_ERR_TIMEOUT and C is unspecified.  The context stays usable. */
 
 typedef struct gemm_opts {
-    int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair); 0 = 1 */
+    int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair);
+                                       0 = per call: pairs when a tile has >= 128 k-blocks */
     int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
     int stages;                     /* shared-memory ring depth; 0 = the most that fits */
     int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */

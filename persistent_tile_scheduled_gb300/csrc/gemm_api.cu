@@ -136,7 +136,7 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
 {
     const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
     pl.num_kb = (K + kelems - 1) / kelems;
-    pl.cg = h->opts.cta_group;
+    pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb);
     pl.part_kb = 0;
     int stages = h->opts.stages;
     if (stages == 0) {   // the deepest ring that fits
@@ -347,10 +347,9 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     *out = nullptr;
     gemm_opts_t o{};
     if (opts) o = *opts;
-    if (o.cta_group == 0) o.cta_group = 1;
     if (o.group_size_m == 0) o.group_size_m = 8;
     if (o.timeout_ns == 0) o.timeout_ns = kDefaultTimeoutNs;
-    if (o.cta_group != 1 && o.cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    if (o.cta_group < 0 || o.cta_group > 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
     if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)

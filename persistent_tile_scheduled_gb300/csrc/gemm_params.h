@@ -105,6 +105,15 @@ inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
     return best;
 }
 
+// CTA group when the caller leaves it to the library: CTA pairs (cta_group 2)
+// halve the B traffic per SM but cost a few microseconds per launch in pair
+// synchronisation; measured on GB300 they pay off from about 128 k-blocks per
+// tile (bf16 8192^3: 625 vs 655 us), single CTAs win below (fp16 4096^2 at
+// K = 128..4096: 6 us per launch).
+constexpr int kPairMinKb = 128;
+
+inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
+
 // Column slices per tile for a problem of `tiles` tiles on `resident`
 // clusters.  Only a problem smaller than one wave is sliced (quarters when it
 // fits in a quarter wave, halves when it fits in half): there slicing puts

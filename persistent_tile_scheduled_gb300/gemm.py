@@ -130,7 +130,7 @@ def gemm_status_string(status: int) -> str:
     return load().gemm_status_string(int(status)).decode()
 
 
-def make_opts(cta_group=1, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
+def make_opts(cta_group=0, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
               timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0, epilogue=0) -> gemm_opts_t:
     return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split,
                        split_k, prefetch, overlap_launch, epilogue)
