@@ -191,8 +191,9 @@ typedef struct gemm_host_problem {
 
 /* Run n GEMMs on HOST buffers with the transfers overlapped: while GEMM i
  * computes on `stream`, the inputs of GEMM i+1 are copied in and the result of
- * GEMM i-1 is copied out, on two copy streams the handle owns, through two
- * device staging slots the handle owns (grown as needed).  Work already
+ * GEMM i-1 is copied out, on two copy streams the handle owns, through four
+ * device staging slots the handle owns (grown as needed), so copy-in may run
+ * up to three GEMMs ahead of copy-out.  Work already
  * queued on `stream` completes before the first copy starts.  Returns after
  * every result is in host memory (the call synchronises), with the device
  * status like gemm_check.  Pinned host memory is needed for the copies to

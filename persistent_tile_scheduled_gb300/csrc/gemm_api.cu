@@ -15,6 +15,7 @@
 
 namespace {
 
+constexpr int kBatchSlots = 4;   // gemm_run_host_batch staging depth
 constexpr int kMapCache = 1024;   // direct-mapped; a K sweep's A, B, C maps rarely collide
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per wait
 
@@ -47,12 +48,11 @@ struct gemm_ctx {
     uint32_t *d_ws_sync = nullptr;            // K-split claim counters / ready flags
     size_t ws_sync_cap = 0;                   // bytes
     uint32_t epoch = 0;                       // launch number for the fixup counters (1 .. 2^29 - 1)
-    // gemm_run_host_batch: two staging slots (A | B | C each), copy streams and events
-    void *d_slot[2] = {nullptr, nullptr};
+    // gemm_run_host_batch: staging slots (A | B | C each), copy streams and events
+    void *d_slot[kBatchSlots] = {};
     size_t slot_cap = 0;
     cudaStream_t s_h2d = nullptr, s_d2h = nullptr;
-    cudaEvent_t ev_entry = nullptr, ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr},
-                ev_free[2] = {nullptr, nullptr};
+    cudaEvent_t ev_entry = nullptr, ev_in[kBatchSlots] = {}, ev_comp[kBatchSlots] = {}, ev_free[kBatchSlots] = {};
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool smem_set[3][2] = {};
     int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
@@ -465,7 +465,7 @@ gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *pr
             || cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking) != cudaSuccess
             || cudaEventCreateWithFlags(&h->ev_entry, cudaEventDisableTiming) != cudaSuccess)
             return cuda_fail(cudaErrorUnknown);
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < kBatchSlots; ++b)
             if (cudaEventCreateWithFlags(&h->ev_in[b], cudaEventDisableTiming) != cudaSuccess
                 || cudaEventCreateWithFlags(&h->ev_comp[b], cudaEventDisableTiming) != cudaSuccess
                 || cudaEventCreateWithFlags(&h->ev_free[b], cudaEventDisableTiming) != cudaSuccess)
@@ -473,12 +473,12 @@ gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *pr
     }
     if (h->slot_cap < need) {
         if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaErrorUnknown);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kBatchSlots; ++b) {
             cudaFree(h->d_slot[b]);
             h->d_slot[b] = nullptr;
         }
         h->slot_cap = 0;
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < kBatchSlots; ++b)
             if (cudaMalloc(&h->d_slot[b], need) != cudaSuccess) return cuda_fail(cudaErrorMemoryAllocation);
         h->slot_cap = need;
     }
@@ -489,15 +489,16 @@ gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *pr
     for (int64_t i = 0; i < n; ++i) {
         const gemm_host_problem_t &q = probs[i];
         if (q.M == 0 || q.N == 0) continue;
-        const int b = int(i & 1);
+        const int b = int(i % kBatchSlots);
         const size_t es = size_t(elem_bytes(q.dtype));
         const size_t a_bytes = size_t(q.M) * size_t(q.K) * es, b_bytes = size_t(q.N) * size_t(q.K) * es;
         const size_t c_bytes = size_t(q.M) * size_t(q.N) * 2;
         char *dA = static_cast<char *>(h->d_slot[b]);
         char *dB = dA + round_up(a_bytes);
         char *dC = dB + round_up(b_bytes);
-        // slot b is free once the copy-out of the GEMM that used it two steps ago is done
-        if (i >= 2 && cudaStreamWaitEvent(h->s_h2d, h->ev_free[b], 0) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+        // slot b is free once the copy-out of the GEMM that used it kBatchSlots steps ago is done
+        if (i >= kBatchSlots && cudaStreamWaitEvent(h->s_h2d, h->ev_free[b], 0) != cudaSuccess)
+            return cuda_fail(cudaErrorUnknown);
         if ((a_bytes && cudaMemcpyAsync(dA, q.A, a_bytes, cudaMemcpyHostToDevice, h->s_h2d) != cudaSuccess)
             || (b_bytes && cudaMemcpyAsync(dB, q.B, b_bytes, cudaMemcpyHostToDevice, h->s_h2d) != cudaSuccess)
             || cudaEventRecord(h->ev_in[b], h->s_h2d) != cudaSuccess || cudaStreamWaitEvent(cs, h->ev_in[b], 0) != cudaSuccess)
@@ -510,7 +511,7 @@ gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *pr
             return cuda_fail(cudaErrorUnknown);
     }
     // the caller's stream continues after the last copy-out
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < kBatchSlots; ++b)
         if (cudaStreamWaitEvent(cs, h->ev_free[b], 0) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
     gemm_status_t st = read_status(h, cs, nullptr);
     return first_error != GEMM_OK ? first_error : st;
@@ -579,7 +580,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
     cudaFree(h->d_host_bufs);
     cudaFree(h->d_ws_partial);
     cudaFree(h->d_ws_sync);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBatchSlots; ++b) {
         cudaFree(h->d_slot[b]);
         if (h->ev_in[b]) cudaEventDestroy(h->ev_in[b]);
         if (h->ev_comp[b]) cudaEventDestroy(h->ev_comp[b]);
