@@ -468,11 +468,59 @@ def extra_configs(pts, dev, stream):
         finally:
             pts.gemm_destroy(hs[1])
         out["concurrent_" + pa.name + "+" + pb.name] = conc
+        out["half_occupied"] = half_occupied(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
     out["note"] = ("library's CTA group per GEMM (pairs from 128 k-blocks per tile); median of back-to-back "
                    "launches; inputs generated on the GPU from seeded generators (parity for these shapes is in "
                    "the tests)")
+    return out
+
+
+def half_occupied(pts, dev, stream, reps=6):
+    """SM availability that differs from the static assumption: a long GEMM
+    (one 128x256 tile per CTA on half the SMs, K=32768, about 0.2 ms) starts
+    first on one stream, then the measured GEMM (5120x5120x4096) on another.
+    A static grid sized to the whole GPU leaves half of its CTAs, and their
+    tiles, waiting for the occupier to finish; CLC lets the resident CTAs take
+    those tiles over."""
+    half = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+    occ = wl.Problem(f"occupier_{half * 128}x256x32768", half * 128, 256, 32768, wl.BF16, "normal_sqrtk", 7200)
+    main = wl.Problem("bf16_5120x5120x4096", 5120, 5120, 4096, wl.BF16, "normal_sqrtk", 7201)
+    io = device_inputs(occ, 7200)
+    im = device_inputs(main, 7201)
+    Co = torch.empty(occ.M, occ.N, dtype=torch.bfloat16, device="cuda")
+    Cm = torch.empty(main.M, main.N, dtype=torch.bfloat16, device="cuda")
+    ho = pts.gemm_create(dev, pts.make_opts(cta_group=1, split=1))   # one CTA per tile, no slicing
+    hm = pts.gemm_create(dev, pts.make_opts(cta_group=1))
+    s_occ = torch.cuda.Stream()
+    out = {}
+    try:
+        for si, name in enumerate(SCHED_NAMES):
+            times = []
+            for rep in range(reps):
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s_occ)
+                stream.wait_event(e0)
+                pts.gemm_run(ho, occ.M, occ.N, occ.K, io[0], io[1], Co, occ.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0,
+                             s_occ)
+                t_launch = time.perf_counter()
+                while time.perf_counter() - t_launch < 25e-6:   # let the occupier's CTAs become resident
+                    pass
+                pts.gemm_run(hm, main.M, main.N, main.K, im[0], im[1], Cm, main.dtype, si, 1.0, 1.0, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if rep >= 2:
+                    times.append(e0.elapsed_time(e1))
+            if pts.gemm_check(hm, stream)[0] != 0 or pts.gemm_check(ho, s_occ)[0] != 0:
+                raise RuntimeError("device error in the half-occupied run")
+            out[name] = {"main_done_ms": round(statistics.median(times), 4)}
+    finally:
+        pts.gemm_destroy(ho)
+        pts.gemm_destroy(hm)
+    out["note"] = (f"time from the occupier's start ({occ.name}, {half} CTAs, one wave) to the end of the "
+                   f"measured GEMM ({main.name}, single CTAs), launched 25 us after the occupier")
     return out
 
 
