@@ -39,8 +39,9 @@ UNIT = "TFLOP/s"
 WORKLOAD = ("fp16 GEMM M=N=4096, K=128..4096 step 128 (32 GEMMs per step), A,B ~ N(0,1)/sqrt(K), "
             "fp32 accumulate, fp16 C, row-major A, column-major B")
 SCHED_NAMES = ["nonpersistent", "static", "clc"]
-TILE_DESC = {0: "128x256x64 per CTA; single CTAs (tcgen05 cta_group::1) for every GEMM of this sweep "
-                "(the library pairs CTAs only from 128 k-blocks per tile)",
+TILE_DESC = {0: "128x256x64 per CTA; the library's CTA group per GEMM: single CTAs (tcgen05 cta_group::1) "
+                "below 16 k-blocks per tile (K < 1024), CTA pairs (one 256x256 cta_group::2 MMA sharing B) "
+                "from there",
              1: "128x256x64 per CTA (tcgen05 cta_group::1)",
              2: "128x256x64 per CTA; CTA pairs run one 256x256 tcgen05 cta_group::2 MMA and share B"}
 HEADLINE = "static"
@@ -342,6 +343,8 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
     hbm = peak_value(peaks, "hbm_gbs", "hbm_GBs")
     head = per_sched.get(HEADLINE) or next(iter(per_sched.values()))
     traffic, launch = profile_traffic()
+    if args.cta_group != 0 or args.epilogue != 0:
+        traffic, launch = None, None   # the capture was taken with the library's defaults
     achieved = head["value"] / world
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": UNIT,
                 "frac": round(achieved / tensor_peak, 4) if tensor_peak else None,
@@ -471,7 +474,7 @@ def extra_configs(pts, dev, stream):
         out["half_occupied"] = half_occupied(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
-    out["note"] = ("library's CTA group per GEMM (pairs from 128 k-blocks per tile); median of back-to-back "
+    out["note"] = ("library's CTA group per GEMM (pairs from 16 k-blocks per tile); median of back-to-back "
                    "launches; inputs generated on the GPU from seeded generators (parity for these shapes is in "
                    "the tests)")
     return out
@@ -606,7 +609,7 @@ def main():
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
-                    help="0 = the library's choice per GEMM (single CTAs below 128 k-blocks per tile)")
+                    help="0 = the library's choice per GEMM (single CTAs below 16 k-blocks per tile)")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],
                     help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

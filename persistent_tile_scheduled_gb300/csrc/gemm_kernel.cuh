@@ -168,8 +168,11 @@ struct WaitCtl {
     uint64_t timeout_ns;
     int32_t *status;
 
+    // Record a failure and tell this CTA (and its peer) to stop.  Called by
+    // every lane of a converged warp, it acts once: in lane 0.
     __device__ void fail(int32_t where) const
     {
+        if (lane_id() != 0) return;
         if (atomicCAS(status, 0, DEV_ERR_TIMEOUT) == 0) {
             status[1] = where;
             status[2] = static_cast<int32_t>(blockIdx.x);
@@ -195,6 +198,17 @@ struct WaitCtl {
                 }
             }
         }
+    }
+
+    // The same for a whole converged warp: every lane waits (each wait is
+    // bounded, so every lane reaches the vote) and all get one answer, so
+    // the warp never splits on a wait's outcome.
+    __device__ bool wait_all(uint32_t bar, uint32_t parity, int32_t where) const
+    {
+        const bool mine = wait(bar, parity, where);
+        const bool all = __all_sync(0xffffffffu, mine);
+        if (!all && mine && lane_id() == 0 && !ld_shared_u32(abort_addr)) fail(where);
+        return all;
     }
 
     // Bounded wait used only while shutting down after an error: ignores the
@@ -311,159 +325,174 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work-id broadcast ring -------------------------------------------
     // Slot r holds the id of work item i (i % kRing == r), or -1 = no more.
+    // Both are called by whole converged warps (producer, MMA) or by lane 0
+    // of an epilogue warp; the slot write and the arrivals happen in lane 0.
+    const uint32_t one = lane == 0 ? 1u : 0u;
     auto publish = [&](int i, int w) -> bool {
         const int slot = i % kRing;
-        if (i >= kRing && !ctl.wait(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
+        if (i >= kRing && !ctl.wait_all(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
             return false;
-        st_shared_u32(ring_w0 + 4 * slot, static_cast<uint32_t>(w));
-        if constexpr (CG == 2) {
-            st_cluster_u32(mapa(ring_w0 + 4 * slot, 1u), static_cast<uint32_t>(w));
-            mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
+        if (lane == 0) {
+            st_shared_u32(ring_w0 + 4 * slot, static_cast<uint32_t>(w));
+            if constexpr (CG == 2) {
+                st_cluster_u32(mapa(ring_w0 + 4 * slot, 1u), static_cast<uint32_t>(w));
+                mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
+            }
+            mbar_arrive(ring_full0 + 8 * slot);
         }
-        mbar_arrive(ring_full0 + 8 * slot);
+        __syncwarp();
         return true;
     };
-    auto ring_read = [&](int i, int &w) -> bool {
+    auto ring_read = [&](int i, int &w, bool whole_warp) -> bool {
         const int slot = i % kRing;
-        if (!ctl.wait(ring_full0 + 8 * slot, (i / kRing) & 1, WHERE_RING_FULL)) return false;
+        const uint32_t par = (i / kRing) & 1;
+        if (!(whole_warp ? ctl.wait_all(ring_full0 + 8 * slot, par, WHERE_RING_FULL)
+                         : ctl.wait(ring_full0 + 8 * slot, par, WHERE_RING_FULL)))
+            return false;
         w = static_cast<int>(ld_shared_u32(ring_w0 + 4 * slot));
         if (CG == 2 && !leader)
-            mbar_arrive_cluster(mapa(ring_empty0 + 8 * slot, 0u));
+            mbar_arrive_cluster_if(one, mapa(ring_empty0 + 8 * slot, 0u));
         else
-            mbar_arrive(ring_empty0 + 8 * slot);
+            mbar_arrive_if(one, ring_empty0 + 8 * slot);
         return true;
     };
 
     if (warp == 0) {
         // =========================== producer / scheduler ======================
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            bool ok = true;
-            auto load_tile = [&](const WorkTile &t) -> bool {
-                const int ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
-                const int yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
-                const CUtensorMap *mb = t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
-                const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
-                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if (!ctl.wait(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
-                    const int x = kb * KELEMS;
-                    const uint32_t fb = full0 + 8 * stage;
-                    // test hook: announce the stage's bytes but never load them,
-                    // so the MMA warp's bounded wait on this stage runs out
-                    const bool skip = (p.debug_flags & DBG_FAULT_SKIP_TMA) && issued == p.fault_arg;
-                    if constexpr (CG == 1) {
-                        mbar_arrive_expect_tx(fb, tx);
-                        if (!skip) {
-                            tma_load_2d(sA + stage * SA, &tmA, fb, x, ya);
-                            tma_load_2d(sB + stage * SB, mb, fb, x, yb);
-                        }
-                    } else {
-                        if (leader) mbar_arrive_expect_tx(fb, tx);
-                        const uint32_t fbc = mapa(fb, 0u);
-                        if (!skip) {
-                            tma_load_2d_pair(sA + stage * SA, &tmA, fbc, x, ya);
-                            tma_load_2d_pair(sB + stage * SB, mb, fbc, x, yb);
-                        }
-                    }
-                    // keep the k-block prefetch_kb ahead of this one on its way into
-                    // L2, so that a stage rarely waits on an HBM miss
-                    const int kp = kb + p.prefetch_kb;
-                    if (p.prefetch_kb > 0 && kp < t.kb_end) {
-                        tma_prefetch_2d(&tmA, kp * KELEMS, ya);
-                        tma_prefetch_2d(mb, kp * KELEMS, yb);
-                    }
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        // All 32 lanes run this loop in step (every branch below is uniform
+        // across the warp); lane 0 issues the loads and the CLC requests.
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        auto load_tile = [&](const WorkTile &t) -> bool {
+            const int ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
+            const int yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
+            const CUtensorMap *mb = t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
+            const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
+            for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+                if (!ctl.wait_all(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
+                const int x = kb * KELEMS;
+                const uint32_t fb = full0 + 8 * stage;
+                // test hook: announce the stage's bytes but never load them,
+                // so the MMA warp's bounded wait on this stage runs out
+                const bool skip = (p.debug_flags & DBG_FAULT_SKIP_TMA) && issued == p.fault_arg;
+                const uint32_t go = skip ? 0u : one;
+                if constexpr (CG == 1) {
+                    mbar_arrive_expect_tx_if(one, fb, tx);
+                    tma_load_2d(go, sA + stage * SA, &tmA, fb, x, ya);
+                    tma_load_2d(go, sB + stage * SB, mb, fb, x, yb);
+                } else {
+                    mbar_arrive_expect_tx_if(leader ? one : 0u, fb, tx);
+                    const uint32_t fbc = mapa(fb, 0u);
+                    tma_load_2d_pair(go, sA + stage * SA, &tmA, fbc, x, ya);
+                    tma_load_2d_pair(go, sB + stage * SB, mb, fbc, x, yb);
                 }
-                return true;
-            };
+                // keep the k-block prefetch_kb ahead of this one on its way into
+                // L2, so that a stage rarely waits on an HBM miss
+                const int kp = kb + p.prefetch_kb;
+                if (p.prefetch_kb > 0 && kp < t.kb_end) {
+                    tma_prefetch_2d(one, &tmA, kp * KELEMS, ya);
+                    tma_prefetch_2d(one, mb, kp * KELEMS, yb);
+                }
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            return true;
+        };
 
-            bool clc_pending = false;
-            if (leader) {
-                int w = cluster_id < p.num_work ? cluster_id : -1;
-                bool may_request = p.sched == SCHED_CLC;
-                uint32_t clc_phase = 0;
-                ok = publish(0, w);
-                for (int i = 0; ok && w >= 0; ++i) {
-                    if (may_request) {
-                        if ((p.debug_flags & DBG_CLC_STOP_AT) && i == p.fault_arg) {
-                            may_request = false;   // behave as if this request had failed
-                        } else {
+        bool clc_pending = false;
+        if (leader) {
+            int w = cluster_id < p.num_work ? cluster_id : -1;
+            bool may_request = p.sched == SCHED_CLC;
+            uint32_t clc_phase = 0;
+            ok = publish(0, w);
+            for (int i = 0; ok && w >= 0; ++i) {
+                if (may_request) {
+                    if ((p.debug_flags & DBG_CLC_STOP_AT) && i == p.fault_arg) {
+                        may_request = false;   // behave as if this request had failed
+                    } else {
+                        if (lane == 0) {
                             fence_proxy_async_smem();   // earlier reads of the slot before the async write
                             mbar_arrive_expect_tx(clc_bar, 16);
                             clc_try_cancel(clc_resp, clc_bar);
-                            clc_pending = true;
                         }
+                        __syncwarp();
+                        clc_pending = true;
                     }
-                    if (!load_tile(work_tile(w, p))) {
-                        ok = false;
-                        break;
-                    }
-                    int next = -1;
-                    if (p.sched == SCHED_STATIC) {
-                        next = (w + num_clusters < p.num_work) ? w + num_clusters : -1;
-                    } else if (clc_pending) {
-                        if (!ctl.wait(clc_bar, clc_phase, WHERE_CLC)) {
-                            ok = false;
-                            break;
-                        }
-                        clc_phase ^= 1u;
-                        clc_pending = false;
-                        uint32_t x;
-                        if (clc_decode(clc_resp, x)) {
-                            next = static_cast<int>(x / CG);
-                            if (next >= p.num_work) {   // cannot happen for a well-formed grid
-                                ctl.fail(WHERE_BAD_TILE);
-                                next = -1;
-                            }
-                        } else {
-                            may_request = false;   // a failed request is never repeated
-                        }
-                    }
-                    ok = publish(i + 1, next);
-                    w = next;
                 }
-                if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
-            } else {
-                for (int i = 0;; ++i) {
-                    int w;
-                    if (!ring_read(i, w)) {
+                if (!load_tile(work_tile(w, p))) {
+                    ok = false;
+                    break;
+                }
+                int next = -1;
+                if (p.sched == SCHED_STATIC) {
+                    next = (w + num_clusters < p.num_work) ? w + num_clusters : -1;
+                } else if (clc_pending) {
+                    if (!ctl.wait_all(clc_bar, clc_phase, WHERE_CLC)) {
                         ok = false;
                         break;
                     }
-                    if (w < 0) break;
-                    if (!load_tile(work_tile(w, p))) {
-                        ok = false;
-                        break;
+                    clc_phase ^= 1u;
+                    clc_pending = false;
+                    // only lane 0 reads the response slot (it alone re-arms it)
+                    uint32_t x = 0, got = 0;
+                    if (lane == 0) got = clc_decode(clc_resp, x) ? 1u : 0u;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    x = __shfl_sync(0xffffffffu, x, 0);
+                    if (got) {
+                        next = static_cast<int>(x / CG);
+                        if (next >= p.num_work) {   // cannot happen for a well-formed grid
+                            ctl.fail(WHERE_BAD_TILE);
+                            next = -1;
+                        }
+                    } else {
+                        may_request = false;   // a failed request is never repeated
                     }
+                }
+                ok = publish(i + 1, next);
+                w = next;
+            }
+            if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
+        } else {
+            for (int i = 0;; ++i) {
+                int w;
+                if (!ring_read(i, w, true)) {
+                    ok = false;
+                    break;
+                }
+                if (w < 0) break;
+                if (!load_tile(work_tile(w, p))) {
+                    ok = false;
+                    break;
                 }
             }
-            if (!ok) {
-                // Stopped early: let the loads already issued land before the
-                // CTA can exit (bounded; the pair's loads signal the leader).
-                if (CG == 1 || leader) {
-                    const long long n = issued < S ? issued : S;
-                    for (long long j = 0; j < n; ++j) {
-                        const long long g = issued - 1 - j;
-                        ctl.drain(full0 + 8 * static_cast<int>(g % S), static_cast<uint32_t>((g / S) & 1),
-                                  10000000ull);
-                    }
-                } else {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (globaltimer_ns() - t0 < 1000000ull) {
-                    }
+        }
+        if (!ok) {
+            // Stopped early: let the loads already issued land before the
+            // CTA can exit (bounded; the pair's loads signal the leader).
+            if (CG == 1 || leader) {
+                const long long n = issued < S ? issued : S;
+                for (long long j = 0; j < n; ++j) {
+                    const long long g = issued - 1 - j;
+                    ctl.drain(full0 + 8 * static_cast<int>(g % S), static_cast<uint32_t>((g / S) & 1),
+                              10000000ull);
+                }
+            } else {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================================ MMA ==================================
-        if (lane == 0 && leader) {
+        // The leader CTA's whole warp runs the loop in step; lane 0 issues
+        // the MMAs and the commits (a commit tracks the MMAs of its own lane).
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -472,16 +501,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t last_phase = 0;
             for (int i = 0;; ++i) {
                 int w;
-                if (!ring_read(i, w) || w < 0) break;
-                if (!ctl.wait(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
+                if (!ring_read(i, w, true) || w < 0) break;
+                if (!ctl.wait_all(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
-                if (p.records != nullptr) p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
+                if (p.records != nullptr && lane == 0)
+                    p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
                 const WorkTile t = work_tile(w, p);
                 const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if (!ctl.wait(full0 + 8 * stage, phase, WHERE_FULL)) {
+                    if (!ctl.wait_all(full0 + 8 * stage, phase, WHERE_FULL)) {
                         ok = false;
                         break;
                     }
@@ -490,8 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd = smem_desc_sw128(sB + stage * SB);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                        umma<KIND, CG>(d, ad + 2 * k, bd + 2 * k, idesc, (kb != t.kb_begin || k != 0) ? 1u : 0u);
-                    umma_commit<CG>(empty0 + 8 * stage, 0x3);
+                        umma<KIND, CG>(one, d, ad + 2 * k, bd + 2 * k, idesc,
+                                       (kb != t.kb_begin || k != 0) ? 1u : 0u);
+                    umma_commit<CG>(one, empty0 + 8 * stage, 0x3);
                     last_stage = stage;
                     last_phase = phase;
                     if (++stage == S) {
@@ -500,14 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit<CG>(acc_full0 + 8 * acc, 0x3);
+                umma_commit<CG>(one, acc_full0 + 8 * acc, 0x3);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // the last stage release is the last asynchronous arrival this
-            // thread caused; see it land before the CTA may exit
+            // warp caused; see it land before the CTA may exit
             if (last_stage >= 0) ctl.drain(empty0 + 8 * last_stage, last_phase, 10000000ull);
         }
         __syncwarp();
@@ -522,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0;; ++i) {
             int w = 0;
             int ok = 1;
-            if (lane == 0) ok = ring_read(i, w) ? 1 : 0;
+            if (lane == 0) ok = ring_read(i, w, false) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             w = __shfl_sync(0xffffffffu, w, 0);
             if (!ok || w < 0) break;

@@ -105,12 +105,14 @@ inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
     return best;
 }
 
-// CTA group when the caller leaves it to the library: CTA pairs (cta_group 2)
-// halve the B traffic per SM but cost a few microseconds per launch in pair
-// synchronisation; measured on GB300 they pay off from about 128 k-blocks per
-// tile (bf16 8192^3: 625 vs 655 us), single CTAs win below (fp16 4096^2 at
-// K = 128..4096: 6 us per launch).
-constexpr int kPairMinKb = 128;
+// CTA group when the caller leaves it to the library.  CTA pairs (cta_group
+// 2) load a third less per SM for the same MMA work, so their mainloop runs
+// faster under full load (fp16 4096^2 x 4096: 0.318 vs 0.326 us per k-block,
+// 90 vs 94 us per launch), but a pair costs a few microseconds more to start
+// and finish.  Measured over the fp16 4096^2 K sweep on GB300, pairs pay off
+// from about 16 k-blocks per tile; single CTAs win below (K = 256: 21.5 vs
+// 28.3 us).
+constexpr int kPairMinKb = 16;
 
 inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
 

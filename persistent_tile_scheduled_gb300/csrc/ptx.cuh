@@ -83,6 +83,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Predicated forms (`_if`, or a leading `pred` argument below): the
+// instruction executes only in the lanes whose `pred` is non-zero.  The
+// producer and MMA warps run their loops with all 32 lanes in step and issue
+// from lane 0 through these, so the per-k-block path has no divergent branch.
+__device__ __forceinline__ void mbar_arrive_if(uint32_t pred, uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q mbarrier.arrive.shared::cta.b64 _, [%1];\n\t}" ::"r"(pred), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster_if(uint32_t pred, uint32_t cluster_bar)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%1];\n\t}" ::"r"(pred),
+                 "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t pred, uint32_t bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(pred), "r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Non-blocking probe of phase `parity`; cluster-scope acquire so that arrivals
 // and async writes made by the peer CTA of a pair are visible afterwards.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
@@ -106,31 +133,36 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 
 // 2-D tiled load into this CTA's shared memory; completion is signalled on
 // `bar` (shared::cta address of this CTA).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                            int y)
+// (Only in the lanes where `pred` is non-zero.)
+__device__ __forceinline__ void tma_load_2d(uint32_t pred, uint32_t dst, const void *tmap, uint32_t bar,
+                                            int x, int y)
 {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-                 "l"(tmap), "r"(bar), "r"(x), "r"(y)
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%1], [%2, {%4, %5}], [%3];\n\t}" ::"r"(pred),
+                 "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y)
                  : "memory");
 }
 
 // Same for a CTA pair: data lands in this CTA's shared memory, completion is
 // signalled on `cluster_bar`, which may live in the peer CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t pred, uint32_t dst, const void *tmap,
                                                  uint32_t cluster_bar, int x, int y)
 {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 ".cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-                 "l"(tmap), "r"(cluster_bar), "r"(x), "r"(y)
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".cta_group::2 [%1], [%2, {%4, %5}], [%3];\n\t}" ::"r"(pred),
+                 "r"(dst), "l"(tmap), "r"(cluster_bar), "r"(x), "r"(y)
                  : "memory");
 }
 
 // Bring a 2-D box of the tensor into L2 (no shared-memory destination, no
 // completion); out-of-bounds parts are ignored.
-__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y)
+__device__ __forceinline__ void tma_prefetch_2d(uint32_t pred, const void *tmap, int x, int y)
 {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%1, {%2, %3}];\n\t}" ::"r"(pred),
+                 "l"(tmap), "r"(x), "r"(y)
                  : "memory");
 }
 
@@ -200,15 +232,16 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // D[tmem] (+)= A[smem] . B[smem]^T, both operands K-major.  KIND 0/1: f16/bf16
-// (kind::f16), KIND 2: e4m3 (kind::f8f6f4).
+// (kind::f16), KIND 2: e4m3 (kind::f8f6f4).  Issued only where `pred` is
+// non-zero (one lane of the MMA warp).
 template <int KIND, int CG>
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                     uint32_t accumulate)
+__device__ __forceinline__ void umma(uint32_t pred, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                     uint32_t idesc, uint32_t accumulate)
 {
-#define PTS_UMMA(K_, G_)                                                                          \
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                                \
-                 "tcgen05.mma.cta_group::" #G_ ".kind::" #K_ " [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem), \
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)                              \
+#define PTS_UMMA(K_, G_)                                                                              \
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"         \
+                 "@q tcgen05.mma.cta_group::" #G_ ".kind::" #K_ " [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem), \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(pred)                       \
                  : "memory")
     if constexpr (KIND == 2 && CG == 1) PTS_UMMA(f8f6f4, 1);
     else if constexpr (KIND == 2 && CG == 2) PTS_UMMA(f8f6f4, 2);
@@ -220,16 +253,20 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
 // far has completed.  CG 2: the arrival is multicast to the barrier at the
 // same offset in each CTA of `cta_mask`.
+// Only where `pred` is non-zero: the lane that issued the MMAs.
 template <int CG>
-__device__ __forceinline__ void umma_commit(uint32_t bar, uint16_t cta_mask)
+__device__ __forceinline__ void umma_commit(uint32_t pred, uint32_t bar, uint16_t cta_mask)
 {
     if constexpr (CG == 1)
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                     "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}"
+                     ::"r"(pred), "r"(bar)
                      : "memory");
     else
-        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                     " [%0], %1;" ::"r"(bar),
-                     "h"(cta_mask)
+        asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                     "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                     " [%1], %2;\n\t}" ::"r"(pred),
+                     "r"(bar), "h"(cta_mask)
                      : "memory");
 }
 
