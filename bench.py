@@ -275,7 +275,7 @@ def run_ours(args, dist, rank, world, local):
 
     per_sched = {}
     clocks = None
-    h = pts.gemm_create(local, pts.make_opts(cta_group=args.cta_group, epilogue=args.epilogue))
+    h = pts.gemm_create(local, pts.make_opts(cta_group=args.cta_group, epilogue=args.epilogue, split_k=args.split_k))
     try:
         for si, name in enumerate(SCHED_NAMES):
             if name not in args.scheds:
@@ -343,7 +343,7 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
     hbm = peak_value(peaks, "hbm_gbs", "hbm_GBs")
     head = per_sched.get(HEADLINE) or next(iter(per_sched.values()))
     traffic, launch = profile_traffic()
-    if args.cta_group != 0 or args.epilogue != 0:
+    if args.cta_group != 0 or args.epilogue != 0 or args.split_k != 0:
         traffic, launch = None, None   # the capture was taken with the library's defaults
     achieved = head["value"] / world
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": UNIT,
@@ -369,7 +369,7 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded N(0,1)/sqrt(K), rounded to fp16)",
         "config": {"workload": WORKLOAD, "tile": TILE_DESC[args.cta_group], "group_size_m": 8,
-                   "cta_group": args.cta_group, "sched": HEADLINE,
+                   "cta_group": args.cta_group, "split_k": args.split_k, "sched": HEADLINE,
                    "launch": "CUDA graph of the 32 gemm_run launches per step" if args.graph else "eager",
                    "l2": "no flush: one step's 32 distinct A,B,C sets (2.1 GB) exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
@@ -610,6 +610,8 @@ def main():
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
                     help="0 = the library's choice per GEMM (single CTAs below 16 k-blocks per tile)")
+    ap.add_argument("--split-k", type=int, default=0, choices=[0, 1, -1],
+                    help="stream-K share of the last waves: 0 = the library's choice, 1 = always, -1 = never")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],
                     help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

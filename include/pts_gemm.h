@@ -77,17 +77,19 @@ typedef enum {
 
 typedef struct gemm_opts {
     int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair);
-                                       0 = per call: pairs when a tile has >= 128 k-blocks */
+                                       0 = per call: pairs when a tile has >= 16 k-blocks */
     int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
     int stages;                     /* shared-memory ring depth; 0 = the most that fits */
     int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */
     unsigned debug_flags;           /* GEMM_DEBUG_* */
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
-    int split;                      /* 0 = automatic; 1 = never cut tiles; 2..4 = cut EVERY
-                                       tile into that many parts (testing) */
-    int split_k;                    /* with split >= 2: 0 = column slices (2 or 4),
-                                       1 = K ranges with a fixup (2, 3 or 4) */
+    int split;                      /* column slices: 0 = automatic (a problem smaller than one
+                                       wave); 1 = never; 2 or 4 = cut EVERY tile into that many
+                                       column slices (testing) */
+    int split_k;                    /* stream-K share of the last waves: 0 = automatic (when it
+                                       saves time), 1 = whenever the tiles leave a partial last
+                                       wave, -1 = never.  Not with split 2 or 4. */
     int prefetch;                   /* L2 prefetch of the operands, in k-blocks ahead of the
                                        loads (<= 64); 0 = default (none), -1 = none */
     int overlap_launch;             /* 0 = default (on): a launch may start while the previous
@@ -99,25 +101,35 @@ typedef struct gemm_opts {
                                        outputs straight from registers */
 } gemm_opts_t;
 
-/* Work items.  Output tiles are visited in grouped order; a work item is one
- * tile, except that some tiles are cut into `split` parts, one work item per
- * part: work ids below full_work are whole tiles, work id
- * full_work + split*j + h is part h of the (full_work + j)-th tile.
- *   - A problem smaller than one wave of resident clusters is cut into
- *     column slices of 256/split columns (split 2 or 4), so more SMs work.
- *   - Otherwise the tiles of the last partial wave may be cut into K ranges
- *     (split 2..4): parts 0..split-2 get part_kb k-blocks each (part h covers
- *     h*part_kb .. (h+1)*part_kb), the last part the rest.  Every part
- *     accumulates its range; each part but the last to finish writes its fp32
- *     partial to a workspace the handle owns, and the last adds them and
- *     stores C.  The shorter first parts publish their partials while the last
- *     part still computes, and the wave ends well before a whole tile would.
+/* Work items.  Output tiles are numbered in grouped order (GROUP_SIZE_M tile-
+ * rows per group, walked column by column).  The schedulers hand out units;
+ * a unit is one or more work items, each computed in one accumulator:
+ *   - Whole tiles: unit u = work item u = tile u.
+ *   - Column slices (split 2 or 4; a problem smaller than one wave of
+ *     resident clusters, so that more SMs take part): unit u = work item u =
+ *     columns (u % split) * 256/split .. +256/split of tile u / split.
+ *   - Stream-K share (split_k): with T tiles on G resident clusters and a
+ *     partial last wave (R = T mod G > 0), the first R + G tiles form a region
+ *     of L = (R + G) * num_kb k-blocks, taken tile by tile.  Unit c < G gets
+ *     k-blocks floor(c*L/G) .. floor((c+1)*L/G) - 1 of it: one work item
+ *     ("piece", record slot 3c + j) for each tile j = 0, 1, 2 the range
+ *     touches, run last tile first (so every unit starts at k-block 0 of a
+ *     tile).  A tile split between two units is summed by a fixup: the
+ *     piece that finishes accumulating first writes its fp32 partial to a
+ *     workspace the handle owns, the other adds it and stores C.  Units
+ *     G, G+1, ... (record slots 3G, 3G+1, ...) are the remaining tiles,
+ *     whole.  Every cluster then does the same number of k-blocks to within
+ *     one, instead of some clusters running a whole extra tile in the last
+ *     wave; the region comes first so that the fixup overlaps whole tiles.
  * Cutting tiles changes which CTA computes what, never the result beyond the
- * fp32 summation order.
+ * fp32 summation order.  The pages on persistent tile scheduling hand out
+ * whole tiles only; the column slices and the stream-K share are this
+ * library's additions for the tail of a grid.
  *
  * Per-work-item record written when GEMM_DEBUG_RECORDS is set (work-id order). */
 typedef struct gemm_tile_record {
-    uint32_t visits;   /* CTAs that stored this item; exactly cta_group when coverage is exact */
+    uint32_t visits;   /* CTAs that stored this item; exactly cta_group when coverage is exact
+                          (0 for the unused slots of a stream-K unit with fewer than 3 pieces) */
     uint32_t tile;     /* tile index tm * tiles_n + tn of the item */
     uint32_t n_off;    /* first column of the item within its tile */
     uint32_t n_len;    /* columns of the item (256, 128 or 64) */
@@ -141,11 +153,12 @@ typedef struct gemm_launch_info {
     int max_active_clusters;        /* resident clusters the device holds for this kernel */
     int smem_bytes;                 /* dynamic shared memory per CTA */
     int threads;                    /* threads per CTA */
-    int split;                      /* parts per tile past full_work (1 = none) */
-    int split_k;                    /* parts are K ranges (1) or column slices (0) */
-    int64_t full_work;              /* work ids below this are whole tiles */
-    int64_t part_kb;                /* K ranges: k-blocks of every part but the last */
-    int64_t work_items;             /* work items in total */
+    int split;                      /* column slices per tile (1 = none, 2 or 4) */
+    int split_k;                    /* 1 when the stream-K share is used */
+    int64_t sk_tiles;               /* tiles of the stream-K region (0 = none) */
+    int64_t sk_units;               /* units sharing it (the resident clusters G) */
+    int64_t work_items;             /* work items = record slots (gemm_read_debug's n_work) */
+    int64_t units;                  /* units the schedulers hand out */
 } gemm_launch_info_t;
 
 typedef struct gemm_ctx *gemm_handle_t;

@@ -50,39 +50,77 @@ def swizzle(w: int, Tm: int, Tn: int, group_m: int) -> Tuple[int, int]:
     return first_m + r % rows_here, r // rows_here
 
 
-def work_items(T: int, full_work: int, split: int, tile_n: int = 256, split_k: bool = False,
-               num_kb: int = 1, part_kb: Optional[int] = None) -> List[Tuple[int, int, int, int, int, int]]:
-    """(work id, grouped-order tile index, first column, columns, first k-block,
-    end k-block) of every work item.
+Item = Tuple[int, int, int, int, int, int]
 
-    Work ids below ``full_work`` are whole tiles.  Each remaining tile is cut
-    into ``split`` parts: work id ``full_work + split*j + h`` is part h of
-    tile ``full_work + j``.  Parts are column slices of ``tile_n / split``
-    columns, or (``split_k``) k-block ranges whose partial sums add up to the
-    tile: parts 0..split-2 take ``part_kb`` k-blocks each (default
-    ``num_kb // split``), part h covering ``[h*part_kb, (h+1)*part_kb)``, and
-    the last part takes the rest, up to ``num_kb``.  Cutting
-    tiles changes how the output is partitioned among CTAs, never what is
-    computed ("Neither mode creates additional independent work at the tail
-    of a grid": cutting is a separate device for the last wave).
+
+def work_units(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_tiles: int = 0,
+               sk_units: int = 0) -> List[List[Item]]:
+    """The units the schedulers hand out, in unit order, each the list of its
+    work items ``(record slot, grouped-order tile, first column, columns,
+    first k-block, end k-block)``.
+
+    * Whole tiles (``split == 1``, no stream-K region): unit u is tile u.
+    * Column slices (``split`` 2 or 4): unit u is columns
+      ``(u % split) * tile_n/split`` onwards of tile ``u // split``.
+    * Stream-K share (``sk_units = U > 0``): the first ``sk_tiles`` tiles form
+      a region of ``L = sk_tiles * num_kb`` k-blocks, tile after tile.  Unit
+      ``c < U`` owns the k-blocks ``x`` with ``floor(c*L/U) <= x <
+      floor((c+1)*L/U)``; it has one item per tile those k-blocks fall in
+      (record slot ``3c + j`` for its j-th such tile) and runs them last tile
+      first.  Units ``U, U+1, ...`` are the remaining tiles, whole (record
+      slots ``3U, 3U+1, ...``).  Items are listed in the order a unit runs
+      them.
+
+    The pages hand out whole tiles only; the column slices and the stream-K
+    share are the library's additions for the tail of a grid (they change
+    which cluster computes what, never the result beyond fp32 summation
+    order).  The stream-K partition is written out here k-block by k-block,
+    not by the closed forms the kernel uses, so the two can be compared.
     """
-    if not (0 <= full_work <= T and 1 <= split <= 4):
-        raise ValueError((T, full_work, split))
-    if not split_k and split not in (1, 2, 4):
-        raise ValueError(split)
-    a = (num_kb // split) if part_kb is None else part_kb
-    if split_k and not (1 <= a and (split - 1) * a < num_kb):
-        raise ValueError((num_kb, split, a))
-    out = [(w, w, 0, tile_n, 0, num_kb) for w in range(full_work)]
-    for j in range(T - full_work):
-        for h in range(split):
-            w = full_work + split * j + h
-            if split_k:
-                out.append((w, full_work + j, 0, tile_n, h * a, num_kb if h == split - 1 else (h + 1) * a))
-            else:
-                step = tile_n // split
-                out.append((w, full_work + j, h * step, step, 0, num_kb))
-    return out
+    if split not in (1, 2, 4) or (split > 1 and sk_units):
+        raise ValueError((split, sk_units))
+    units: List[List[Item]] = []
+    if sk_units:
+        U, L = sk_units, sk_tiles * num_kb
+        if not (0 < sk_tiles <= T and U <= L):
+            raise ValueError((T, sk_tiles, U, num_kb))
+        starts = [c * L // U for c in range(U)]
+        owner = []
+        for x in range(L):
+            c = 0
+            while c + 1 < U and starts[c + 1] <= x:
+                c += 1
+            owner.append(c)
+        for c in range(U):
+            mine = [x for x in range(L) if owner[x] == c]
+            items = []
+            for j, t in enumerate(sorted({x // num_kb for x in mine})):
+                ks = [x - t * num_kb for x in mine if x // num_kb == t]
+                items.append((3 * c + j, t, 0, tile_n, min(ks), max(ks) + 1))
+            units.append(items[::-1])
+        for j in range(T - sk_tiles):
+            units.append([(3 * U + j, sk_tiles + j, 0, tile_n, 0, num_kb)])
+    elif split > 1:
+        step = tile_n // split
+        for u in range(T * split):
+            units.append([(u, u // split, (u % split) * step, step, 0, num_kb)])
+    else:
+        for u in range(T):
+            units.append([(u, u, 0, tile_n, 0, num_kb)])
+    return units
+
+
+def work_items(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_tiles: int = 0,
+               sk_units: int = 0) -> List[Item]:
+    """Every work item of :func:`work_units`, in unit order."""
+    return [it for u in work_units(T, split, tile_n, num_kb, sk_tiles, sk_units) for it in u]
+
+
+def record_slots(T: int, split: int = 1, sk_tiles: int = 0, sk_units: int = 0) -> int:
+    """Record slots of a launch: three per stream-K unit plus one per other unit."""
+    if sk_units:
+        return 3 * sk_units + T - sk_tiles
+    return T * split
 
 
 def static_grid(T: int, max_clusters: int) -> int:

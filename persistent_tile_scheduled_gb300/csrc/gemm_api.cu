@@ -41,11 +41,12 @@ struct gemm_ctx {
     int64_t records_cap = 0;                  // in work items
     int64_t last_work = 0;
     int last_cta_group = 1;
+    int64_t last_sk_tiles = 0, last_sk_units = 0, last_num_kb = 0;   // which record slots are pieces
     void *d_host_bufs = nullptr;              // gemm_run_host staging (A | B | C)
     size_t host_bufs_cap = 0;
-    float *d_ws_partial = nullptr;            // K-split fixup workspace
+    float *d_ws_partial = nullptr;            // stream-K fixup workspace
     size_t ws_partial_cap = 0;                // bytes
-    uint32_t *d_ws_sync = nullptr;            // K-split claim counters / ready flags
+    uint32_t *d_ws_sync = nullptr;            // stream-K claim counters / ready flags
     size_t ws_sync_cap = 0;                   // bytes
     uint32_t epoch = 0;                       // launch number for the fixup counters (1 .. 2^29 - 1)
     // gemm_run_host_batch: staging slots (A | B | C each), copy streams and events
@@ -109,12 +110,12 @@ pts::KernelOps ops_for(int kind, int cg) { return cg == 2 ? pts::kernel_ops_cg2(
 struct Plan {
     int cg, stages, smem;
     int64_t tiles_m, tiles_n, tiles;
-    int split;               // parts per tile past full_work
-    int split_k;             // parts are K ranges (1) or column slices (0)
-    int64_t part_kb;         // K ranges: k-blocks of every part but the last
+    int split;               // column slices per tile (1, 2 or 4)
+    int64_t sk_tiles;        // stream-K region: its tiles and units (0 = none)
+    int64_t sk_units;
     int64_t num_kb;          // k-blocks per whole tile
-    int64_t full_work;       // work ids below this are whole tiles
-    int64_t work;            // work items in total
+    int64_t units;           // work ids the schedulers hand out
+    int64_t work;            // work items (record slots)
     int64_t grid_ctas;
     int max_active_clusters;
 };
@@ -137,7 +138,6 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
     pl.num_kb = (K + kelems - 1) / kelems;
     pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb);
-    pl.part_kb = 0;
     int stages = h->opts.stages;
     if (stages == 0) {   // the deepest ring that fits
         stages = pts::kMaxStages;
@@ -169,27 +169,17 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
     int64_t resident = pl.max_active_clusters;
     if (h->opts.max_clusters > 0 && h->opts.max_clusters < resident) resident = h->opts.max_clusters;
-    if (h->opts.split > 0) {   // forced (testing): every tile is cut the same way
-        pl.split = h->opts.split;
-        pl.split_k = h->opts.split_k;
-        if (pl.split_k && pl.split > pl.num_kb) pl.split = static_cast<int>(pl.num_kb < 1 ? 1 : pl.num_kb);
-        if (pl.split == 1) pl.split_k = 0;
-        pl.full_work = pl.split == 1 ? pl.tiles : 0;
-        pl.part_kb = pl.split_k ? pl.num_kb / pl.split : 0;   // even parts, the last takes the remainder
-    } else if ((pl.split = pts::choose_split(pl.tiles, resident)) > 1) {
-        pl.split_k = 0;                                   // a sub-wave problem: column slices
-        pl.full_work = 0;
-    } else if ((pl.split = pts::choose_split_k(pl.tiles, resident, pl.num_kb)) > 1) {
-        pl.split_k = 1;                                   // the last partial wave: K ranges + fixup
-        pl.full_work = pl.tiles - pl.tiles % resident;
-        pl.part_kb = pts::split_part_kb(pl.num_kb, pl.split);
-    } else {
-        pl.split_k = 0;
-        pl.full_work = pl.tiles;
-    }
-    pl.work = pl.full_work + pl.split * (pl.tiles - pl.full_work);
-    int64_t clusters = pl.work;
-    if (sched == GEMM_SCHED_STATIC) clusters = pl.work < resident ? pl.work : resident;
+    // column slices for a problem smaller than one wave (or forced, for testing)
+    pl.split = h->opts.split > 0 ? h->opts.split : pts::choose_split(pl.tiles, resident);
+    pl.sk_tiles = 0;
+    pl.sk_units = 0;
+    if (pl.split == 1 && (pl.sk_tiles = pts::choose_stream_k(pl.tiles, resident, pl.num_kb, h->opts.split_k)) > 0)
+        pl.sk_units = resident;
+    pl.units = pl.sk_units > 0 ? pl.sk_units + pl.tiles - pl.sk_tiles : pl.tiles * pl.split;
+    pl.work = pl.sk_units > 0 ? pts::kSkMaxPieces * pl.sk_units + pl.tiles - pl.sk_tiles : pl.units;
+    if (pl.work > (int64_t(1) << 31) - 1) return GEMM_ERR_INVALID_ARG;
+    int64_t clusters = pl.units;
+    if (sched == GEMM_SCHED_STATIC) clusters = pl.units < resident ? pl.units : resident;
     pl.grid_ctas = clusters * pl.cg;
     return GEMM_OK;
 }
@@ -216,10 +206,10 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     Plan pl;
     gemm_status_t st = make_plan(h, M, N, K, dtype, sched, pl);
     if (st != GEMM_OK) return st;
-    if (pl.split_k) {   // fixup workspace: partials of all parts but the last, and the sync words
-        const size_t split_tiles = size_t(pl.tiles - pl.full_work);
-        const size_t need_p = split_tiles * size_t(pl.split - 1) * pl.cg * pts::kPartialFloats * sizeof(float);
-        const size_t need_s = split_tiles * pl.cg * pts::kEpiWarps * 4 * sizeof(uint32_t);
+    if (pl.sk_units > 0) {   // fixup workspace: a partial slot and 4 sync words per (region tile, CTA, warp)
+        const size_t tiles = size_t(pl.sk_tiles);
+        const size_t need_p = tiles * size_t(pts::kSkMaxParts - 1) * pl.cg * pts::kPartialFloats * sizeof(float);
+        const size_t need_s = tiles * pl.cg * pts::kEpiWarps * 4 * sizeof(uint32_t);
         if (h->ws_partial_cap < need_p) {
             cudaFree(h->d_ws_partial);
             h->d_ws_partial = nullptr;
@@ -243,7 +233,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
     const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
-    const bool slices = pl.split > 1 && !pl.split_k;
+    const bool slices = pl.split > 1;
     CUtensorMap ma, mb0, mb_slice, mc;
     const CUtensorMap *m;
     if (!(m = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems))) return GEMM_ERR_CUDA;
@@ -270,13 +260,13 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.tiles_m = static_cast<int32_t>(pl.tiles_m);
     p.tiles_n = static_cast<int32_t>(pl.tiles_n);
     p.num_tiles = static_cast<int32_t>(pl.tiles);
-    p.full_work = static_cast<int32_t>(pl.full_work);
     p.split = pl.split;
-    p.split_k = pl.split_k;
-    p.part_kb = static_cast<int32_t>(pl.part_kb);
+    p.sk_tiles = static_cast<int32_t>(pl.sk_tiles);
+    p.sk_units = static_cast<int32_t>(pl.sk_units);
     p.epoch = h->epoch;
-    p.ws_partial = pl.split_k ? h->d_ws_partial : nullptr;
-    p.ws_sync = pl.split_k ? h->d_ws_sync : nullptr;
+    p.ws_partial = pl.sk_units > 0 ? h->d_ws_partial : nullptr;
+    p.ws_sync = pl.sk_units > 0 ? h->d_ws_sync : nullptr;
+    p.num_units = static_cast<int32_t>(pl.units);
     p.num_work = static_cast<int32_t>(pl.work);
     p.group_m = h->opts.group_size_m;
     p.sched = static_cast<int32_t>(sched);
@@ -305,6 +295,9 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     }
     h->last_work = pl.work;
     h->last_cta_group = pl.cg;
+    h->last_sk_tiles = pl.sk_tiles;
+    h->last_sk_units = pl.sk_units;
+    h->last_num_kb = pl.num_kb;
 
     cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(ma, mb, mc, p, static_cast<int>(pl.grid_ctas),
                                                                    pl.smem, stream, h->opts.overlap_launch >= 0);
@@ -354,7 +347,8 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
         return GEMM_ERR_INVALID_ARG;
     if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)
         return GEMM_ERR_INVALID_ARG;
-    if (o.split < 0 || o.split > 4 || (!o.split_k && o.split == 3) || (o.split_k != 0 && o.split_k != 1))
+    if (o.split < 0 || o.split > 4 || o.split == 3 || o.split_k < -1 || o.split_k > 1
+        || (o.split > 1 && o.split_k == 1))
         return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
         return GEMM_ERR_INVALID_ARG;
@@ -537,10 +531,11 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     info->tiles_n = pl.tiles_n;
     info->tiles = pl.tiles;
     info->split = pl.split;
-    info->split_k = pl.split_k;
-    info->part_kb = pl.part_kb;
-    info->full_work = pl.full_work;
+    info->split_k = pl.sk_units > 0 ? 1 : 0;
+    info->sk_tiles = pl.sk_tiles;
+    info->sk_units = pl.sk_units;
     info->work_items = pl.work;
+    info->units = pl.units;
     info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;
     info->max_active_clusters = pl.max_active_clusters;
     info->smem_bytes = pl.smem;
@@ -566,8 +561,15 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
                                  cudaMemcpyDeviceToHost) != cudaSuccess)
         return cuda_fail(cudaErrorUnknown);
     if (st != GEMM_OK) return st;
-    for (int64_t t = 0; t < n_work; ++t)
-        if (records[t].visits != static_cast<uint32_t>(h->last_cta_group)) return GEMM_ERR_COVERAGE;
+    // every work item stored by each CTA of its cluster once; the unused
+    // record slots of stream-K units with fewer than 3 pieces never
+    const int64_t U = h->last_sk_units, L = h->last_sk_tiles * h->last_num_kb;
+    for (int64_t t = 0; t < n_work; ++t) {
+        bool used = true;
+        if (U > 0 && t < pts::kSkMaxPieces * U)
+            used = t % pts::kSkMaxPieces < pts::sk_pieces(t / pts::kSkMaxPieces, L, U, h->last_num_kb);
+        if (records[t].visits != (used ? static_cast<uint32_t>(h->last_cta_group) : 0u)) return GEMM_ERR_COVERAGE;
+    }
     return GEMM_OK;
 }
 

@@ -44,7 +44,7 @@ enum : int32_t {
     WHERE_RING_FULL = 6,    // a role waiting for the next tile id
     WHERE_CLC = 7,          // scheduler waiting for a CLC response
     WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
-    WHERE_FIXUP = 9,        // the last part of a K-split tile waiting for the other parts
+    WHERE_FIXUP = 9,        // the second piece of a cut tile waiting for the first's partial
 };
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
@@ -99,50 +99,84 @@ __device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int gro
     tn = r / rows;
 }
 
-// A work item: tile (tm, tn), its column slice [n_off, n_off + n_len) and its
-// k-block range [kb_begin, kb_end).  Work ids below full_work are whole tiles
-// in grouped order.  Each later tile is cut into `split` parts: column slices
-// (split_k == 0), or K ranges (split_k == 1: part_kb k-blocks for each part
-// but the last, which takes the rest) whose fp32 partials are summed by the
-// part that finishes last; `ks` is then the index of the split tile among
-// them (else -1).
+// A work item: tile (tm, tn), its column slice [n_off, n_off + n_len), its
+// k-block range [kb_begin, kb_end), and for a stream-K piece of a tile that
+// is cut in two, the tile's index in the stream-K region (ks; else -1).
 struct WorkTile {
     int tm, tn, n_off, n_len, kb_begin, kb_end, ks;
 };
 
-__device__ __forceinline__ WorkTile work_tile(int w, const GemmParams &p)
+// Work item (record slot) s.
+//  - With a stream-K region (sk_units = U > 0): s < 3U is piece s % 3 of
+//    unit s / 3, the part of the unit's k-block range inside its (s % 3)-th
+//    tile (only slots of pieces that exist are handed out); s >= 3U is the
+//    whole tile sk_tiles + s - 3U.
+//  - With column slices (split 2 or 4): slice s % split of tile s / split.
+//  - Otherwise the whole tile s.
+// Tiles are numbered in grouped order (tile_of).
+__device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
 {
     WorkTile t;
-    int tile = w;
+    int tile = s;
     t.n_off = 0;
     t.n_len = kTileN;
     t.kb_begin = 0;
     t.kb_end = p.num_kb;
     t.ks = -1;
-    if (w >= p.full_work) {
-        const int q = w - p.full_work;
-        const int j = q / p.split;
-        const int h = q - j * p.split;
-        tile = p.full_work + j;
-        if (p.split_k) {
-            t.kb_begin = h * p.part_kb;
-            t.kb_end = h == p.split - 1 ? p.num_kb : (h + 1) * p.part_kb;
-            t.ks = j;
+    if (p.sk_units > 0) {
+        const int U = p.sk_units;
+        if (s < kSkMaxPieces * U) {
+            const int64_t L = static_cast<int64_t>(p.sk_tiles) * p.num_kb;
+            const int c = s / kSkMaxPieces;
+            const int j = s - c * kSkMaxPieces;
+            const int64_t a = sk_unit_begin(c, L, U), b = sk_unit_begin(c + 1, L, U);
+            tile = static_cast<int>(a / p.num_kb) + j;
+            const int64_t t0 = static_cast<int64_t>(tile) * p.num_kb;
+            t.kb_begin = static_cast<int>((a > t0 ? a : t0) - t0);
+            t.kb_end = static_cast<int>((b < t0 + p.num_kb ? b : t0 + p.num_kb) - t0);
+            // cut in two when its first and last k-blocks belong to different units
+            if (sk_unit_of(t0, L, U) != sk_unit_of(t0 + p.num_kb - 1, L, U)) t.ks = tile;
         } else {
-            t.n_len = kTileN / p.split;
-            t.n_off = h * t.n_len;
+            tile = p.sk_tiles + (s - kSkMaxPieces * U);
         }
+    } else if (p.split > 1) {
+        tile = s / p.split;
+        const int h = s - tile * p.split;
+        t.n_len = kTileN / p.split;
+        t.n_off = h * t.n_len;
     }
     tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
     return t;
 }
 
-// K-split fixup, per (split tile, CTA of the pair, epilogue warp): the warp's
+// Pieces of unit u (the work ids the schedulers hand out): 1 to 3 for a
+// stream-K unit (one per tile its k-block range touches), else 1.
+__device__ __forceinline__ int unit_items(int u, const GemmParams &p)
+{
+    if (p.sk_units > 0 && u < p.sk_units)
+        return sk_pieces(u, static_cast<int64_t>(p.sk_tiles) * p.num_kb, p.sk_units, p.num_kb);
+    return 1;
+}
+
+// Work item that unit u (of `pieces` pieces) runs j-th.  A stream-K unit
+// runs its pieces last tile first: every unit then starts at k-block 0 of a
+// tile, as whole tiles do, so clusters that share A rows or B columns read
+// the same k-blocks at the start and find them in L2.  (Its first piece also
+// finishes early and its last late, so the early piece of a cut tile writes
+// the partial and the late one, followed by whole tiles, adds it.)
+__device__ __forceinline__ int unit_item(int u, int j, int pieces, const GemmParams &p)
+{
+    if (p.sk_units > 0)
+        return u < p.sk_units ? u * kSkMaxPieces + (pieces - 1 - j) : kSkMaxPieces * p.sk_units + (u - p.sk_units);
+    return u;
+}
+
+// Stream-K fixup, per (cut tile, CTA of the pair, epilogue warp): the warp's
 // 32 rows of the tile are reduced independently of the other warps, so no
 // warp ever waits for another warp of its CTA.  Sync words: [0] claim counter
-// (epoch << 3 | parts claimed), [1..3] ready flags of partial slots 0..2
-// (each holds the epoch of the launch that filled the slot).  A unit has
-// split - 1 partial slots.
+// (epoch << 3 | pieces claimed), [1] ready flag of the partial slot (the
+// epoch of the launch that filled it).  A cut tile has kSkMaxParts pieces and
+// kSkMaxParts - 1 partial slots.
 // Partial slot layout: float4 index (chunk * 16 + g) * 32 + lane, so every
 // warp-wide access is 512 contiguous bytes.
 constexpr int kPartialFloat4PerWarp = kEpiRowsPerWarp * kTileN / 4;
@@ -304,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (!p.split_k && p.split == 2) prefetch_tmap(&tmB2);
-        if (!p.split_k && p.split == 4) prefetch_tmap(&tmB4);
+        if (p.split == 2) prefetch_tmap(&tmB2);
+        if (p.split == 4) prefetch_tmap(&tmB4);
         prefetch_tmap(&tmC);
     }
     if (warp == 1) {
@@ -317,17 +351,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CG == 2) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    const uint32_t one = lane == 0 ? 1u : 0u;
+
+    // Rows of this CTA's A and B boxes for work item t, and the B map of the
+    // item's column width.
+    auto boxes = [&](const WorkTile &t, int &ya, int &yb) -> const CUtensorMap * {
+        ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
+        yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
+        return t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
+    };
+
     // Back-to-back launches: the set-up above may overlap the end of the
-    // previous grid in the stream; nothing touches global memory before it
-    // has completed (A and B may be its outputs, C its inputs).
+    // previous grid in the stream; no load or store of A, B or C happens
+    // before it has completed (A and B may be its outputs, C its inputs).
+    // Before waiting, the producer asks L2 for the first k-blocks of its
+    // cluster's first unit: an L2 prefetch brings lines into the coherent L2
+    // and changes nothing any load returns, so the first stages then fill
+    // from L2 instead of HBM.
     pdl_launch_dependents();
+    if (warp == 0 && cluster_id < p.num_units) {
+        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), p);
+        int ya, yb;
+        const CUtensorMap *mb = boxes(t0, ya, yb);
+        const int kb_end = t0.kb_end < t0.kb_begin + S ? t0.kb_end : t0.kb_begin + S;
+        for (int kb = t0.kb_begin; kb < kb_end; ++kb) {
+            tma_prefetch_2d(one, &tmA, kb * KELEMS, ya);
+            tma_prefetch_2d(one, mb, kb * KELEMS, yb);
+        }
+    }
     pdl_wait();
 
     // ---- work-id broadcast ring -------------------------------------------
     // Slot r holds the id of work item i (i % kRing == r), or -1 = no more.
     // Both are called by whole converged warps (producer, MMA) or by lane 0
     // of an epilogue warp; the slot write and the arrivals happen in lane 0.
-    const uint32_t one = lane == 0 ? 1u : 0u;
     auto publish = [&](int i, int w) -> bool {
         const int slot = i % kRing;
         if (i >= kRing && !ctl.wait_all(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
@@ -366,9 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long issued = 0;
         bool ok = true;
         auto load_tile = [&](const WorkTile &t) -> bool {
-            const int ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
-            const int yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
-            const CUtensorMap *mb = t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
+            int ya, yb;
+            const CUtensorMap *mb = boxes(t, ya, yb);
             const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
             for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                 if (!ctl.wait_all(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
@@ -406,13 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         bool clc_pending = false;
         if (leader) {
-            int w = cluster_id < p.num_work ? cluster_id : -1;
+            // Units come from the scheduler; each is published as its pieces.
+            int u = cluster_id < p.num_units ? cluster_id : -1;
             bool may_request = p.sched == SCHED_CLC;
             uint32_t clc_phase = 0;
-            ok = publish(0, w);
-            for (int i = 0; ok && w >= 0; ++i) {
+            int i = 0;   // ring slot sequence
+            for (int n = 0; ok && u >= 0; ++n) {
                 if (may_request) {
-                    if ((p.debug_flags & DBG_CLC_STOP_AT) && i == p.fault_arg) {
+                    if ((p.debug_flags & DBG_CLC_STOP_AT) && n == p.fault_arg) {
                         may_request = false;   // behave as if this request had failed
                     } else {
                         if (lane == 0) {
@@ -424,13 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         clc_pending = true;
                     }
                 }
-                if (!load_tile(work_tile(w, p))) {
-                    ok = false;
-                    break;
+                const int pieces = unit_items(u, p);
+                for (int j = 0; ok && j < pieces; ++j) {
+                    const int w = unit_item(u, j, pieces, p);
+                    ok = publish(i++, w) && load_tile(work_tile(w, p));
                 }
+                if (!ok) break;
                 int next = -1;
                 if (p.sched == SCHED_STATIC) {
-                    next = (w + num_clusters < p.num_work) ? w + num_clusters : -1;
+                    next = (u + num_clusters < p.num_units) ? u + num_clusters : -1;
                 } else if (clc_pending) {
                     if (!ctl.wait_all(clc_bar, clc_phase, WHERE_CLC)) {
                         ok = false;
@@ -445,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x = __shfl_sync(0xffffffffu, x, 0);
                     if (got) {
                         next = static_cast<int>(x / CG);
-                        if (next >= p.num_work) {   // cannot happen for a well-formed grid
+                        if (next >= p.num_units) {   // cannot happen for a well-formed grid
                             ctl.fail(WHERE_BAD_TILE);
                             next = -1;
                         }
@@ -453,9 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         may_request = false;   // a failed request is never repeated
                     }
                 }
-                ok = publish(i + 1, next);
-                w = next;
+                u = next;
             }
+            if (ok) ok = publish(i, -1);
             if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
         } else {
             for (int i = 0;; ++i) {
@@ -582,11 +641,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * kTileN);
             const int chunks = t.n_len / kEpiChunkCols;
 
-            // K-split tile: claim a part number for this warp's rows.  Parts
-            // other than the last claimed write their fp32 partial and raise a
-            // flag; the last claimed waits for those flags (every such part has
-            // already claimed, so it is running and never waits itself) and
-            // adds the partials before storing C.
+            // A stream-K piece of a cut tile: claim a part number for this
+            // warp's rows.  Pieces other than the last claimed write their fp32
+            // partial and raise a flag; the last claimed waits for those flags
+            // (every such piece has already claimed, so it is past its
+            // mainloop and never waits itself) and adds the partials before
+            // storing C.
+            constexpr int nparts = kSkMaxParts;   // pieces of a cut tile
             int part = -1;
             uint32_t *sync = nullptr;
             const float4 *partials = nullptr;
@@ -594,13 +655,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long unit = (static_cast<long long>(t.ks) * CG + rank) * kEpiWarps + q;
                 sync = p.ws_sync + unit * 4;
                 partials = reinterpret_cast<const float4 *>(p.ws_partial)
-                           + unit * (p.split - 1) * kPartialFloat4PerWarp;
+                           + unit * (nparts - 1) * kPartialFloat4PerWarp;
                 uint32_t mine = 0;
                 if (lane == 0) mine = fixup_claim(sync, p.epoch);
                 part = static_cast<int>(__shfl_sync(0xffffffffu, mine, 0));
-                if (part == p.split - 1) {
+                if (part == nparts - 1) {
                     if (lane == 0) {
-                        for (int sl = 0; sl < p.split - 1; ++sl) {
+                        for (int sl = 0; sl < nparts - 1; ++sl) {
                             const uint64_t t0 = globaltimer_ns();
                             while (ld_acquire_gpu(sync + 1 + sl) != p.epoch) {
                                 if (ld_shared_u32(abort_flag)) break;
@@ -612,10 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    for (int sl = 0; sl < p.split - 1; ++sl) (void)ld_acquire_gpu(sync + 1 + sl);
+                    for (int sl = 0; sl < nparts - 1; ++sl) (void)ld_acquire_gpu(sync + 1 + sl);
                 }
             }
-            const bool write_partial = part >= 0 && part < p.split - 1;
+            const bool write_partial = part >= 0 && part < nparts - 1;
             // Chunks of 64 columns, software-pipelined: the TMEM loads of
             // chunk c+1 are in flight while chunk c is converted and stored.
             uint32_t ra0[32], ra1[32], rb0[32], rb1[32];
@@ -656,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3])));
                     continue;
                 }
-                if (part > 0) {   // the last part of a K-split tile: add the others' partials
+                if (part > 0) {   // the last piece of a cut tile: add the others' partials
                     for (int sl = 0; sl < part; ++sl) {
                         // issue 8 loads before using any, so their latencies overlap
                         const float4 *src = partials + sl * kPartialFloat4PerWarp + c * 16 * 32 + lane;
@@ -731,7 +792,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (lane == 0) bulk_wait_all();
+        // the last stores must have read their staging buffers before the
+        // CTA's shared memory goes away (their writes to C complete with the
+        // grid)
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
     }
 

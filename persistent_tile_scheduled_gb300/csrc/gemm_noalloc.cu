@@ -160,9 +160,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int ci = cta_group - 1;
     const int64_t resident = s->clusters[dtype][ci];
-    const int split = pts::choose_split(tiles, resident);
-    const int64_t full_work = split == 1 ? tiles : tiles - tiles % resident;
-    const int64_t work = full_work + split * (tiles - full_work);
+    const int split = pts::choose_split(tiles, resident);   // column slices below one wave
+    const int64_t work = tiles * split;
     if (work > GEMM_NOALLOC_MAX_WORK_ITEMS) return GEMM_ERR_INVALID_ARG;   // one scratch record per item
 
     // status words and the records of this problem's work items must start at zero
@@ -188,12 +187,13 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.num_tiles = static_cast<int32_t>(tiles);
-    p.full_work = static_cast<int32_t>(full_work);
     p.split = split;
-    p.split_k = 0;   // no K-split fixup: its workspace would not fit a modest static array
+    p.sk_tiles = 0;   // no stream-K share: its fixup workspace would not fit a modest static array
+    p.sk_units = 0;
     p.epoch = 1;
     p.ws_partial = nullptr;
     p.ws_sync = nullptr;
+    p.num_units = static_cast<int32_t>(work);
     p.num_work = static_cast<int32_t>(work);
     p.group_m = 8;
     p.sched = static_cast<int32_t>(sched);

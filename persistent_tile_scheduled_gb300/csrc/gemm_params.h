@@ -29,8 +29,8 @@ enum : int32_t { SCHED_NONPERSISTENT = 0, SCHED_STATIC = 1, SCHED_CLC = 2 };
 enum : int32_t { DEV_ERR_TIMEOUT = 1 };
 enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u, DBG_FAULT_SKIP_TMA = 0x4u };
 
-// Debug record of one work item (a tile, or a column slice of a tile of the
-// last partial wave).  Times are the low 32 bits of %globaltimer (ns): the
+// Debug record of one work item (a whole tile, a column slice of one, or a
+// stream-K piece: one tile's share of a unit's k-blocks).  Times are the low 32 bits of %globaltimer (ns): the
 // MMA thread starting the item, the epilogue seeing its accumulator complete,
 // the epilogue having issued the item's last store.
 struct TileRecord {
@@ -42,12 +42,12 @@ struct GemmParams {
     int32_t num_kb;             // k-blocks per tile
     int32_t tiles_m, tiles_n;   // output tiles (per cluster) along M and N
     int32_t num_tiles;
-    int32_t full_work;          // work ids below this are whole tiles
-    int32_t split;              // each later tile is cut into `split` parts (1..4)
-    int32_t split_k;            // 0: parts are column slices; 1: parts are K ranges, reduced in a fixup
-    int32_t part_kb;            // K ranges: k-blocks of each part but the last (the last gets the rest)
+    int32_t split;              // column slices per tile (1, 2 or 4); 1 when sk_units > 0
+    int32_t sk_tiles;           // tiles of the stream-K region (the first in grouped order); 0 = none
+    int32_t sk_units;           // units sharing the region's k-blocks (0 = none)
     uint32_t epoch;             // launch number (29 bits, never 0) tagging the fixup counters and flags
-    int32_t num_work;           // full_work + split * (num_tiles - full_work)
+    int32_t num_units;          // work ids the schedulers hand out
+    int32_t num_work;           // work items (record slots); see work_tile()
     int32_t group_m;            // GROUP_SIZE_M
     int32_t sched;
     int32_t stages;
@@ -59,50 +59,58 @@ struct GemmParams {
     int32_t fault_arg;
     uint64_t timeout_ns;
     int32_t *status;            // 4 ints
-    float *ws_partial;          // K-split partial accumulators (fixup workspace), or null
-    uint32_t *ws_sync;          // K-split claim counters and ready flags, 4 words per (tile, CTA)
+    float *ws_partial;          // stream-K partial accumulators (fixup workspace), or null
+    uint32_t *ws_sync;          // stream-K claim counters and ready flags, 4 words per (tile, CTA, warp)
     TileRecord *records;        // num_work entries, or null
 };
 
-// Floats of one K-split partial: a CTA's 128 x 256 fp32 accumulator.
+// Floats of one stream-K partial: a CTA's 128 x 256 fp32 accumulator.
 constexpr int kPartialFloats = kRowsPerCta * kTileN;
 
-// K-split of the last partial wave.  The first split-1 parts get `part_kb`
-// k-blocks each and the last part the rest, which is longer: the first parts
-// finish early and write their fp32 partials while the last one still
-// computes, so it finds them ready.  Measured on GB300 a writer needs about
-// kFixupWriteKb k-blocks' time to publish its partial and the last part about
-// kFixupReadKb per partial it adds.
-constexpr int kFixupWriteKb = 13;
-constexpr int kFixupReadKb = 5;
+// Stream-K share of the last waves.  With T tiles on G resident clusters and
+// R = T mod G > 0, the first R + G tiles (grouped order) form the stream-K
+// region of L = (R + G) * num_kb k-blocks, taken tile by tile.  Unit c
+// (0 <= c < G) gets the k-blocks [floor(c*L/G), floor((c+1)*L/G)), at least
+// num_kb and fewer than 2*num_kb of them: up to 3 pieces (one per tile it
+// touches), and every tile gets at most 2 pieces.  The remaining tiles are
+// whole-tile units G, G+1, ...  Every cluster then does the same number of
+// k-blocks to within one, instead of some clusters running a whole extra
+// tile in the last wave.  A tile cut in two is summed by a fixup: the piece
+// whose accumulation ends first writes its fp32 partial, the other adds it
+// and stores C.  The stream-K units come first, so that fixup overlaps the
+// whole tiles that follow.
+constexpr int kSkMaxPieces = 3;      // record slots per stream-K unit
+constexpr int kSkMaxParts = 2;       // pieces per tile
+// Use it when it saves each cluster at least this many k-blocks' time.  The
+// price, measured on GB300 (fp16 4096^2, CTA pairs): a writer's epilogue
+// takes ~4 us longer than a plain one and a reader's ~4.5 us; hidden behind a
+// long next tile, but not behind a short one.  Break-even was near 14
+// k-blocks saved (K = 2048: 20 saved, 2 us gained; K = 4096: 40 saved, 7 us).
+constexpr int kSkMinSavedKb = 16;
 
-inline int64_t split_part_kb(int64_t num_kb, int split)
+__host__ __device__ inline int64_t sk_unit_begin(int64_t c, int64_t L, int64_t U) { return c * L / U; }
+
+// The unit whose range holds k-block x of the region: the largest c with
+// floor(c*L/U) <= x.
+__host__ __device__ inline int64_t sk_unit_of(int64_t x, int64_t L, int64_t U) { return ((x + 1) * U - 1) / L; }
+
+// Pieces of stream-K unit c: one per tile its k-block range touches (1..3).
+__host__ __device__ inline int sk_pieces(int64_t c, int64_t L, int64_t U, int64_t num_kb)
 {
-    const int64_t a = (num_kb - kFixupWriteKb) / split;
-    return a < 1 ? 1 : a;
+    const int64_t a = sk_unit_begin(c, L, U), b = sk_unit_begin(c + 1, L, U);
+    return static_cast<int>((b - 1) / num_kb - a / num_kb + 1);
 }
 
-// K parts per leftover tile of the last partial wave (1 = no split): the
-// count that shortens the wave most, if it saves more than 8 k-blocks' time;
-// parts must fit the idle clusters of that wave.
-inline int choose_split_k(int64_t tiles, int64_t resident, int64_t num_kb)
+// Tiles in the stream-K region for `tiles` tiles of `num_kb` k-blocks on
+// `resident` clusters (0 = do not use it).  force: 1 = whenever the last wave
+// is partial, -1 = never, 0 = when it saves kSkMinSavedKb k-blocks' time.
+inline int64_t choose_stream_k(int64_t tiles, int64_t resident, int64_t num_kb, int force)
 {
+    if (force < 0 || num_kb < 1 || resident < 1 || tiles < resident) return 0;
     const int64_t r = tiles % resident;
-    if (tiles < resident || r == 0) return 1;
-    int best = 1;
-    int64_t best_tail = num_kb - 8;
-    for (int s = 2; s <= 4; ++s) {
-        if (s * r > resident || s > num_kb) break;
-        const int64_t a = split_part_kb(num_kb, s);
-        const int64_t last = num_kb - (s - 1) * a;
-        const int64_t writers_done = a + kFixupWriteKb;
-        const int64_t tail = (last > writers_done ? last : writers_done) + kFixupReadKb * (s - 1);
-        if (tail < best_tail) {
-            best_tail = tail;
-            best = s;
-        }
-    }
-    return best;
+    if (r == 0) return 0;
+    if (force == 0 && num_kb * (resident - r) < kSkMinSavedKb * resident) return 0;
+    return r + resident;
 }
 
 // CTA group when the caller leaves it to the library.  CTA pairs (cta_group

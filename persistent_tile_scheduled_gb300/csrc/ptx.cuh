@@ -181,11 +181,6 @@ __device__ __forceinline__ void bulk_wait_read()
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Order this thread's generic-proxy shared-memory accesses with later
 // async-proxy accesses (TMA store source, CLC response slot reuse).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -252,8 +247,8 @@ __device__ __forceinline__ void umma(uint32_t pred, uint32_t d_tmem, uint64_t ad
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
 // far has completed.  CG 2: the arrival is multicast to the barrier at the
-// same offset in each CTA of `cta_mask`.
-// Only where `pred` is non-zero: the lane that issued the MMAs.
+// same offset in each CTA of `cta_mask`.  Only where `pred` is non-zero: the
+// lane that issued the MMAs.
 template <int CG>
 __device__ __forceinline__ void umma_commit(uint32_t pred, uint32_t bar, uint16_t cta_mask)
 {

@@ -46,8 +46,8 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("cta_group", ctypes.c_int), ("stages", ctypes.c_int), ("tiles_m", ctypes.c_int64),
                 ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64),
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
-                ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("full_work", ctypes.c_int64),
-                ("part_kb", ctypes.c_int64), ("work_items", ctypes.c_int64)]
+                ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("sk_tiles", ctypes.c_int64),
+                ("sk_units", ctypes.c_int64), ("work_items", ctypes.c_int64), ("units", ctypes.c_int64)]
 
 
 class gemm_host_problem_t(ctypes.Structure):

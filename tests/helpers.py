@@ -64,12 +64,17 @@ def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, see
 def check_records(records, info, sched: int, K: int, group_m: int = 8):
     """Per-work-item records against what the schedulers must do (bit-exact)."""
     T, Tm, Tn, cg = int(info.tiles), int(info.tiles_m), int(info.tiles_n), int(info.cta_group)
-    W, F, split = int(info.work_items), int(info.full_work), int(info.split)
+    W, split = int(info.work_items), int(info.split)
     G = int(info.grid_ctas) // cg
     num_kb = -(-int(K) // int(info.tile_k))
-    items = osched.work_items(T, F, split, split_k=bool(info.split_k), num_kb=num_kb,
-                              part_kb=int(info.part_kb) if info.split_k else None)
-    assert len(items) == W
+    units = osched.work_units(T, split, num_kb=num_kb, sk_tiles=int(info.sk_tiles), sk_units=int(info.sk_units))
+    assert len(units) == int(info.units)
+    assert W == osched.record_slots(T, split, int(info.sk_tiles), int(info.sk_units))
+    items = [it for u in units for it in u]
+    used = {it[0] for it in items}
+    for w in range(W):
+        if w not in used:
+            assert records[w].visits == 0, f"unused record slot {w} was stored"
     cover = {}
     for w, t_order, n_off, n_len, k0, k1 in items:
         r = records[w]
@@ -77,28 +82,38 @@ def check_records(records, info, sched: int, K: int, group_m: int = 8):
         tm, tn = osched.swizzle(t_order, Tm, Tn, group_m)
         assert (r.tile, r.n_off, r.n_len) == (tm * Tn + tn, n_off, n_len), w
         assert (r.kb_begin, r.kb_end) == (k0, k1), w
-        cover.setdefault(r.tile, []).append((r.kb_begin, r.kb_end, r.n_off, r.n_len))
+        cover.setdefault(r.tile, set())
+        cells = {(c, kb) for c in range(n_off, n_off + n_len, 64) for kb in range(k0, k1)}
+        assert not (cover[r.tile] & cells), f"tile {r.tile} computed twice"
+        cover[r.tile] |= cells
     # the items partition every tile (columns x k-blocks) exactly once
     assert sorted(cover) == list(range(T))
-    for t, parts in cover.items():
-        cells = sum((k1 - k0) * n for k0, k1, _, n in parts)
-        kb_total = max(k1 for _, k1, _, _ in parts)
-        assert cells == 256 * kb_total, t
-    by_work = {w: (records[w].owner, records[w].iter) for w in range(W)}
+    full = {(c, kb) for c in range(0, 256, 64) for kb in range(num_kb)}
+    assert all(cells == full for cells in cover.values())
+    by_work = {it[0]: (records[it[0]].owner, records[it[0]].iter) for it in items}
     if sched == pts.GEMM_SCHED_STATIC:
-        want = {w: (c, it) for w, c, it in osched.static_assignment(W, G)}
+        want = {}
+        for c in range(G):
+            it_no = 0
+            for u in range(c, len(units), G):
+                for it in units[u]:
+                    want[it[0]] = (c, it_no)
+                    it_no += 1
         assert by_work == want
     elif sched == pts.GEMM_SCHED_NONPERSISTENT:
-        want = {w: (c, it) for w, c, it in osched.nonpersistent_assignment(W)}
+        want = {it[0]: (u, j) for u, its in enumerate(units) for j, it in enumerate(its)}
         assert by_work == want
     else:
-        # CLC: a cluster's first item is its own id; its later items were
-        # cancelled clusters, each run exactly once; iterations are 0..n-1
+        # CLC: a unit runs on one cluster, its items back to back; a cluster's
+        # first unit is its own id; its later units were cancelled clusters,
+        # each run exactly once; every cluster's items count 0..n-1
         per_owner = {}
-        for w, (owner, it) in by_work.items():
-            if it == 0:
-                assert owner == w
-            per_owner.setdefault(owner, []).append(it)
+        for u, its in enumerate(units):
+            owner, it0 = by_work[its[0][0]]
+            assert [by_work[it[0]] for it in its] == [(owner, it0 + j) for j in range(len(its))], u
+            if it0 == 0:
+                assert owner == u
+            per_owner.setdefault(owner, []).extend(range(it0, it0 + len(its)))
         for owner, its in per_owner.items():
             assert sorted(its) == list(range(len(its))), owner
     return by_work

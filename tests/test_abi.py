@@ -77,6 +77,8 @@ def test_struct_layouts_match_the_header():
       printf("%zu %zu\n", sizeof(gemm_tile_record_t), offsetof(gemm_tile_record_t, smid));
       printf("%zu %zu %zu %zu\n", sizeof(gemm_launch_info_t), offsetof(gemm_launch_info_t, tiles_m),
              offsetof(gemm_launch_info_t, grid_ctas), offsetof(gemm_launch_info_t, threads));
+      printf("%zu %zu %zu\n", offsetof(gemm_launch_info_t, sk_tiles), offsetof(gemm_launch_info_t, work_items),
+             offsetof(gemm_launch_info_t, units));
       return 0;
     }
     """
@@ -91,7 +93,9 @@ def test_struct_layouts_match_the_header():
             g.gemm_opts_t.timeout_ns.offset,
             ctypes.sizeof(g.gemm_tile_record_t), g.gemm_tile_record_t.smid.offset,
             ctypes.sizeof(g.gemm_launch_info_t), g.gemm_launch_info_t.tiles_m.offset,
-            g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset]
+            g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset,
+            g.gemm_launch_info_t.sk_tiles.offset, g.gemm_launch_info_t.work_items.offset,
+            g.gemm_launch_info_t.units.offset]
     assert got == want
 
 

@@ -141,17 +141,26 @@ def test_forced_column_slices(cg, split, sched):
 
 
 @pytest.mark.parametrize("cg", [1, 2])
-@pytest.mark.parametrize("split", [2, 3, 4])
+@pytest.mark.parametrize("G", [3, 5])
 @pytest.mark.parametrize("sched", SCHEDS)
-def test_forced_k_split_with_fixup(cg, split, sched):
-    """Every tile cut into 2-4 K ranges; all but the last part to finish write
-    fp32 partials that the last one adds before storing C."""
-    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, split=split, split_k=1,
+def test_forced_stream_k_share(cg, G, sched):
+    """The last waves shared stream-K style on G clusters: each unit's k-block
+    range cut at tile boundaries into pieces; a tile split between two units
+    is summed by the fixup (the first piece to finish writes its fp32 partial,
+    the other adds it and stores C).  Ragged shapes, every dtype."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, split_k=1, max_clusters=G,
                                          debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
-        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3)]:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3),
+                              (1000, 1800, 2000, wl.BF16)]:
             dist = "normal" if dt == wl.E4M3 else "uniform"
-            x = wl.make_inputs(wl.Problem("ksplit", M, N, K, dt, dist, M + N + K + 10 * split))
+            x = wl.make_inputs(wl.Problem("streamk", M, N, K, dt, dist, M + N + K + 10 * G))
+            info = pts.gemm_query(h, M, N, K, dt, sched)
+            T = int(info.tiles)
+            assert info.split_k == (1 if T >= G and T % G else 0)
+            if info.split_k:
+                assert (info.sk_tiles, info.sk_units) == (T % G + G, G)
+                assert info.work_items == 3 * G + T - info.sk_tiles and info.units == G + T - info.sk_tiles
             for _ in range(2):      # twice: the claim counters of one launch must not leak into the next
                 _run_checked(h, x, sched)
     finally:
@@ -159,10 +168,11 @@ def test_forced_k_split_with_fixup(cg, split, sched):
 
 
 @pytest.mark.parametrize("cg", [1, 2])
-@pytest.mark.parametrize("split,split_k", [(1, 0), (2, 0), (2, 1)])
-def test_direct_store_epilogue(cg, split, split_k):
-    """The epilogue that stores C rows straight from registers (no TMA store)."""
-    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, epilogue=2, split=split, split_k=split_k,
+@pytest.mark.parametrize("split,split_k,G", [(1, -1, 0), (2, 0, 0), (1, 1, 5)])
+def test_direct_store_epilogue(cg, split, split_k, G):
+    """The epilogue that stores C rows straight from registers (no TMA store):
+    whole tiles, column slices, stream-K pieces."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, epilogue=2, split=split, split_k=split_k, max_clusters=G,
                                          debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
         for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3)]:
@@ -174,17 +184,23 @@ def test_direct_store_epilogue(cg, split, split_k):
         pts.gemm_destroy(h)
 
 
-def test_automatic_k_split_of_the_last_wave():
-    """A last partial wave that fits half a wave is cut along K when K is long."""
+def test_automatic_stream_k_share():
+    """A partial last wave is shared stream-K style when that saves time."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
         info = pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        G = int(info.max_active_clusters)
-        r = int(info.tiles) % G
-        if r and 2 * r <= G:
-            assert info.split_k == 1 and info.split >= 2 and info.full_work == info.tiles - r
-        info = pts.gemm_query(h, 4096, 4096, 1024, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.split == 1                       # 16 k-blocks: a fixup would cost more than it saves
+        G, T = int(info.max_active_clusters), int(info.tiles)
+        if T % G:
+            assert info.split_k == 1 and (info.sk_tiles, info.sk_units) == (T % G + G, G)
+        h1 = pts.gemm_create(0, pts.make_opts(cta_group=1))
+        try:
+            G1 = int(pts.gemm_query(h1, 4096, 4096, 128, pts.GEMM_F16, 1).max_active_clusters)
+            info = pts.gemm_query(h1, 4096, 4096, 128, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+            assert info.split_k == 0 and info.sk_tiles == 0   # 2 k-blocks: saves less than the fixup costs
+            info = pts.gemm_query(h1, 128 * G1, 256, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+            assert info.split_k == 0                    # whole waves: nothing to share
+        finally:
+            pts.gemm_destroy(h1)
         x = wl.make_inputs(wl.Problem("k8192", 4096, 4096, 8192, wl.F16, "normal_sqrtk", 77))
         for sched in SCHEDS:
             _run_checked(h, x, sched, full=False)
@@ -215,9 +231,9 @@ def test_automatic_slicing_of_sub_wave_problems():
     h = pts.gemm_create(0, pts.make_opts(cta_group=1))
     try:
         info = pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.split == 1 or info.split_k == 1        # past one wave: never column slices
+        assert info.split == 1                              # past one wave: never column slices
         info = pts.gemm_query(h, 512, 512, 512, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.tiles == 8 and info.split == 4 and info.full_work == 0 and info.work_items == 32
+        assert info.tiles == 8 and info.split == 4 and info.sk_tiles == 0 and info.work_items == 32
     finally:
         pts.gemm_destroy(h)
 

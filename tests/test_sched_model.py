@@ -105,38 +105,81 @@ def test_clc_replay_uneven_costs_cover_exactly_once():
 
 
 def test_work_items_hand_worked():
-    # 5 tiles of 8 k-blocks, 4 whole, the fifth cut in two: columns 0-127 and 128-255
-    assert sm.work_items(5, 4, 2, num_kb=8) == [
-        (0, 0, 0, 256, 0, 8), (1, 1, 0, 256, 0, 8), (2, 2, 0, 256, 0, 8), (3, 3, 0, 256, 0, 8),
-        (4, 4, 0, 128, 0, 8), (5, 4, 128, 128, 0, 8)]
-    assert [i[2:4] for i in sm.work_items(2, 0, 4)[:4]] == [(0, 64), (64, 64), (128, 64), (192, 64)]
-    # the same tile cut along K in three: k-blocks 0-2, 3-5, 6-9
-    assert sm.work_items(5, 4, 3, split_k=True, num_kb=10)[4:] == [
-        (4, 4, 0, 256, 0, 3), (5, 4, 0, 256, 3, 6), (6, 4, 0, 256, 6, 10)]
-    # uneven K parts: a short first part (25 k-blocks) and a long last one (39)
-    assert sm.work_items(5, 4, 2, split_k=True, num_kb=64, part_kb=25)[4:] == [
-        (4, 4, 0, 256, 0, 25), (5, 4, 0, 256, 25, 64)]
-    with pytest.raises(ValueError):      # parts must leave the last one at least a k-block
-        sm.work_items(5, 4, 3, split_k=True, num_kb=10, part_kb=5)
+    # whole tiles; a sub-wave problem cut into column slices of 128 and 64 columns
+    assert sm.work_items(3, num_kb=8) == [(0, 0, 0, 256, 0, 8), (1, 1, 0, 256, 0, 8), (2, 2, 0, 256, 0, 8)]
+    assert sm.work_items(2, 2, num_kb=8) == [
+        (0, 0, 0, 128, 0, 8), (1, 0, 128, 128, 0, 8), (2, 1, 0, 128, 0, 8), (3, 1, 128, 128, 0, 8)]
+    assert [i[2:4] for i in sm.work_items(2, 4)[:4]] == [(0, 64), (64, 64), (128, 64), (192, 64)]
+    with pytest.raises(ValueError):
+        sm.work_items(4, 3)
+    with pytest.raises(ValueError):      # slices and the stream-K share exclude each other
+        sm.work_items(4, 2, num_kb=4, sk_tiles=4, sk_units=2)
 
 
-@pytest.mark.parametrize("T,F,s,k,a", [(512, 456, 2, False, None), (8, 0, 4, False, None),
-                                       (528, 456, 2, False, None), (150, 150, 1, False, None),
-                                       (800, 760, 2, False, None), (512, 456, 2, True, None),
-                                       (256, 228, 3, True, None), (800, 760, 4, True, None), (8, 0, 4, True, None),
-                                       (512, 456, 2, True, 2), (256, 228, 3, True, 1)])
-def test_work_items_partition_every_tile(T, F, s, k, a):
-    num_kb = 7
-    items = sm.work_items(T, F, s, split_k=k, num_kb=num_kb, part_kb=a)
-    assert [i[0] for i in items] == list(range(F + s * (T - F)))
+def test_stream_k_hand_worked(golden_dir):
+    with open(os.path.join(golden_dir, "stream_k_T5_G3_kb4.json")) as f:
+        g = json.load(f)
+    units = sm.work_units(g["T"], num_kb=g["num_kb"], sk_tiles=g["sk_tiles"], sk_units=g["sk_units"])
+    assert [[list(it) for it in u] for u in units] == g["units"]
+    assert sm.record_slots(g["T"], sk_tiles=g["sk_tiles"], sk_units=g["sk_units"]) == g["slots"]
+    pieces = {}
+    for it in sm.work_items(g["T"], num_kb=g["num_kb"], sk_tiles=g["sk_tiles"], sk_units=g["sk_units"]):
+        pieces[it[1]] = pieces.get(it[1], 0) + 1
+    assert sorted(t for t, n in pieces.items() if n > 1) == g["cut_tiles"]
+    # with whole tiles after the region: T = 8 on G = 3 -> R = 2, region = 5 tiles, 3 whole tiles
+    units = sm.work_units(8, num_kb=4, sk_tiles=5, sk_units=3)
+    assert units[:3] == sm.work_units(5, num_kb=4, sk_tiles=5, sk_units=3)
+    assert units[3:] == [[(9, 5, 0, 256, 0, 4)], [(10, 6, 0, 256, 0, 4)], [(11, 7, 0, 256, 0, 4)]]
+
+
+def _cells_partition(items, T, num_kb, tile_n=256):
     cells = {}
     for _, t, off, n, k0, k1 in items:
         assert k1 > k0
-        cells.setdefault(t, []).append((off, n, k0, k1))
+        cells.setdefault(t, set())
+        new = {(c, kb) for c in range(off, off + n, 64) for kb in range(k0, k1)}
+        assert not (cells[t] & new)                     # nothing computed twice
+        cells[t] |= new
+    assert sorted(cells) == list(range(T))
     for t in range(T):
-        got = set()
-        for off, n, k0, k1 in cells[t]:
-            new = {(c, kb) for c in range(off, off + n) for kb in range(k0, k1)}
-            assert not (got & new)                      # nothing computed twice
-            got |= new
-        assert got == {(c, kb) for c in range(256) for kb in range(num_kb)}
+        assert cells[t] == {(c, kb) for c in range(0, tile_n, 64) for kb in range(num_kb)}
+
+
+@pytest.mark.parametrize("T,s", [(8, 4), (20, 2), (150, 1), (1, 4), (37, 2)])
+def test_slices_partition_every_tile(T, s):
+    items = sm.work_items(T, s, num_kb=3)
+    assert [i[0] for i in items] == list(range(sm.record_slots(T, s)))
+    _cells_partition(items, T, 3)
+
+
+@pytest.mark.parametrize("T,G,num_kb", [(5, 3, 4), (8, 3, 4), (20, 7, 2), (20, 7, 9), (512, 152, 64),
+                                        (256, 76, 64), (528, 152, 32), (800, 152, 1), (153, 152, 3),
+                                        (303, 152, 5), (1024, 76, 128), (11, 10, 1), (19, 10, 7)])
+def test_stream_k_partition_and_balance(T, G, num_kb):
+    R = T % G
+    sk_tiles = R + G
+    units = sm.work_units(T, num_kb=num_kb, sk_tiles=sk_tiles, sk_units=G)
+    items = [it for u in units for it in u]
+    assert len(units) == G + T - sk_tiles
+    _cells_partition(items, T, num_kb)
+    slots = [it[0] for it in items]
+    assert len(set(slots)) == len(slots) and max(slots) < sm.record_slots(T, sk_tiles=sk_tiles, sk_units=G)
+    L = sk_tiles * num_kb
+    pieces_per_tile = {}
+    for c, u in enumerate(units[:G]):
+        assert 1 <= len(u) <= 3
+        assert [it[0] for it in u] == list(range(3 * c + len(u) - 1, 3 * c - 1, -1))   # last tile first
+        assert u[0][4] == 0                             # every unit starts at k-block 0 of a tile
+        kb = sum(it[5] - it[4] for it in u)
+        assert kb in (L // G, -(-L // G))               # even shares, to within one k-block
+        assert kb >= num_kb                             # at least a tile's worth each
+        for it in u:
+            pieces_per_tile[it[1]] = pieces_per_tile.get(it[1], 0) + 1
+    assert max(pieces_per_tile.values()) <= 2
+    # static assignment: cluster c runs units c, c + G, ...; every cluster ends
+    # up with the same number of k-blocks to within one
+    load = [0] * G
+    for u, its in enumerate(units):
+        load[u % G] += sum(it[5] - it[4] for it in its)
+    assert max(load) - min(load) <= 1
+    assert sum(load) == T * num_kb
