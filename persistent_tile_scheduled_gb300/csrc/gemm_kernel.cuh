@@ -695,12 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) {
-                        if (CG == 2 && !leader)
-                            mbar_arrive_cluster(mapa(acc_empty0 + 8 * acc, 0u));
-                        else
-                            mbar_arrive(acc_empty0 + 8 * acc);
-                    }
+                    if (CG == 2 && !leader)
+                        mbar_arrive_cluster_if(one, mapa(acc_empty0 + 8 * acc, 0u));
+                    else
+                        mbar_arrive_if(one, acc_empty0 + 8 * acc);
                 }
                 if (write_partial) {
                     float4 *dst = const_cast<float4 *>(partials) + part * kPartialFloat4PerWarp
@@ -763,7 +761,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 const uint32_t buf = stage_base + (nstore & 1u) * kEpiBufBytes;
-                if (lane == 0) bulk_wait_read<1>();   // the store that used this buffer has read it
+                // the store that used this buffer has read it (only lane 0 has
+                // stores in flight; the other lanes return at once)
+                bulk_wait_read<1>();
                 __syncwarp();
                 // row `lane`, 16-byte chunk j stored at chunk j ^ (row % 8): the
                 // layout the 128-byte-swizzled tensor map expects
@@ -774,10 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
-                    bulk_commit();
-                }
+                tma_store_2d_if((row0 < p.M && col < p.N) ? one : 0u, &tmC, buf, col, row0);
+                bulk_commit();   // (an empty group in lanes 1-31)
                 ++nstore;
             }
             if (write_partial) {
@@ -795,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the last stores must have read their staging buffers before the
         // CTA's shared memory goes away (their writes to C complete with the
         // grid)
-        if (lane == 0) bulk_wait_read<0>();
+        bulk_wait_read<0>();
         __syncwarp();
     }
 

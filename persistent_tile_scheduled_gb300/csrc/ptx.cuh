@@ -166,14 +166,16 @@ __device__ __forceinline__ void tma_prefetch_2d(uint32_t pred, const void *tmap,
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y)
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// TMA store of a shared-memory box, only where `pred` is non-zero.
+__device__ __forceinline__ void tma_store_2d_if(uint32_t pred, const void *tmap, uint32_t src, int x, int y)
 {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
-                 ::"l"(tmap), "r"(src), "r"(x), "r"(y)
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%1, {%3, %4}], [%2];\n\t}"
+                 ::"r"(pred), "l"(tmap), "r"(src), "r"(x), "r"(y)
                  : "memory");
 }
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>
 __device__ __forceinline__ void bulk_wait_read()
