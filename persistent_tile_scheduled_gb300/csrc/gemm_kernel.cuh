@@ -677,21 +677,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const bool write_partial = part >= 0 && part < nparts - 1;
-            // Chunks of 64 columns, software-pipelined: the TMEM loads of
-            // chunk c+1 are in flight while chunk c is converted and stored.
-            uint32_t ra0[32], ra1[32], rb0[32], rb1[32];
-            tmem_ld_32x32b_x32(tbase, ra0);
-            tmem_ld_32x32b_x32(tbase + 32, ra1);
+            // Chunks of 64 columns.  A TMEM read returns within a few dozen
+            // cycles, so each chunk is read when it is needed.  The piece that
+            // adds the partial keeps the next chunk's partial sums in flight
+            // while the current chunk is converted and stored.
+            const float4 *src = part > 0 ? partials + lane : nullptr;   // the one partial slot
+            float4 pa[16];
+            if (part > 0) {
+#pragma unroll
+                for (int g = 0; g < 16; ++g) pa[g] = __ldcg(src + g * 32);
+            }
 #pragma unroll
             for (int c = 0; c < kTileN / kEpiChunkCols; ++c) {
                 if (c >= chunks) break;
-                uint32_t(&v0)[32] = (c & 1) ? rb0 : ra0;
-                uint32_t(&v1)[32] = (c & 1) ? rb1 : ra1;
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
+                tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols + 32, v1);
                 tmem_wait_ld();
-                if (c + 1 < chunks) {
-                    tmem_ld_32x32b_x32(tbase + (c + 1) * kEpiChunkCols, (c & 1) ? ra0 : rb0);
-                    tmem_ld_32x32b_x32(tbase + (c + 1) * kEpiChunkCols + 32, (c & 1) ? ra1 : rb1);
-                } else {
+                if (c + 1 == chunks) {
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
@@ -701,8 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_if(one, acc_empty0 + 8 * acc);
                 }
                 if (write_partial) {
-                    float4 *dst = const_cast<float4 *>(partials) + part * kPartialFloat4PerWarp
-                                  + c * 16 * 32 + lane;
+                    float4 *dst = const_cast<float4 *>(partials) + c * 16 * 32 + lane;
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
                         __stcg(dst + g * 32, make_float4(__uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]),
@@ -715,29 +717,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            __uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3])));
                     continue;
                 }
-                if (part > 0) {   // the last piece of a cut tile: add the others' partials
-                    for (int sl = 0; sl < part; ++sl) {
-                        // issue 8 loads before using any, so their latencies overlap
-                        const float4 *src = partials + sl * kPartialFloat4PerWarp + c * 16 * 32 + lane;
-                        float4 a[8];
+                if (part > 0) {   // the last piece of a cut tile: add the other's partial
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) a[g] = __ldcg(src + g * 32);
+                    for (int g = 0; g < 8; ++g) {
+                        v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + pa[g].x);
+                        v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + pa[g].y);
+                        v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + pa[g].z);
+                        v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + pa[g].w);
+                        v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + pa[8 + g].x);
+                        v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + pa[8 + g].y);
+                        v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + pa[8 + g].z);
+                        v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + pa[8 + g].w);
+                    }
+                    if (c + 1 < chunks) {   // the next chunk's partial, in flight from here on
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            v0[4 * g] = __float_as_uint(__uint_as_float(v0[4 * g]) + a[g].x);
-                            v0[4 * g + 1] = __float_as_uint(__uint_as_float(v0[4 * g + 1]) + a[g].y);
-                            v0[4 * g + 2] = __float_as_uint(__uint_as_float(v0[4 * g + 2]) + a[g].z);
-                            v0[4 * g + 3] = __float_as_uint(__uint_as_float(v0[4 * g + 3]) + a[g].w);
-                        }
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) a[g] = __ldcg(src + (8 + g) * 32);
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            v1[4 * g] = __float_as_uint(__uint_as_float(v1[4 * g]) + a[g].x);
-                            v1[4 * g + 1] = __float_as_uint(__uint_as_float(v1[4 * g + 1]) + a[g].y);
-                            v1[4 * g + 2] = __float_as_uint(__uint_as_float(v1[4 * g + 2]) + a[g].z);
-                            v1[4 * g + 3] = __float_as_uint(__uint_as_float(v1[4 * g + 3]) + a[g].w);
-                        }
+                        for (int g = 0; g < 16; ++g) pa[g] = __ldcg(src + (c + 1) * 16 * 32 + g * 32);
                     }
                 }
                 uint32_t pk[32];
