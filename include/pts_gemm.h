@@ -79,7 +79,9 @@ typedef struct gemm_opts {
     int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair);
                                        0 = per call: pairs when a tile has >= 16 k-blocks */
     int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
-    int stages;                     /* shared-memory ring depth; 0 = the most that fits */
+    int stages;                     /* shared-memory ring depth in stages (a stage holds one
+                                       k-block for single CTAs, two for CTA pairs); 0 = the
+                                       most that fits (4 and 3) */
     int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */
     unsigned debug_flags;           /* GEMM_DEBUG_* */
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
@@ -145,7 +147,8 @@ typedef struct gemm_tile_record {
 
 /* Launch shape chosen for a problem. */
 typedef struct gemm_launch_info {
-    int tile_m, tile_n, tile_k;     /* output tile per cluster, k-block per stage (elements) */
+    int tile_m, tile_n, tile_k;     /* output tile per cluster, k-block (elements; a CTA pair's
+                                       ring stage holds two k-blocks) */
     int cta_group;
     int stages;
     int64_t tiles_m, tiles_n, tiles;

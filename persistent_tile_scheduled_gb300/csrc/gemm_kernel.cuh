@@ -281,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     // tmB / tmB2 / tmB4: B boxes of 256/CG, 128/CG and 64/CG rows, for whole
     // tiles and for halves and quarters of the last wave's tiles
-    constexpr int SA = stage_bytes_a();
+    constexpr int KBS = kb_per_stage(CG);   // k-blocks per ring stage
+    constexpr int SA = stage_bytes_a(CG);
     constexpr int SB = stage_bytes_b(CG);
     constexpr int KELEMS = (KIND == 2) ? kKBlockBytes : kKBlockBytes / 2;   // K elements per k-block
 
@@ -425,10 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_tile = [&](const WorkTile &t) -> bool {
             int ya, yb;
             const CUtensorMap *mb = boxes(t, ya, yb);
-            const uint32_t tx = static_cast<uint32_t>(CG * (SA + (t.n_len / CG) * kKBlockBytes));
-            for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+            // a stage holds KBS k-blocks (the last stage of an item may hold fewer)
+            for (int kb = t.kb_begin; kb < t.kb_end; kb += KBS) {
                 if (!ctl.wait_all(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
-                const int x = kb * KELEMS;
+                const int nk = t.kb_end - kb < KBS ? t.kb_end - kb : KBS;
+                const uint32_t tx =
+                    static_cast<uint32_t>(CG * nk * (SA / KBS + (t.n_len / CG) * kKBlockBytes));
                 const uint32_t fb = full0 + 8 * stage;
                 // test hook: announce the stage's bytes but never load them,
                 // so the MMA warp's bounded wait on this stage runs out
@@ -436,13 +439,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t go = skip ? 0u : one;
                 if constexpr (CG == 1) {
                     mbar_arrive_expect_tx_if(one, fb, tx);
-                    tma_load_2d(go, sA + stage * SA, &tmA, fb, x, ya);
-                    tma_load_2d(go, sB + stage * SB, mb, fb, x, yb);
+                    for (int j = 0; j < nk; ++j) {
+                        tma_load_2d(go, sA + stage * SA + j * (SA / KBS), &tmA, fb, (kb + j) * KELEMS, ya);
+                        tma_load_2d(go, sB + stage * SB + j * (SB / KBS), mb, fb, (kb + j) * KELEMS, yb);
+                    }
                 } else {
                     mbar_arrive_expect_tx_if(leader ? one : 0u, fb, tx);
                     const uint32_t fbc = mapa(fb, 0u);
-                    tma_load_2d_pair(go, sA + stage * SA, &tmA, fbc, x, ya);
-                    tma_load_2d_pair(go, sB + stage * SB, mb, fbc, x, yb);
+                    for (int j = 0; j < nk; ++j) {
+                        tma_load_2d_pair(go, sA + stage * SA + j * (SA / KBS), &tmA, fbc, (kb + j) * KELEMS, ya);
+                        tma_load_2d_pair(go, sB + stage * SB + j * (SB / KBS), mb, fbc, (kb + j) * KELEMS, yb);
+                    }
                 }
                 // keep the k-block prefetch_kb ahead of this one on its way into
                 // L2, so that a stage rarely waits on an HBM miss
@@ -569,18 +576,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
-                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+                for (int kb = t.kb_begin; kb < t.kb_end; kb += KBS) {
                     if (!ctl.wait_all(full0 + 8 * stage, phase, WHERE_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_sw128(sA + stage * SA);
-                    const uint64_t bd = smem_desc_sw128(sB + stage * SB);
+                    const int nk = t.kb_end - kb < KBS ? t.kb_end - kb : KBS;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                        umma<KIND, CG>(one, d, ad + 2 * k, bd + 2 * k, idesc,
-                                       (kb != t.kb_begin || k != 0) ? 1u : 0u);
+                    for (int j = 0; j < KBS; ++j) {
+                        if (j >= nk) break;
+                        const uint64_t ad = smem_desc_sw128(sA + stage * SA + j * (SA / KBS));
+                        const uint64_t bd = smem_desc_sw128(sB + stage * SB + j * (SB / KBS));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                            umma<KIND, CG>(one, d, ad + 2 * k, bd + 2 * k, idesc,
+                                           (kb + j != t.kb_begin || k != 0) ? 1u : 0u);
+                    }
                     umma_commit<CG>(one, empty0 + 8 * stage, 0x3);
                     last_stage = stage;
                     last_phase = phase;

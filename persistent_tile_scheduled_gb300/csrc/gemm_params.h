@@ -138,15 +138,23 @@ inline int choose_split(int64_t tiles, int64_t resident)
     return 1;
 }
 
-__host__ __device__ constexpr int stage_bytes_a() { return kRowsPerCta * kKBlockBytes; }
-__host__ __device__ constexpr int stage_bytes_b(int cg) { return (kTileN / cg) * kKBlockBytes; }
+// K-blocks per ring stage.  A stage's fixed costs (its barrier waits, the
+// expect-tx arrival, the commit that frees it) are paid once per stage, so a
+// CTA pair, whose 32 KB k-blocks leave room for 3 stages of 2, takes 2 per
+// stage: measured on GB300 (fp16 4096^2 x 4096) 75.7 vs 79.0 us from the first
+// MMA to the last store.  A single CTA keeps 1 (4 stages of 48 KB): with 2 per
+// stage it would have only 2 stages in flight, too few to cover the loads
+// (K = 768: 26.6 vs 24.8 us).
+__host__ __device__ constexpr int kb_per_stage(int cg) { return cg == 2 ? 2 : 1; }
+__host__ __device__ constexpr int stage_bytes_a(int cg) { return kRowsPerCta * kKBlockBytes * kb_per_stage(cg); }
+__host__ __device__ constexpr int stage_bytes_b(int cg) { return (kTileN / cg) * kKBlockBytes * kb_per_stage(cg); }
 __host__ __device__ constexpr int epi_bytes() { return kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes; }
 
 // Dynamic shared memory needed for `stages` stages (plus 1 KB for aligning
 // the base to the 1024-byte swizzle period).
 __host__ __device__ constexpr int smem_bytes(int cg, int stages)
 {
-    return 1024 + stages * (stage_bytes_a() + stage_bytes_b(cg)) + epi_bytes()
+    return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg)) + epi_bytes()
            + 8 * (2 * kMaxStages + 4 + 2 * kRing + 1)    // mbarriers
            + 16                                          // CLC response
            + 4 * kRing + 16;                             // ring payload, TMEM base, abort flag
