@@ -205,11 +205,16 @@ typedef struct gemm_host_problem {
     float scale_a, scale_b; /* e4m3 only */
 } gemm_host_problem_t;
 
-/* Run n GEMMs on HOST buffers with the transfers overlapped: while GEMM i
- * computes on `stream`, the inputs of GEMM i+1 are copied in and the result of
- * GEMM i-1 is copied out, on two copy streams the handle owns, through four
- * device staging slots the handle owns (grown as needed), so copy-in may run
- * up to three GEMMs ahead of copy-out.  Work already
+/* Run n independent GEMMs on HOST buffers with the transfers overlapped:
+ * while one GEMM computes on `stream`, the inputs of the next are copied in
+ * (one copy stream) and the results of earlier ones are copied out (two copy
+ * streams, alternating), all owned by the handle, through six device staging
+ * slots the handle owns (grown as needed), so copy-in may run up to five GEMMs
+ * ahead of copy-out.  The
+ * problems are processed in an order the library picks (alternately the most
+ * output-heavy and the most input-heavy remaining one), so that both
+ * directions of the host link carry data at once; every C is written exactly
+ * as if they ran in the given order.  Work already
  * queued on `stream` completes before the first copy starts.  Returns after
  * every result is in host memory (the call synchronises), with the device
  * status like gemm_check.  Pinned host memory is needed for the copies to

@@ -167,6 +167,22 @@ def test_forced_stream_k_share(cg, G, sched):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("cg,stages", [(1, 2), (1, 3), (1, 4), (2, 2), (2, 3)])
+def test_every_ring_depth(cg, stages):
+    """Shallower rings than the default: a single CTA's stage holds one k-block,
+    a pair's two (so an item with an odd k-block count ends on a half stage)."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, stages=stages, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        assert pts.gemm_query(h, 512, 512, 512, pts.GEMM_F16, 1).stages == stages
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1088, wl.F16), (257, 264, 384, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("ring", M, N, K, dt, dist, M + N + K + stages))
+            for sched in SCHEDS:
+                _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
 @pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("split,split_k,G", [(1, -1, 0), (2, 0, 0), (1, 1, 5)])
 def test_direct_store_epilogue(cg, split, split_k, G):
