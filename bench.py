@@ -104,11 +104,17 @@ def peak_value(peaks, *keys):
 
 
 def kernel_hash() -> str:
+    """sha256[:16] of the kernel sources without their // comments and blank
+    lines, so that a comment-only edit does not retire a profile."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -5,22 +5,29 @@
 // One CTA (CG = 1) or one CTA pair (CG = 2, tcgen05 cta_group::2) computes a
 // (128*CG) x 256 output tile at a time.  Warp roles:
 //   warp 0     producer: TMA loads of A and B k-blocks into an S-stage
-//              shared-memory ring guarded by full/empty mbarriers; on the
-//              leader CTA it is also the tile scheduler (static arithmetic or
-//              Cluster Launch Control) and publishes every tile id into a
-//              small broadcast ring read by all other roles
-//   warp 1     MMA issuer (one thread of the leader CTA): tcgen05.mma into one
-//              of two 256-column TMEM accumulators, so the epilogue of tile i
-//              overlaps the mainloop of tile i+1
+//              shared-memory ring guarded by full/empty mbarriers (one k-block
+//              per stage for a single CTA, two for a pair); on the leader CTA
+//              it is also the scheduler (static arithmetic or Cluster Launch
+//              Control): it takes units, splits each into its work items and
+//              publishes their ids into a small broadcast ring read by every
+//              other role
+//   warp 1     MMA issuer (the leader CTA's warp, lane 0 issuing): tcgen05.mma
+//              into one of two 256-column TMEM accumulators, so the epilogue
+//              of item i overlaps the mainloop of item i+1
 //   warps 2-5  epilogue: tcgen05.ld -> (scale) -> fp16/bf16 -> swizzled
-//              shared-memory staging -> TMA store
+//              shared-memory staging -> TMA store; for a tile cut in two by
+//              the stream-K share, the fp32 partial fixup
+// The producer and MMA warps run their loops with all 32 lanes in step and
+// issue through predicated instructions from lane 0.
 //
 // Scheduling follows "Persistent Kernels with Cluster Launch Control": a
-// static scheduler derives later tiles in software (w, w+G, w+2G, ...); a CLC
+// static scheduler derives later units in software (u, u+G, u+2G, ...); a CLC
 // scheduler asks the hardware to cancel a not-yet-launched cluster of the same
-// grid and takes that cluster's id as its next tile, never asking again after
-// one failed request.  The non-persistent mode runs exactly one tile per
+// grid and takes that cluster's id as its next unit, never asking again after
+// one failed request.  The non-persistent mode runs exactly one unit per
 // cluster ("question about persistent kernel concept": a thread block per tile).
+// A unit is a whole tile, a column slice of one, or a stream-K unit's pieces
+// (see work_tile()).
 //
 // Every mbarrier wait is bounded: on time-out the kernel records an error in
 // the device status block, tells every role (and the peer CTA) to stop, drains
@@ -41,7 +48,7 @@ enum : int32_t {
     WHERE_ACC_EMPTY = 3,    // MMA waiting for a drained accumulator
     WHERE_ACC_FULL = 4,     // epilogue waiting for a finished accumulator
     WHERE_RING_EMPTY = 5,   // scheduler waiting for a free broadcast slot
-    WHERE_RING_FULL = 6,    // a role waiting for the next tile id
+    WHERE_RING_FULL = 6,    // a role waiting for the next work item id
     WHERE_CLC = 7,          // scheduler waiting for a CLC response
     WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
     WHERE_FIXUP = 9,        // the second piece of a cut tile waiting for the first's partial
@@ -280,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmC, const GemmParams p)
 {
     // tmB / tmB2 / tmB4: B boxes of 256/CG, 128/CG and 64/CG rows, for whole
-    // tiles and for halves and quarters of the last wave's tiles
+    // tiles and for the column slices (halves, quarters) of a problem smaller
+    // than one wave
     constexpr int KBS = kb_per_stage(CG);   // k-blocks per ring stage
     constexpr int SA = stage_bytes_a(CG);
     constexpr int SB = stage_bytes_b(CG);
