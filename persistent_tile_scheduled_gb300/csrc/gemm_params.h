@@ -115,12 +115,12 @@ inline int64_t choose_stream_k(int64_t tiles, int64_t resident, int64_t num_kb, 
 
 // CTA group when the caller leaves it to the library.  CTA pairs (cta_group
 // 2) load a third less per SM for the same MMA work, so their mainloop runs
-// faster under full load (fp16 4096^2 x 4096: 0.318 vs 0.326 us per k-block,
-// 90 vs 94 us per launch), but a pair costs a few microseconds more to start
-// and finish.  Measured over the fp16 4096^2 K sweep on GB300, pairs pay off
-// from about 16 k-blocks per tile; single CTAs win below (K = 256: 21.5 vs
-// 28.3 us).
-constexpr int kPairMinKb = 16;
+// faster under full load, but a pair costs 3-5 us more per launch to start,
+// fill and finish.  Measured on GB300 on fp16 4096^2 with cold inputs (eight
+// buffer sets in turn), single vs pair per launch: K = 1024 32.1 vs 34.7 us,
+// K = 2048 52.3 vs 53.2, K = 2560 61.7 vs 61.8, K = 3072 70.8 vs 69.9.  So
+// pairs from 40 k-blocks per tile.
+constexpr int kPairMinKb = 40;
 
 inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
 

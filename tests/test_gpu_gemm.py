@@ -225,14 +225,14 @@ def test_automatic_stream_k_share():
 
 
 def test_automatic_cta_group():
-    """CTA pairs from 16 k-blocks per tile, single CTAs below."""
+    """CTA pairs from 40 k-blocks per tile, single CTAs below."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=0))
     try:
         assert pts.gemm_query(h, 4096, 4096, 512, pts.GEMM_F16, 1).cta_group == 1      # 8 k-blocks
-        assert pts.gemm_query(h, 4096, 4096, 960, pts.GEMM_F16, 1).cta_group == 1      # 15
-        assert pts.gemm_query(h, 4096, 4096, 1024, pts.GEMM_F16, 1).cta_group == 2     # 16
+        assert pts.gemm_query(h, 4096, 4096, 2496, pts.GEMM_F16, 1).cta_group == 1     # 39
+        assert pts.gemm_query(h, 4096, 4096, 2560, pts.GEMM_F16, 1).cta_group == 2     # 40
         assert pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_BF16, 1).cta_group == 2    # 128
-        assert pts.gemm_query(h, 8192, 8192, 1024, pts.GEMM_E4M3, 1).cta_group == 1    # 8 (128-wide k-blocks)
+        assert pts.gemm_query(h, 8192, 8192, 4096, pts.GEMM_E4M3, 1).cta_group == 1    # 32 (128-wide k-blocks)
         assert pts.gemm_query(h, 8192, 8192, 8192, pts.GEMM_E4M3, 1).cta_group == 2    # 64
         x = wl.custom(640, 1000, 8192, wl.BF16, "normal_sqrtk", 12)
         C = run_device(h, x, pts.GEMM_SCHED_CLC)
