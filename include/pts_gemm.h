@@ -32,7 +32,7 @@
  *   - Calls are asynchronous on the given stream unless stated otherwise.
  *   - A handle is not thread-safe; use one handle per host thread.  GEMMs
  *     that run at the same time on different streams need one handle each:
- *     a handle's workspace (K-split partials, debug records) serves one
+ *     a handle's workspace (stream-K partials, debug records) serves one
  *     launch at a time.
  */
 #ifndef PTS_GEMM_H
