@@ -318,6 +318,26 @@ def test_full_size_sampled(handle, name, arg):
         _run_checked(h, x, sched, full=False)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("K", [128, 1024, 1792, 2560, 4096])
+def test_bench_configuration_sampled(K):
+    """The exact launch configuration bench.py times: library defaults (CTA
+    group, ring depth, stream-K share chosen per GEMM) on sweep GEMMs that take
+    each plan: single CTAs without and with the stream-K share, CTA pairs with
+    it."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
+        info = pts.gemm_query(h, 4096, 4096, K, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
+        assert info.cta_group == (2 if K // 64 >= 40 else 1)
+        for sched in SCHEDS:
+            _run_checked(h, x, sched, full=False)
+    finally:
+        pts.gemm_destroy(h)
+
+
 # ---------------------------------------------------------------- CLC extras
 
 @pytest.mark.parametrize("stop_at", [0, 1, 3])
