@@ -349,7 +349,7 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.cta_group < 0 || o.cta_group > 2) return GEMM_ERR_INVALID_ARG;
     if (o.group_size_m < 1 || o.stages < 0 || o.stages == 1 || o.stages > pts::kMaxStages || o.max_clusters < 0)
         return GEMM_ERR_INVALID_ARG;
-    if (o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)
+    if (o.prefetch < -1 || o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)
         return GEMM_ERR_INVALID_ARG;
     if (o.split < 0 || o.split > 4 || o.split == 3 || o.split_k < -1 || o.split_k > 1
         || (o.split > 1 && o.split_k == 1))
