@@ -195,7 +195,7 @@ def gemm_flops(M, N, K):
 def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_graph=True):
     """Warm-up, then `steps` timed passes over the sweep (events only at step
     boundaries, so consecutive GEMMs may overlap their launches), then one
-    extra pass with an event between GEMMs for the per-K breakdown.  With
+    extra passes with an event between GEMMs for the per-K breakdown.  With
     use_graph the 32 launches of a pass are captured once in a CUDA graph and
     each step replays it (the same kernels, without the host launch cost)."""
     def one_pass():
@@ -235,16 +235,24 @@ def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_g
     if st != 0:
         raise RuntimeError(f"device status {dev:#x} in the timed region")
     total_ms = ev[0].elapsed_time(ev[steps])
-    # per-K breakdown (outside the timed region): an event around every GEMM
+    # per-K breakdown (outside the timed region): an event around every GEMM.
+    # The pass starts behind one untimed GEMM, so that the first timed launch
+    # does not also pay for waking an idle stream; three passes, the median
+    # per K.
     n = len(problems)
-    kev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-    with torch.cuda.stream(stream):
-        for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
-            kev[i].record(stream)
-            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
-        kev[n].record(stream)
-    torch.cuda.synchronize()
-    per_k = [kev[i].elapsed_time(kev[i + 1]) for i in range(n)]
+    passes = []
+    for _ in range(3):
+        kev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        with torch.cuda.stream(stream):
+            p0, (A0, B0, C0) = problems[-1], bufs[-1]
+            pts.gemm_run(h, p0.M, p0.N, p0.K, A0, B0, C0, p0.dtype, sched, 1.0, 1.0, stream)
+            for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
+                kev[i].record(stream)
+                pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+            kev[n].record(stream)
+        torch.cuda.synchronize()
+        passes.append([kev[i].elapsed_time(kev[i + 1]) for i in range(n)])
+    per_k = [statistics.median(v) for v in zip(*passes)]
     return total_ms, per_k, (t0, t1)
 
 
@@ -381,6 +389,9 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
                    "parallelism": f"replicas x{world}"},
         "pct_tensor_peak": round(achieved / tensor_peak, 4) if tensor_peak else None,
         "per_scheduler": {k: {kk: vv for kk, vv in v.items() if kk != "per_k_ms"} for k, v in per_sched.items()},
+        "persistent_ahead_at_every_K": (all(min(s_, c_) < n_ for s_, c_, n_ in zip(
+            per_sched["static"]["per_k_ms"], per_sched["clc"]["per_k_ms"], per_sched["nonpersistent"]["per_k_ms"]))
+            if all(k in per_sched for k in SCHED_NAMES) else None),
         "per_k_roofline": per_k_roof,
         "roofline": roofline,
         "e2e": e2e,
@@ -428,12 +439,25 @@ def time_one(pts, h, p, A, B, C, sa, sb, sched, stream, reps):
 
 
 def extra_configs(pts, dev, stream):
-    """The other workloads, TFLOP/s per scheduler: bf16 8192 sweep
-    points, e4m3 8192^3, the tail shapes, and two GEMMs at once on two streams."""
+    """The other workloads, TFLOP/s per scheduler: the whole bf16 8192 sweep,
+    e4m3 8192^3, the tail shapes, and two GEMMs at once on two streams."""
     out = {}
     h = pts.gemm_create(dev, pts.make_opts(cta_group=0))
     try:
-        probs = (wl.bf16_8192_ksweep([256, 1024, 2048, 4096, 6144, 8192]) + wl.e4m3_8192() + wl.bf16_tail())
+        # bf16 M = N = 8192, every K of the sweep (one K at a time, inputs freed after)
+        sweep = {"K": []}
+        for i, p in enumerate(wl.bf16_8192_ksweep()):
+            A, B, sa, sb = device_inputs(p, 6000 + i)
+            C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+            sweep["K"].append(p.K)
+            for si, name in enumerate(SCHED_NAMES):
+                ms = time_one(pts, h, p, A, B, C, sa, sb, si, stream, 5)
+                sweep.setdefault(name, []).append(round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1))
+            del A, B, C
+        sweep["persistent_ahead_at_every_K"] = all(
+            min(s_, c_) > n_ for s_, c_, n_ in zip(sweep["static"], sweep["clc"], sweep["nonpersistent"]))
+        out["bf16_8192_ksweep"] = sweep
+        probs = wl.e4m3_8192() + wl.bf16_tail()
         for i, p in enumerate(probs):
             A, B, sa, sb = device_inputs(p, 7000 + i)
             C = torch.empty(p.M, p.N, dtype=wl.output_torch_dtype(p.dtype), device="cuda")
