@@ -557,17 +557,19 @@ def half_occupied(pts, dev, stream, reps=6):
     return out
 
 
-def square_8192(pts, dev, stream, reps=10):
+def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)):
     """bf16 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
     p = wl.bf16_8192_ksweep([8192])[0]
     x = wl.make_inputs(p)
     A, B = x.A.cuda(), x.B.cuda()
     C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
     out = {}
-    for cg in (1, 2):
+    for cg in cgs:
         h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
         try:
             for si, name in enumerate(SCHED_NAMES):
+                if name not in scheds:
+                    continue
                 for _ in range(3):
                     pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, 1.0, 1.0, stream)
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
@@ -646,7 +648,17 @@ def main():
                     help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the 32 GEMMs of a step one by one instead of replaying a CUDA graph")
+    ap.add_argument("--square-only", action="store_true",
+                    help="only the bf16 8192^3 measurement (for profiling it), restricted by --cta-group and "
+                         "--scheds; prints its numbers, not the benchmark line")
     args = ap.parse_args()
+    if args.square_only:
+        import persistent_tile_scheduled_gb300 as pts
+        pts.load(build_if_missing=False)
+        out = square_8192(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
+                          scheds=tuple(args.scheds))
+        print(json.dumps({"square_8192_bf16": out}), flush=True)
+        return
     if args.warmup < 3:
         log("warm-up raised to 3 steps")
         args.warmup = 3
