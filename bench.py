@@ -557,11 +557,12 @@ def half_occupied(pts, dev, stream, reps=6):
     return out
 
 
-def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)):
-    """bf16 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
-    p = wl.bf16_8192_ksweep([8192])[0]
+def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES), dtype="bf16"):
+    """bf16 (or e4m3) 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
+    p = wl.bf16_8192_ksweep([8192])[0] if dtype == "bf16" else wl.e4m3_8192()[0]
     x = wl.make_inputs(p)
     A, B = x.A.cuda(), x.B.cuda()
+    sa, sb = (x.scale_a, x.scale_b) if dtype == "e4m3" else (1.0, 1.0)
     C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
     out = {}
     for cg in cgs:
@@ -571,12 +572,12 @@ def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)
                 if name not in scheds:
                     continue
                 for _ in range(3):
-                    pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, 1.0, 1.0, stream)
+                    pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, sa, sb, stream)
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
                 with torch.cuda.stream(stream):
                     for r in range(reps):
                         ev[r].record(stream)
-                        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, 1.0, 1.0, stream)
+                        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, si, sa, sb, stream)
                     ev[reps].record(stream)
                 torch.cuda.synchronize()
                 if pts.gemm_check(h, stream)[0] != 0:
@@ -649,15 +650,16 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the 32 GEMMs of a step one by one instead of replaying a CUDA graph")
     ap.add_argument("--square-only", action="store_true",
-                    help="only the bf16 8192^3 measurement (for profiling it), restricted by --cta-group and "
-                         "--scheds; prints its numbers, not the benchmark line")
+                    help="only the 8192^3 measurement (for profiling it), restricted by --cta-group, --scheds "
+                         "and --square-dtype; prints its numbers, not the benchmark line")
+    ap.add_argument("--square-dtype", choices=["bf16", "e4m3"], default="bf16")
     args = ap.parse_args()
     if args.square_only:
         import persistent_tile_scheduled_gb300 as pts
         pts.load(build_if_missing=False)
         out = square_8192(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
-                          scheds=tuple(args.scheds))
-        print(json.dumps({"square_8192_bf16": out}), flush=True)
+                          scheds=tuple(args.scheds), dtype=args.square_dtype)
+        print(json.dumps({f"square_8192_{args.square_dtype}": out}), flush=True)
         return
     if args.warmup < 3:
         log("warm-up raised to 3 steps")
