@@ -586,7 +586,8 @@ def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)
                 out[f"cg{cg}_{name}"] = round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1)
         finally:
             pts.gemm_destroy(h)
-    out["note"] = "median of 10 back-to-back launches; A,B = 256 MB > L2"
+    ab_mb = (A.numel() * A.element_size() + B.numel() * B.element_size()) / 1e6
+    out["note"] = f"median of {reps} back-to-back launches; A,B = {ab_mb:.0f} MB (L2 is 129 MB)"
     return out
 
 
