@@ -143,6 +143,8 @@ typedef struct gemm_tile_record {
      * item's last store (leader CTA) */
     uint32_t t_mma_start, t_acc_full, t_stored;
     uint32_t kb_begin, kb_end;  /* k-block range of the item */
+    uint32_t group;    /* problem of the item in a grouped launch (0 otherwise); `tile` is then the
+                          tile index within that problem */
 } gemm_tile_record_t;
 
 /* Launch shape chosen for a problem. */
@@ -221,6 +223,47 @@ typedef struct gemm_host_problem {
  * overlap.  Same size rules per problem as gemm_run; n == 0 does nothing. */
 gemm_status_t gemm_run_host_batch(gemm_handle_t h, const gemm_host_problem_t *problems, int64_t n,
                                   gemm_sched_t sched, void *stream);
+
+/* ---- grouped launch ----------------------------------------------------
+ * One problem of gemm_run_grouped: C = A . B with device pointers and the
+ * layouts, size rules and scales of gemm_run (M, N, K >= 0; M == 0 or N == 0
+ * contributes no tiles; K == 0 makes C zero). */
+typedef struct gemm_group_problem {
+    int64_t M, N, K;
+    const void *A;          /* device, M x K */
+    const void *B;          /* device, N x K */
+    void *C;                /* device, M x N */
+    float scale_a, scale_b; /* e4m3 only */
+} gemm_group_problem_t;
+
+#define GEMM_GROUPED_MAX_PROBLEMS 65536
+
+/* `count` independent GEMMs of one dtype in ONE launch.  The tiles of all
+ * problems form one list of work ids (problem 0's tiles first, each problem's
+ * in GROUP_SIZE_M-grouped order) that the scheduler hands out as it does one
+ * problem's tiles; a tile costs time in proportion to its problem's K, so
+ * the tiles differ in cost and a scheduler that hands out work as clusters
+ * finish (CLC, or the hardware's for the non-persistent grid) can balance
+ * what the static stride cannot ("Choosing between static and CLC
+ * scheduling": dynamic scheduling pays off when the work per tile varies).
+ * No stream-K share and no column slices.  CTA group (cta_group 0): pairs
+ * when the mean k-blocks per tile, weighted by output size, is at least 40.
+ * The handle keeps the problem table (tensor maps and tile counts, 512 bytes
+ * per problem) in device memory it owns, in two slots: a call with the same
+ * problems as the previous one reuses its table; a different list is copied
+ * to the other slot on `stream`, after the host has waited for the launch
+ * that last read that slot.  `problems` is host memory, read during the call
+ * only.  A capturing stream is refused (GEMM_ERR_INVALID_ARG): a graph would
+ * keep referring to a table later calls rewrite.  count in
+ * [0, GEMM_GROUPED_MAX_PROBLEMS]; total tiles < 2^30.  Records
+ * (GEMM_DEBUG_RECORDS) are per tile in work-id order with `group` set. */
+gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_group_problem_t *problems, int64_t count,
+                               gemm_dtype_t dtype, gemm_sched_t sched, void *stream);
+
+/* Launch shape gemm_run_grouped would use (no GPU work): tiles, work_items
+ * and units are the total over all problems; tiles_m, tiles_n are 0. */
+gemm_status_t gemm_query_grouped(gemm_handle_t h, const gemm_group_problem_t *problems, int64_t count,
+                                 gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info);
 
 /* Launch shape gemm_run would use (no GPU work).  Same argument rules. */
 gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,

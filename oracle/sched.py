@@ -123,6 +123,22 @@ def record_slots(T: int, split: int = 1, sk_tiles: int = 0, sk_units: int = 0) -
     return T * split
 
 
+def grouped_items(problems, BM: int, BN: int, group_m: int) -> List[Tuple[int, int, int]]:
+    """Work ids of a grouped launch (several independent GEMMs, one list of
+    tiles): ``(problem, tile-row, tile-col)`` per work id.  Problem 0's tiles
+    come first, each problem's in grouped order; a problem with M or N = 0
+    has no tiles.  ``problems``: sequence of (M, N)."""
+    out = []
+    for g, (M, N) in enumerate(problems):
+        if M == 0 or N == 0:
+            continue
+        Tm, Tn = tile_grid(M, N, BM, BN)
+        for w in range(Tm * Tn):
+            tm, tn = swizzle(w, Tm, Tn, group_m)
+            out.append((g, tm, tn))
+    return out
+
+
 def static_grid(T: int, max_clusters: int) -> int:
     """Resident clusters launched by the static persistent scheduler."""
     return max(1, min(T, max_clusters)) if T > 0 else 0

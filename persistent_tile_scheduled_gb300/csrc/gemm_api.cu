@@ -18,6 +18,7 @@
 namespace {
 
 constexpr int kBatchSlots = 6;   // gemm_run_host_batch staging depth
+constexpr int kGroupSlots = 2;   // gemm_run_grouped problem tables in flight
 constexpr int kMapCache = 1024;   // direct-mapped; a K sweep's A, B, C maps rarely collide
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per wait
 
@@ -58,6 +59,15 @@ struct gemm_ctx {
                                                                     // streams: one reaches ~146 GB/s of
                                                                     // the ~190 two reach (GB300)
     cudaEvent_t ev_entry = nullptr, ev_in[kBatchSlots] = {}, ev_comp[kBatchSlots] = {}, ev_free[kBatchSlots] = {};
+    // gemm_run_grouped: problem tables (GroupDesc[count] then int32 group_start[count + 1]),
+    // each as uploaded (pinned host copy) and on the device, and the event after the
+    // last launch that read it
+    void *tab_host[kGroupSlots] = {};
+    void *tab_dev[kGroupSlots] = {};
+    size_t tab_cap[kGroupSlots] = {};
+    size_t tab_bytes[kGroupSlots] = {};   // bytes of the table the slot holds (0 = none)
+    cudaEvent_t ev_tab[kGroupSlots] = {};
+    int tab_cur = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool smem_set[3][2] = {};
     int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
@@ -136,12 +146,9 @@ gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, g
     return GEMM_OK;
 }
 
-gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_sched_t sched,
-                        Plan &pl)
+// Ring depth, shared memory and resident clusters of the kernel for pl.cg.
+gemm_status_t kernel_shape(gemm_ctx *h, gemm_dtype_t dtype, Plan &pl)
 {
-    const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
-    pl.num_kb = (K + kelems - 1) / kelems;
-    pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb);
     int stages = h->opts.stages;
     if (stages == 0) {   // the deepest ring that fits
         stages = pts::kMaxStages;
@@ -150,12 +157,6 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     pl.stages = stages;
     pl.smem = pts::smem_bytes(pl.cg, stages);
     if (pl.smem > h->max_smem_optin) return GEMM_ERR_INVALID_ARG;
-    const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
-    pl.tiles_m = (M + tile_m - 1) / tile_m;
-    pl.tiles_n = (N + pts::kTileN - 1) / pts::kTileN;
-    pl.tiles = pl.tiles_m * pl.tiles_n;
-    if (pl.tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
-
     const int kind = static_cast<int>(dtype);
     const int ci = pl.cg - 1;
     pts::KernelOps ops = ops_for(kind, pl.cg);
@@ -171,8 +172,30 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     }
     pl.max_active_clusters = h->occ_clusters[kind][ci];
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+int64_t resident_clusters(const gemm_ctx *h, const Plan &pl)
+{
     int64_t resident = pl.max_active_clusters;
     if (h->opts.max_clusters > 0 && h->opts.max_clusters < resident) resident = h->opts.max_clusters;
+    return resident;
+}
+
+gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_sched_t sched,
+                        Plan &pl)
+{
+    const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
+    pl.num_kb = (K + kelems - 1) / kelems;
+    pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb);
+    const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
+    pl.tiles_m = (M + tile_m - 1) / tile_m;
+    pl.tiles_n = (N + pts::kTileN - 1) / pts::kTileN;
+    pl.tiles = pl.tiles_m * pl.tiles_n;
+    if (pl.tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = kernel_shape(h, dtype, pl);
+    if (st != GEMM_OK) return st;
+    int64_t resident = resident_clusters(h, pl);
     // column slices for a problem smaller than one wave (or forced, for testing)
     pl.split = h->opts.split > 0 ? h->opts.split : pts::choose_split(pl.tiles, resident);
     pl.sk_tiles = 0;
@@ -185,6 +208,26 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     int64_t clusters = pl.units;
     if (sched == GEMM_SCHED_STATIC) clusters = pl.units < resident ? pl.units : resident;
     pl.grid_ctas = clusters * pl.cg;
+    return GEMM_OK;
+}
+
+// With GEMM_DEBUG_RECORDS: zeroed records for `work` work items on `stream`
+// (grown as needed), handed to the kernel in p.records; else p.records = null.
+gemm_status_t prepare_records(gemm_ctx *h, int64_t work, cudaStream_t stream, pts::GemmParams &p)
+{
+    p.records = nullptr;
+    if (!(h->opts.debug_flags & GEMM_DEBUG_RECORDS)) return GEMM_OK;
+    if (h->records_cap < work) {
+        cudaFree(h->d_records);
+        h->d_records = nullptr;
+        h->records_cap = 0;
+        if (cudaMalloc(&h->d_records, size_t(work) * sizeof(pts::TileRecord)) != cudaSuccess)
+            return cuda_fail(cudaErrorMemoryAllocation);
+        h->records_cap = work;
+    }
+    if (cudaMemsetAsync(h->d_records, 0, size_t(work) * sizeof(pts::TileRecord), stream) != cudaSuccess)
+        return cuda_fail(cudaErrorInvalidValue);
+    p.records = h->d_records;
     return GEMM_OK;
 }
 
@@ -283,20 +326,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.fault_arg = h->opts.fault_arg;
     p.timeout_ns = h->opts.timeout_ns;
     p.status = h->d_status;
-    p.records = nullptr;
-    if (h->opts.debug_flags & GEMM_DEBUG_RECORDS) {
-        if (h->records_cap < pl.work) {
-            cudaFree(h->d_records);
-            h->d_records = nullptr;
-            h->records_cap = 0;
-            if (cudaMalloc(&h->d_records, size_t(pl.work) * sizeof(pts::TileRecord)) != cudaSuccess)
-                return cuda_fail(cudaErrorMemoryAllocation);
-            h->records_cap = pl.work;
-        }
-        if (cudaMemsetAsync(h->d_records, 0, size_t(pl.work) * sizeof(pts::TileRecord), stream) != cudaSuccess)
-            return cuda_fail(cudaErrorInvalidValue);
-        p.records = h->d_records;
-    }
+    if ((st = prepare_records(h, pl.work, stream, p)) != GEMM_OK) return st;
     h->last_work = pl.work;
     h->last_cta_group = pl.cg;
     h->last_sk_tiles = pl.sk_tiles;
@@ -307,6 +337,203 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
                                                                    pl.smem, stream, h->opts.overlap_launch >= 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return cuda_fail(cudaGetLastError());
+}
+
+// ---- grouped launch ---------------------------------------------------------
+
+gemm_status_t check_group_problem(const gemm_group_problem_t &q, gemm_dtype_t dtype, gemm_sched_t sched)
+{
+    gemm_status_t st = check_sizes(q.M, q.N, q.K, dtype, sched);
+    if (st != GEMM_OK) return st;
+    if (q.M == 0 || q.N == 0) return GEMM_OK;
+    if (q.C == nullptr || reinterpret_cast<uintptr_t>(q.C) % 16 != 0) return GEMM_ERR_INVALID_ARG;
+    if (q.K == 0) return GEMM_OK;
+    if (q.A == nullptr || q.B == nullptr || reinterpret_cast<uintptr_t>(q.A) % 16 != 0
+        || reinterpret_cast<uintptr_t>(q.B) % 16 != 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (dtype == GEMM_E4M3) {
+        if (!(q.scale_a > 0.0f) || !(q.scale_b > 0.0f) || !std::isfinite(q.scale_a) || !std::isfinite(q.scale_b)
+            || !std::isfinite(1.0f / (q.scale_a * q.scale_b)))
+            return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+// Launch shape of a grouped launch, and (encode) its problem table: one
+// GroupDesc per problem, then the tile prefix sums group_start[0..count].
+struct GroupedPlan {
+    Plan pl;
+    std::vector<pts::GroupDesc> desc;
+    std::vector<int32_t> start;
+};
+
+gemm_status_t plan_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t count, gemm_dtype_t dtype,
+                           gemm_sched_t sched, bool encode, GroupedPlan &gp)
+{
+    if (count < 0 || count > GEMM_GROUPED_MAX_PROBLEMS || (count > 0 && q == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if (dtype < GEMM_F16 || dtype > GEMM_E4M3) return GEMM_ERR_INVALID_ARG;
+    const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
+    // CTA group: the single-problem rule applied to the mean k-blocks per
+    // tile, weighted by output size
+    double w_sum = 0.0, kb_sum = 0.0;
+    for (int64_t g = 0; g < count; ++g) {
+        gemm_status_t st = check_group_problem(q[g], dtype, sched);
+        if (st != GEMM_OK) return st;
+        const double w = double(q[g].M) * double(q[g].N);
+        w_sum += w;
+        kb_sum += w * double((q[g].K + kelems - 1) / kelems);
+    }
+    Plan &pl = gp.pl;
+    pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group
+                                   : pts::choose_cta_group(w_sum > 0.0 ? int64_t(kb_sum / w_sum) : 0);
+    const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
+    gp.start.assign(size_t(count) + 1, 0);
+    int64_t tiles = 0;
+    for (int64_t g = 0; g < count; ++g) {
+        if (q[g].M > 0 && q[g].N > 0)
+            tiles += ((q[g].M + tile_m - 1) / tile_m) * ((q[g].N + pts::kTileN - 1) / pts::kTileN);
+        if (tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
+        gp.start[size_t(g) + 1] = static_cast<int32_t>(tiles);
+    }
+    pl.tiles_m = pl.tiles_n = 0;
+    pl.tiles = tiles;
+    pl.num_kb = 0;
+    pl.split = 1;
+    pl.sk_tiles = pl.sk_units = 0;
+    pl.units = pl.work = tiles;
+    gemm_status_t st = kernel_shape(h, dtype, pl);
+    if (st != GEMM_OK) return st;
+    const int64_t resident = resident_clusters(h, pl);
+    pl.grid_ctas = (sched == GEMM_SCHED_STATIC && tiles > resident ? resident : tiles) * pl.cg;
+    if (!encode) return GEMM_OK;
+
+    // Each map is copied out of the cache at once (a later lookup may reuse its slot).
+    gp.desc.resize(size_t(count));
+    const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
+    const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
+    for (int64_t g = 0; g < count; ++g) {
+        pts::GroupDesc &d = gp.desc[size_t(g)];
+        std::memset(&d, 0, sizeof(d));   // padding too: tables are compared byte for byte
+        const gemm_group_problem_t &x = q[g];
+        if (x.M == 0 || x.N == 0) continue;
+        d.M = static_cast<int32_t>(x.M);
+        d.N = static_cast<int32_t>(x.N);
+        d.num_kb = static_cast<int32_t>((x.K + kelems - 1) / kelems);
+        d.tiles_m = static_cast<int32_t>((x.M + tile_m - 1) / tile_m);
+        d.tiles_n = static_cast<int32_t>((x.N + pts::kTileN - 1) / pts::kTileN);
+        d.out_scale = (dtype == GEMM_E4M3 && x.K > 0) ? 1.0f / (x.scale_a * x.scale_b) : 1.0f;
+        const CUtensorMap *m;
+        if (!(m = get_map(h, x.C, uint64_t(x.M), uint64_t(x.N), cdt, pts::kEpiRowsPerWarp, pts::kEpiChunkCols)))
+            return GEMM_ERR_CUDA;
+        d.tmC = *m;
+        if (x.K == 0) continue;
+        if (!(m = get_map(h, x.A, uint64_t(x.M), uint64_t(x.K), dtype, pts::kRowsPerCta, uint32_t(kelems))))
+            return GEMM_ERR_CUDA;
+        d.tmA = *m;
+        if (!(m = get_map(h, x.B, uint64_t(x.N), uint64_t(x.K), dtype, brows, uint32_t(kelems))))
+            return GEMM_ERR_CUDA;
+        d.tmB = *m;
+    }
+    return GEMM_OK;
+}
+
+// Put the problem table on the device.  The same table as the last one
+// uploaded is used again as it is; a new one goes to the other slot, once
+// the launch that last read that slot has finished (the host waits for it),
+// copied from pinned memory on `stream`.
+gemm_status_t upload_table(gemm_ctx *h, const GroupedPlan &gp, cudaStream_t stream, int &slot, bool &uploaded)
+{
+    const size_t desc_bytes = gp.desc.size() * sizeof(pts::GroupDesc);
+    const size_t bytes = desc_bytes + gp.start.size() * sizeof(int32_t);
+    const int cur = h->tab_cur;
+    if (h->tab_bytes[cur] == bytes && std::memcmp(h->tab_host[cur], gp.desc.data(), desc_bytes) == 0
+        && std::memcmp(static_cast<char *>(h->tab_host[cur]) + desc_bytes, gp.start.data(), bytes - desc_bytes) == 0) {
+        slot = cur;
+        uploaded = false;
+        return GEMM_OK;
+    }
+    if (h->ev_tab[0] == nullptr)
+        for (int b = 0; b < kGroupSlots; ++b)
+            if (cudaEventCreateWithFlags(&h->ev_tab[b], cudaEventDisableTiming) != cudaSuccess)
+                return cuda_fail(cudaErrorUnknown);
+    const int s = (cur + 1) % kGroupSlots;
+    if (cudaEventSynchronize(h->ev_tab[s]) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    h->tab_bytes[s] = 0;
+    if (h->tab_cap[s] < bytes) {
+        cudaFreeHost(h->tab_host[s]);
+        cudaFree(h->tab_dev[s]);
+        h->tab_host[s] = h->tab_dev[s] = nullptr;
+        h->tab_cap[s] = 0;
+        const size_t cap = std::max(bytes, size_t(64) << 10);
+        if (cudaMallocHost(&h->tab_host[s], cap) != cudaSuccess || cudaMalloc(&h->tab_dev[s], cap) != cudaSuccess)
+            return cuda_fail(cudaErrorMemoryAllocation);
+        h->tab_cap[s] = cap;
+    }
+    std::memcpy(h->tab_host[s], gp.desc.data(), desc_bytes);
+    std::memcpy(static_cast<char *>(h->tab_host[s]) + desc_bytes, gp.start.data(), bytes - desc_bytes);
+    if (cudaMemcpyAsync(h->tab_dev[s], h->tab_host[s], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+    h->tab_bytes[s] = bytes;
+    h->tab_cur = s;
+    slot = s;
+    uploaded = true;
+    return GEMM_OK;
+}
+
+gemm_status_t launch_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t count, gemm_dtype_t dtype,
+                             gemm_sched_t sched, cudaStream_t stream)
+{
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    // the problem table outlives no launch that a graph could replay later
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    if (cap != cudaStreamCaptureStatusNone) return GEMM_ERR_INVALID_ARG;
+    GroupedPlan gp;
+    gemm_status_t st = plan_grouped(h, q, count, dtype, sched, true, gp);
+    if (st != GEMM_OK) return st;
+    const Plan &pl = gp.pl;
+    if (pl.tiles == 0) return GEMM_OK;
+    int slot = 0;
+    bool uploaded = false;
+    if ((st = upload_table(h, gp, stream, slot, uploaded)) != GEMM_OK) return st;
+
+    pts::GemmParams p{};
+    p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.split = 1;
+    p.num_units = static_cast<int32_t>(pl.units);
+    p.num_work = static_cast<int32_t>(pl.work);
+    p.group_m = h->opts.group_size_m;
+    p.sched = static_cast<int32_t>(sched);
+    p.stages = pl.stages;
+    p.prefetch_kb = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
+    p.out_scale = 1.0f;
+    p.debug_flags = h->opts.debug_flags;
+    p.fault_arg = h->opts.fault_arg;
+    p.timeout_ns = h->opts.timeout_ns;
+    p.status = h->d_status;
+    p.num_groups = static_cast<int32_t>(count);
+    p.groups = static_cast<const pts::GroupDesc *>(h->tab_dev[slot]);
+    p.group_start = reinterpret_cast<const int32_t *>(static_cast<const char *>(h->tab_dev[slot])
+                                                      + gp.desc.size() * sizeof(pts::GroupDesc));
+    if ((st = prepare_records(h, pl.work, stream, p)) != GEMM_OK) return st;
+    h->last_work = pl.work;
+    h->last_cta_group = pl.cg;
+    h->last_sk_tiles = h->last_sk_units = h->last_num_kb = 0;
+
+    // the kernel's own maps are unused in a grouped launch
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof(none));
+    const CUtensorMap *mb[3] = {&none, &none, &none};
+    // A launch right after an upload does not overlap the previous grid: the
+    // copy sits between them in the stream.
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg)
+                        .launch(none, mb, none, p, static_cast<int>(pl.grid_ctas), pl.smem, stream,
+                                h->opts.overlap_launch >= 0 && !uploaded);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    // (the first launch always uploads, which creates the events)
+    if (cudaEventRecord(h->ev_tab[slot], stream) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    return GEMM_OK;
 }
 
 gemm_status_t read_status(gemm_ctx *h, cudaStream_t stream, int *device_status)
@@ -571,6 +798,39 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     return GEMM_OK;
 }
 
+gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_group_problem_t *problems, int64_t count,
+                               gemm_dtype_t dtype, gemm_sched_t sched, void *stream)
+{
+    if (h == nullptr) return GEMM_ERR_INVALID_ARG;
+    return launch_grouped(h, problems, count, dtype, sched, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_query_grouped(gemm_handle_t h, const gemm_group_problem_t *problems, int64_t count,
+                                 gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info)
+{
+    if (h == nullptr || info == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->device) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+    GroupedPlan gp;
+    gemm_status_t st = plan_grouped(h, problems, count, dtype, sched, false, gp);
+    if (st != GEMM_OK) return st;
+    const Plan &pl = gp.pl;
+    std::memset(info, 0, sizeof(*info));
+    info->tile_m = pts::kRowsPerCta * pl.cg;
+    info->tile_n = pts::kTileN;
+    info->tile_k = dtype == GEMM_E4M3 ? 128 : 64;
+    info->cta_group = pl.cg;
+    info->stages = pl.stages;
+    info->tiles = pl.tiles;
+    info->grid_ctas = pl.tiles == 0 ? 0 : pl.grid_ctas;
+    info->max_active_clusters = pl.max_active_clusters;
+    info->smem_bytes = pl.smem;
+    info->threads = pts::kThreads;
+    info->split = 1;
+    info->work_items = pl.work;
+    info->units = pl.units;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status)
 {
     if (h == nullptr) return GEMM_ERR_INVALID_ARG;
@@ -617,6 +877,11 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
         if (h->ev_free[b]) cudaEventDestroy(h->ev_free[b]);
     }
     if (h->ev_entry) cudaEventDestroy(h->ev_entry);
+    for (int b = 0; b < kGroupSlots; ++b) {
+        cudaFreeHost(h->tab_host[b]);
+        cudaFree(h->tab_dev[b]);
+        if (h->ev_tab[b]) cudaEventDestroy(h->ev_tab[b]);
+    }
     if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
     for (cudaStream_t s : h->s_d2h)
         if (s) cudaStreamDestroy(s);

@@ -106,12 +106,33 @@ __device__ __forceinline__ void tile_of(int w, int tiles_m, int tiles_n, int gro
     tn = r / rows;
 }
 
-// A work item: tile (tm, tn), its column slice [n_off, n_off + n_len), its
+// A work item: tile (tm, tn) of problem g (0 unless the launch is grouped),
+// idx = tm * tiles_n + tn, its column slice [n_off, n_off + n_len), its
 // k-block range [kb_begin, kb_end), and for a stream-K piece of a tile that
 // is cut in two, the tile's index in the stream-K region (ks; else -1).
 struct WorkTile {
-    int tm, tn, n_off, n_len, kb_begin, kb_end, ks;
+    int tm, tn, n_off, n_len, kb_begin, kb_end, ks, g, idx;
 };
+
+// Problem of work id w in a grouped launch: the g with group_start[g] <= w <
+// group_start[g + 1] (problems without tiles have equal bounds and are never
+// the answer).  Called by a whole converged warp: each round the 32 lanes
+// test 32 evenly spaced bounds at once and keep the interval between the
+// last bound at or below w and the next one, so 1024 problems take two
+// rounds of one load per lane.
+__device__ __forceinline__ int group_of(int w, const GemmParams &p)
+{
+    int lo = 0, hi = p.num_groups;   // group_start[lo] <= w < group_start[hi]
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = lo + static_cast<int>(lane_id()) * step;
+        const bool below = idx < hi && __ldg(p.group_start + idx) <= w;
+        const uint32_t b = __ballot_sync(0xffffffffu, below);   // lane 0 always set
+        lo += (31 - __clz(b)) * step;
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
 
 // Work item (record slot) s.
 //  - With a stream-K region (sk_units = U > 0): s < 3U is piece s % 3 of
@@ -120,8 +141,9 @@ struct WorkTile {
 //    whole tile sk_tiles + s - 3U.
 //  - With column slices (split 2 or 4): slice s % split of tile s / split.
 //  - Otherwise the whole tile s.
+//  - In a grouped launch: whole tile s - group_start[g] of problem g.
 // Tiles are numbered in grouped order (tile_of).
-__device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
+__device__ __forceinline__ WorkTile work_tile(int s, int g, const GemmParams &p)
 {
     WorkTile t;
     int tile = s;
@@ -130,6 +152,15 @@ __device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
     t.kb_begin = 0;
     t.kb_end = p.num_kb;
     t.ks = -1;
+    t.g = g;
+    if (p.num_groups > 0) {
+        const GroupDesc *d = p.groups + g;
+        const int tiles_n = __ldg(&d->tiles_n);
+        t.kb_end = __ldg(&d->num_kb);
+        tile_of(s - __ldg(p.group_start + g), __ldg(&d->tiles_m), tiles_n, p.group_m, t.tm, t.tn);
+        t.idx = t.tm * tiles_n + t.tn;
+        return t;
+    }
     if (p.sk_units > 0) {
         const int U = p.sk_units;
         if (s < kSkMaxPieces * U) {
@@ -153,6 +184,7 @@ __device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
         t.n_off = h * t.n_len;
     }
     tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
+    t.idx = t.tm * p.tiles_n + t.tn;
     return t;
 }
 
@@ -310,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_empty0 = ring_full0 + 8 * kRing;     // + 8*r
     const uint32_t clc_bar = ring_empty0 + 8 * kRing;
     const uint32_t clc_resp = (clc_bar + 8 + 15) & ~15u;
-    const uint32_t ring_w0 = clc_resp + 16;                  // + 4*r
-    const uint32_t tmem_slot = ring_w0 + 4 * kRing;
+    const uint32_t ring_w0 = clc_resp + 16;                  // + 4*r: work id
+    const uint32_t ring_g0 = ring_w0 + 4 * kRing;            // + 4*r: its problem (grouped launch)
+    const uint32_t tmem_slot = ring_g0 + 4 * kRing;
     const uint32_t abort_flag = tmem_slot + 4;
 
     const uint32_t warp = threadIdx.x >> 5;
@@ -344,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_shared_u32(abort_flag, 0u);
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    const bool grouped = p.num_groups > 0;
+    if (warp == 0 && lane == 0 && !grouped) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         if (p.split == 2) prefetch_tmap(&tmB2);
@@ -362,11 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
     const uint32_t one = lane == 0 ? 1u : 0u;
 
-    // Rows of this CTA's A and B boxes for work item t, and the B map of the
-    // item's column width.
-    auto boxes = [&](const WorkTile &t, int &ya, int &yb) -> const CUtensorMap * {
+    // Rows of this CTA's A and B boxes for work item t, its A map, and the B
+    // map of the item's column width (a grouped launch: its problem's maps).
+    auto boxes = [&](const WorkTile &t, int &ya, int &yb, const CUtensorMap *&ma) -> const CUtensorMap * {
         ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
         yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
+        if (grouped) {
+            ma = &p.groups[t.g].tmA;
+            return &p.groups[t.g].tmB;
+        }
+        ma = &tmA;
         return t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
     };
 
@@ -377,31 +416,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // cluster's first unit: an L2 prefetch brings lines into the coherent L2
     // and changes nothing any load returns, so the first stages then fill
     // from L2 instead of HBM.
+    // (Not in a grouped launch, whose problem table is read only after the wait.)
     pdl_launch_dependents();
-    if (warp == 0 && cluster_id < p.num_units) {
-        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), p);
+    if (warp == 0 && cluster_id < p.num_units && !grouped) {
+        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), 0, p);
         int ya, yb;
-        const CUtensorMap *mb = boxes(t0, ya, yb);
+        const CUtensorMap *ma;
+        const CUtensorMap *mb = boxes(t0, ya, yb, ma);
         const int kb_end = t0.kb_end < t0.kb_begin + S ? t0.kb_end : t0.kb_begin + S;
         for (int kb = t0.kb_begin; kb < kb_end; ++kb) {
-            tma_prefetch_2d(one, &tmA, kb * KELEMS, ya);
+            tma_prefetch_2d(one, ma, kb * KELEMS, ya);
             tma_prefetch_2d(one, mb, kb * KELEMS, yb);
         }
     }
     pdl_wait();
 
     // ---- work-id broadcast ring -------------------------------------------
-    // Slot r holds the id of work item i (i % kRing == r), or -1 = no more.
-    // Both are called by whole converged warps (producer, MMA) or by lane 0
-    // of an epilogue warp; the slot write and the arrivals happen in lane 0.
-    auto publish = [&](int i, int w) -> bool {
+    // Slot r holds the id of work item i (i % kRing == r), or -1 = no more,
+    // and the item's problem g.  Both are called by whole converged warps
+    // (producer, MMA) or by lane 0 of an epilogue warp; the slot writes and
+    // the arrivals happen in lane 0.
+    auto publish = [&](int i, int w, int g) -> bool {
         const int slot = i % kRing;
         if (i >= kRing && !ctl.wait_all(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
             return false;
         if (lane == 0) {
             st_shared_u32(ring_w0 + 4 * slot, static_cast<uint32_t>(w));
+            st_shared_u32(ring_g0 + 4 * slot, static_cast<uint32_t>(g));
             if constexpr (CG == 2) {
                 st_cluster_u32(mapa(ring_w0 + 4 * slot, 1u), static_cast<uint32_t>(w));
+                st_cluster_u32(mapa(ring_g0 + 4 * slot, 1u), static_cast<uint32_t>(g));
                 mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
             }
             mbar_arrive(ring_full0 + 8 * slot);
@@ -409,13 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         return true;
     };
-    auto ring_read = [&](int i, int &w, bool whole_warp) -> bool {
+    auto ring_read = [&](int i, int &w, int &g, bool whole_warp) -> bool {
         const int slot = i % kRing;
         const uint32_t par = (i / kRing) & 1;
         if (!(whole_warp ? ctl.wait_all(ring_full0 + 8 * slot, par, WHERE_RING_FULL)
                          : ctl.wait(ring_full0 + 8 * slot, par, WHERE_RING_FULL)))
             return false;
         w = static_cast<int>(ld_shared_u32(ring_w0 + 4 * slot));
+        g = static_cast<int>(ld_shared_u32(ring_g0 + 4 * slot));
         if (CG == 2 && !leader)
             mbar_arrive_cluster_if(one, mapa(ring_empty0 + 8 * slot, 0u));
         else
@@ -431,9 +476,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
+        int maps_of = -1;   // the problem whose maps this thread has acquired (grouped launch)
         auto load_tile = [&](const WorkTile &t) -> bool {
             int ya, yb;
-            const CUtensorMap *mb = boxes(t, ya, yb);
+            const CUtensorMap *ma;
+            const CUtensorMap *mb = boxes(t, ya, yb, ma);
+            if (grouped && t.g != maps_of) {
+                tmap_acquire(one, ma);
+                tmap_acquire(one, mb);
+                maps_of = t.g;
+            }
             // a stage holds KBS k-blocks (the last stage of an item may hold fewer)
             for (int kb = t.kb_begin; kb < t.kb_end; kb += KBS) {
                 if (!ctl.wait_all(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
@@ -448,14 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (CG == 1) {
                     mbar_arrive_expect_tx_if(one, fb, tx);
                     for (int j = 0; j < nk; ++j) {
-                        tma_load_2d(go, sA + stage * SA + j * (SA / KBS), &tmA, fb, (kb + j) * KELEMS, ya);
+                        tma_load_2d(go, sA + stage * SA + j * (SA / KBS), ma, fb, (kb + j) * KELEMS, ya);
                         tma_load_2d(go, sB + stage * SB + j * (SB / KBS), mb, fb, (kb + j) * KELEMS, yb);
                     }
                 } else {
                     mbar_arrive_expect_tx_if(leader ? one : 0u, fb, tx);
                     const uint32_t fbc = mapa(fb, 0u);
                     for (int j = 0; j < nk; ++j) {
-                        tma_load_2d_pair(go, sA + stage * SA + j * (SA / KBS), &tmA, fbc, (kb + j) * KELEMS, ya);
+                        tma_load_2d_pair(go, sA + stage * SA + j * (SA / KBS), ma, fbc, (kb + j) * KELEMS, ya);
                         tma_load_2d_pair(go, sB + stage * SB + j * (SB / KBS), mb, fbc, (kb + j) * KELEMS, yb);
                     }
                 }
@@ -463,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // L2, so that a stage rarely waits on an HBM miss
                 const int kp = kb + p.prefetch_kb;
                 if (p.prefetch_kb > 0 && kp < t.kb_end) {
-                    tma_prefetch_2d(one, &tmA, kp * KELEMS, ya);
+                    tma_prefetch_2d(one, ma, kp * KELEMS, ya);
                     tma_prefetch_2d(one, mb, kp * KELEMS, yb);
                 }
                 ++issued;
@@ -497,9 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int pieces = unit_items(u, p);
+                const int g = grouped ? group_of(u, p) : 0;   // (a grouped launch's units are tiles)
                 for (int j = 0; ok && j < pieces; ++j) {
                     const int w = unit_item(u, j, pieces, p);
-                    ok = publish(i++, w) && load_tile(work_tile(w, p));
+                    ok = publish(i++, w, g) && load_tile(work_tile(w, g, p));
                 }
                 if (!ok) break;
                 int next = -1;
@@ -529,17 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 u = next;
             }
-            if (ok) ok = publish(i, -1);
+            if (ok) ok = publish(i, -1, 0);
             if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
         } else {
             for (int i = 0;; ++i) {
-                int w;
-                if (!ring_read(i, w, true)) {
+                int w, g;
+                if (!ring_read(i, w, g, true)) {
                     ok = false;
                     break;
                 }
                 if (w < 0) break;
-                if (!load_tile(work_tile(w, p))) {
+                if (!load_tile(work_tile(w, g, p))) {
                     ok = false;
                     break;
                 }
@@ -574,13 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_stage = -1;
             uint32_t last_phase = 0;
             for (int i = 0;; ++i) {
-                int w;
-                if (!ring_read(i, w, true) || w < 0) break;
+                int w, g;
+                if (!ring_read(i, w, g, true) || w < 0) break;
                 if (!ctl.wait_all(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
                 if (p.records != nullptr && lane == 0)
                     p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
-                const WorkTile t = work_tile(w, p);
+                const WorkTile t = work_tile(w, g, p);
                 const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
@@ -629,14 +682,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t nstore = 0;
+        int maps_of = -1;   // the problem whose C map this warp's lane 0 has acquired (grouped launch)
         for (int i = 0;; ++i) {
-            int w = 0;
+            int w = 0, g = 0;
             int ok = 1;
-            if (lane == 0) ok = ring_read(i, w, false) ? 1 : 0;
+            if (lane == 0) ok = ring_read(i, w, g, false) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             w = __shfl_sync(0xffffffffu, w, 0);
+            g = __shfl_sync(0xffffffffu, g, 0);
             if (!ok || w < 0) break;
-            const WorkTile t = work_tile(w, p);
+            const WorkTile t = work_tile(w, g, p);
+            // the item's output: its problem's C map, sizes and scale
+            const CUtensorMap *mc = &tmC;
+            int cM = p.M, cN = p.N;
+            float oscale = p.out_scale;
+            if (grouped) {
+                const GroupDesc *d = p.groups + g;
+                mc = &d->tmC;
+                cM = __ldg(&d->M);
+                cN = __ldg(&d->N);
+                oscale = __ldg(&d->out_scale);
+                if (g != maps_of) {
+                    tmap_acquire(one, mc);
+                    maps_of = g;
+                }
+            }
+            // K = 0 (a grouped launch's empty problem): nothing was accumulated,
+            // the tile is the empty sum
+            const bool empty_sum = t.kb_begin == t.kb_end;
             if (lane == 0) ok = ctl.wait(acc_full0 + 8 * acc, acc_phase, WHERE_ACC_FULL) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -645,7 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rec != nullptr) {
                 atomicAdd(&rec->visits, 1u);
                 if (leader) {
-                    rec->tile = static_cast<uint32_t>(t.tm * p.tiles_n + t.tn);
+                    rec->tile = static_cast<uint32_t>(t.idx);
+                    rec->group = static_cast<uint32_t>(g);
                     rec->n_off = static_cast<uint32_t>(t.n_off);
                     rec->n_len = static_cast<uint32_t>(t.n_len);
                     rec->kb_begin = static_cast<uint32_t>(t.kb_begin);
@@ -714,6 +788,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
                 tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols + 32, v1);
                 tmem_wait_ld();
+                if (empty_sum) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v0[j] = v1[j] = 0u;
+                }
                 if (c + 1 == chunks) {
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
@@ -757,19 +835,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[32];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    pk[j] = pack2<KIND>(v0[2 * j], v0[2 * j + 1], p.out_scale);
-                    pk[16 + j] = pack2<KIND>(v1[2 * j], v1[2 * j + 1], p.out_scale);
+                    pk[j] = pack2<KIND>(v0[2 * j], v0[2 * j + 1], oscale);
+                    pk[16 + j] = pack2<KIND>(v1[2 * j], v1[2 * j + 1], oscale);
                 }
                 const int col = t.tn * kTileN + t.n_off + c * kEpiChunkCols;
                 if (p.epi_direct) {
                     // this lane's row: 64 outputs = 8 x 16 bytes, straight to global
                     const int row = row0 + static_cast<int>(lane);
-                    if (row < p.M) {
+                    if (row < cM) {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c_ptr)
-                                                               + static_cast<long long>(row) * p.N + col);
+                                                               + static_cast<long long>(row) * cN + col);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            if (col + 8 * j < p.N)
+                            if (col + 8 * j < cN)
                                 dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     }
                     continue;
@@ -788,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                tma_store_2d_if((row0 < p.M && col < p.N) ? one : 0u, &tmC, buf, col, row0);
+                tma_store_2d_if((row0 < cM && col < cN) ? one : 0u, mc, buf, col, row0);
                 bulk_commit();   // (an empty group in lanes 1-31)
                 ++nstore;
             }

@@ -1,6 +1,8 @@
 // Kernel parameters and compile-time tile geometry shared by the launcher
 // and the kernels (host and device).
 #pragma once
+#include <cuda.h>
+
 #include <cstdint>
 
 namespace pts {
@@ -34,8 +36,21 @@ enum : uint32_t { DBG_RECORDS = 0x1u, DBG_CLC_STOP_AT = 0x2u, DBG_FAULT_SKIP_TMA
 // MMA thread starting the item, the epilogue seeing its accumulator complete,
 // the epilogue having issued the item's last store.
 struct TileRecord {
-    uint32_t visits, tile, n_off, n_len, owner, iter, smid, t_mma_start, t_acc_full, t_stored, kb_begin, kb_end;
+    uint32_t visits, tile, n_off, n_len, owner, iter, smid, t_mma_start, t_acc_full, t_stored, kb_begin, kb_end,
+        group;
 };
+
+// One problem of a grouped launch, in the device table the launcher fills:
+// its tensor maps (A: boxes of 128 rows, B: boxes of 256/CG rows, C: the
+// epilogue's 32 x 64 store box; A and B unused when K = 0), its sizes in
+// tiles and k-blocks, and its output scale.  512 bytes (tensor maps are
+// 128-byte aligned).
+struct GroupDesc {
+    CUtensorMap tmA, tmB, tmC;
+    int32_t M, N, num_kb, tiles_m, tiles_n;
+    float out_scale;
+};
+static_assert(sizeof(GroupDesc) == 512, "problem table entry");
 
 struct GemmParams {
     int32_t M, N, K;
@@ -62,6 +77,14 @@ struct GemmParams {
     float *ws_partial;          // stream-K partial accumulators (fixup workspace), or null
     uint32_t *ws_sync;          // stream-K claim counters and ready flags, 4 words per (tile, CTA, warp)
     TileRecord *records;        // num_work entries, or null
+    // Grouped launch (num_groups > 0): work id w is tile w - group_start[g] of
+    // problem g, where group_start[g] <= w < group_start[g + 1], numbered in
+    // grouped order within the problem; M, N, K, num_kb, tiles_m, tiles_n,
+    // out_scale and the kernel's own tensor maps are then unused.  No
+    // stream-K share and no column slices.
+    int32_t num_groups;
+    const GroupDesc *groups;    // num_groups entries (device)
+    const int32_t *group_start; // num_groups + 1 entries (device), group_start[0] = 0
 };
 
 // Floats of one stream-K partial: a CTA's 128 x 256 fp32 accumulator.
@@ -157,7 +180,7 @@ __host__ __device__ constexpr int smem_bytes(int cg, int stages)
     return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg)) + epi_bytes()
            + 8 * (2 * kMaxStages + 4 + 2 * kRing + 1)    // mbarriers
            + 16                                          // CLC response
-           + 4 * kRing + 16;                             // ring payload, TMEM base, abort flag
+           + 8 * kRing + 16;                             // ring payload, TMEM base, abort flag
 }
 
 }  // namespace pts

@@ -131,6 +131,17 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Order this thread's later uses of the 128-byte tensor map at `tmap` (in
+// global memory) after the generic-proxy writes that filled it, such as a
+// table the host rewrote between launches.  Only where `pred` is non-zero.
+__device__ __forceinline__ void tmap_acquire(uint32_t pred, const void *tmap)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q fence.proxy.tensormap::generic.acquire.gpu [%1], 128;\n\t}" ::"r"(pred),
+                 "l"(tmap)
+                 : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory; completion is signalled on
 // `bar` (shared::cta address of this CTA).
 // (Only in the lanes where `pred` is non-zero.)

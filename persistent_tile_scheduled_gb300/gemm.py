@@ -23,8 +23,9 @@ GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
             "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc",
-            "gemm_run_host_batch")
+            "gemm_run_host_batch", "gemm_run_grouped", "gemm_query_grouped")
 GEMM_NOALLOC_MAX_WORK_ITEMS = 16384
+GEMM_GROUPED_MAX_PROBLEMS = 65536
 
 
 class gemm_opts_t(ctypes.Structure):
@@ -38,7 +39,8 @@ class gemm_tile_record_t(ctypes.Structure):
     _fields_ = [("visits", ctypes.c_uint32), ("tile", ctypes.c_uint32), ("n_off", ctypes.c_uint32),
                 ("n_len", ctypes.c_uint32), ("owner", ctypes.c_uint32), ("iter", ctypes.c_uint32),
                 ("smid", ctypes.c_uint32), ("t_mma_start", ctypes.c_uint32), ("t_acc_full", ctypes.c_uint32),
-                ("t_stored", ctypes.c_uint32), ("kb_begin", ctypes.c_uint32), ("kb_end", ctypes.c_uint32)]
+                ("t_stored", ctypes.c_uint32), ("kb_begin", ctypes.c_uint32), ("kb_end", ctypes.c_uint32),
+                ("group", ctypes.c_uint32)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
@@ -53,6 +55,12 @@ class gemm_launch_info_t(ctypes.Structure):
 class gemm_host_problem_t(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("A", ctypes.c_void_p),
                 ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("dtype", ctypes.c_int), ("scale_a", ctypes.c_float),
+                ("scale_b", ctypes.c_float)]
+
+
+class gemm_group_problem_t(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("A", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("scale_a", ctypes.c_float),
                 ("scale_b", ctypes.c_float)]
 
 
@@ -89,6 +97,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gemm_run_host_batch.restype = st
     lib.gemm_query.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(gemm_launch_info_t)]
     lib.gemm_query.restype = st
+    lib.gemm_run_grouped.argtypes = [vp, ctypes.POINTER(gemm_group_problem_t), i64, ctypes.c_int, ctypes.c_int, vp]
+    lib.gemm_run_grouped.restype = st
+    lib.gemm_query_grouped.argtypes = [vp, ctypes.POINTER(gemm_group_problem_t), i64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(gemm_launch_info_t)]
+    lib.gemm_query_grouped.restype = st
     lib.gemm_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     lib.gemm_check.restype = st
     lib.gemm_read_debug.argtypes = [vp, vp, ctypes.POINTER(gemm_tile_record_t), i64, ctypes.POINTER(ctypes.c_int)]
@@ -163,6 +176,29 @@ def gemm_run_host_batch(h, problems, sched, stream=None) -> int:
         arr[i] = gemm_host_problem_t(M, N, K, _ptr(A), _ptr(B), _ptr(C), int(dt), float(sa), float(sb))
     return _check(load().gemm_run_host_batch(h, arr, len(problems), int(sched), _stream(stream)),
                   "gemm_run_host_batch")
+
+
+def _group_array(problems):
+    arr = (gemm_group_problem_t * max(len(problems), 1))()
+    for i, q in enumerate(problems):
+        M, N, K, A, B, C = q[:6]
+        sa, sb = (q[6], q[7]) if len(q) > 6 else (1.0, 1.0)
+        arr[i] = gemm_group_problem_t(M, N, K, _ptr(A), _ptr(B), _ptr(C), float(sa), float(sb))
+    return arr
+
+
+def gemm_run_grouped(h, problems, dtype, sched, stream=None) -> int:
+    """problems: sequence of (M, N, K, A, B, C[, scale_a, scale_b]) with
+    device tensors or raw device addresses; one launch for all of them."""
+    return _check(load().gemm_run_grouped(h, _group_array(problems), len(problems), int(dtype), int(sched),
+                                          _stream(stream)), "gemm_run_grouped")
+
+
+def gemm_query_grouped(h, problems, dtype, sched) -> gemm_launch_info_t:
+    info = gemm_launch_info_t()
+    _check(load().gemm_query_grouped(h, _group_array(problems), len(problems), int(dtype), int(sched),
+                                     ctypes.byref(info)), "gemm_query_grouped")
+    return info
 
 
 def gemm_query(h, M, N, K, dtype, sched) -> gemm_launch_info_t:

@@ -77,7 +77,10 @@ def test_struct_layouts_match_the_header():
     int main(void) {
       printf("%zu %zu %zu %zu\n", sizeof(gemm_opts_t), offsetof(gemm_opts_t, debug_flags),
              offsetof(gemm_opts_t, fault_arg), offsetof(gemm_opts_t, timeout_ns));
-      printf("%zu %zu\n", sizeof(gemm_tile_record_t), offsetof(gemm_tile_record_t, smid));
+      printf("%zu %zu %zu\n", sizeof(gemm_tile_record_t), offsetof(gemm_tile_record_t, smid),
+             offsetof(gemm_tile_record_t, group));
+      printf("%zu %zu %zu %zu\n", sizeof(gemm_group_problem_t), offsetof(gemm_group_problem_t, A),
+             offsetof(gemm_group_problem_t, scale_a), (size_t)GEMM_GROUPED_MAX_PROBLEMS);
       printf("%zu %zu %zu %zu\n", sizeof(gemm_launch_info_t), offsetof(gemm_launch_info_t, tiles_m),
              offsetof(gemm_launch_info_t, grid_ctas), offsetof(gemm_launch_info_t, threads));
       printf("%zu %zu %zu\n", offsetof(gemm_launch_info_t, sk_tiles), offsetof(gemm_launch_info_t, work_items),
@@ -94,7 +97,9 @@ def test_struct_layouts_match_the_header():
     got = [int(v) for v in out]
     want = [ctypes.sizeof(g.gemm_opts_t), g.gemm_opts_t.debug_flags.offset, g.gemm_opts_t.fault_arg.offset,
             g.gemm_opts_t.timeout_ns.offset,
-            ctypes.sizeof(g.gemm_tile_record_t), g.gemm_tile_record_t.smid.offset,
+            ctypes.sizeof(g.gemm_tile_record_t), g.gemm_tile_record_t.smid.offset, g.gemm_tile_record_t.group.offset,
+            ctypes.sizeof(g.gemm_group_problem_t), g.gemm_group_problem_t.A.offset,
+            g.gemm_group_problem_t.scale_a.offset, g.GEMM_GROUPED_MAX_PROBLEMS,
             ctypes.sizeof(g.gemm_launch_info_t), g.gemm_launch_info_t.tiles_m.offset,
             g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset,
             g.gemm_launch_info_t.sk_tiles.offset, g.gemm_launch_info_t.work_items.offset,

@@ -183,3 +183,25 @@ def test_stream_k_partition_and_balance(T, G, num_kb):
         load[u % G] += sum(it[5] - it[4] for it in its)
     assert max(load) - min(load) <= 1
     assert sum(load) == T * num_kb
+
+
+def test_grouped_items_hand_worked():
+    """Problems (300, 600), (0, 512), (128, 100) with 128 x 256 tiles and
+    GROUP_SIZE_M = 2: the first has a 3 x 3 tile grid (rows 0-1 walked column
+    by column, then row 2), the second none, the third one tile."""
+    got = sm.grouped_items([(300, 600), (0, 512), (128, 100)], 128, 256, 2)
+    assert got == [(0, 0, 0), (0, 1, 0), (0, 0, 1), (0, 1, 1), (0, 0, 2), (0, 1, 2),
+                   (0, 2, 0), (0, 2, 1), (0, 2, 2), (2, 0, 0)]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_grouped_items_cover_every_problem_tile_once(seed):
+    rng = random.Random(seed)
+    probs = [(rng.choice([0, 1, 127, 128, 129, 700]), rng.choice([0, 8, 256, 264, 1000])) for _ in range(12)]
+    items = sm.grouped_items(probs, 256, 256, 8)
+    want = {(g, tm, tn) for g, (M, N) in enumerate(probs) if M and N
+            for tm in range(sm.cdiv(M, 256)) for tn in range(sm.cdiv(N, 256))}
+    assert len(items) == len(want) and set(items) == want
+    # problems in order, each a contiguous run
+    gs = [g for g, _, _ in items]
+    assert gs == sorted(gs)

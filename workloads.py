@@ -16,6 +16,10 @@ square fp16 case, an fp8 case and tail-effect shapes):
   e4m3_8192         M=N=K=8192, A,B ~ N(0,1), scaled per tensor so max|x| = 448,
                     rounded to e4m3; C in bf16 with the dequant scale applied
   bf16_tail         (5120,5120,4096), (4224,3968,2048), (19200,256,8192)
+  bf16_grouped_vark 64 problems of M=N=1024 in one grouped launch, K log-uniform
+                    in [256, 8192] (multiples of 8), A,B ~ N(0,1)/sqrt(K): tiles
+                    whose cost varies 32-fold, where a dynamic scheduler can
+                    balance what a static one cannot
 
 A is M x K row-major; B is stored N x K row-major (K x N column-major).
 """
@@ -68,12 +72,24 @@ def bf16_tail() -> List[Problem]:
             for i, (m, n, k) in enumerate(shapes)]
 
 
+def bf16_grouped_vark(count: int = 64, M: int = 1024, N: int = 1024, seed: int = 6000) -> List[Problem]:
+    """`count` bf16 problems of M x N whose K differ: K = 8 * round(2^u / 8)
+    with u ~ U[8, 13] drawn by a generator seeded `seed` (problem i's inputs
+    are seeded seed + 1 + i)."""
+    gen = torch.Generator().manual_seed(seed)
+    u = torch.rand(count, generator=gen, dtype=torch.float64) * 5.0 + 8.0
+    ks = [max(8, 8 * int(round(2.0 ** float(x) / 8.0))) for x in u]
+    return [Problem(f"bf16_grouped_{i}_{M}x{N}x{k}", M, N, k, BF16, "normal_sqrtk", seed + 1 + i)
+            for i, k in enumerate(ks)]
+
+
 WORKLOADS = {
     "fp16_512": fp16_512,
     "fp16_4096_ksweep": fp16_4096_ksweep,
     "bf16_8192_ksweep": bf16_8192_ksweep,
     "e4m3_8192": e4m3_8192,
     "bf16_tail": bf16_tail,
+    "bf16_grouped_vark": bf16_grouped_vark,
 }
 
 
