@@ -502,6 +502,7 @@ def extra_configs(pts, dev, stream):
             pts.gemm_destroy(hs[1])
         out["concurrent_" + pa.name + "+" + pb.name] = conc
         out["half_occupied"] = half_occupied(pts, dev, stream)
+        out["bf16_grouped_vark"] = grouped_vark(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
     out["note"] = ("library's CTA group per GEMM (pairs from 40 k-blocks per tile); median of back-to-back "
@@ -554,6 +555,49 @@ def half_occupied(pts, dev, stream, reps=6):
         pts.gemm_destroy(hm)
     out["note"] = (f"time from the occupier's start ({occ.name}, {half} CTAs, one wave) to the end of the "
                    f"measured GEMM ({main.name}, single CTAs), launched 25 us after the occupier")
+    return out
+
+
+def grouped_vark(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)):
+    """The grouped workload (64 bf16 problems of M=N=1024, K log-uniform in
+    [256, 8192]) in ONE launch per scheduler and CTA group: TFLOP/s over all
+    problems' flops, median of back-to-back launches (the same problem list
+    each time, so the problem table is uploaded once)."""
+    probs = wl.bf16_grouped_vark()
+    ins = [device_inputs(p, 8000 + i) for i, p in enumerate(probs)]
+    Cs = [torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda") for p in probs]
+    lst = [(p.M, p.N, p.K, A, B, C) for p, (A, B, _, _), C in zip(probs, ins, Cs)]
+    flops = sum(gemm_flops(p.M, p.N, p.K) for p in probs)
+    ks = [p.K for p in probs]
+    out = {"problems": len(probs), "M": probs[0].M, "N": probs[0].N, "K_min": min(ks), "K_max": max(ks),
+           "K_mean": round(sum(ks) / len(ks), 1)}
+    for cg in cgs:
+        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
+        try:
+            for si, name in enumerate(SCHED_NAMES):
+                if name not in scheds:
+                    continue
+                for _ in range(3):
+                    pts.gemm_run_grouped(h, lst, wl.BF16, si, stream)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                with torch.cuda.stream(stream):
+                    for r in range(reps):
+                        ev[r].record(stream)
+                        pts.gemm_run_grouped(h, lst, wl.BF16, si, stream)
+                    ev[reps].record(stream)
+                torch.cuda.synchronize()
+                if pts.gemm_check(h, stream)[0] != 0:
+                    raise RuntimeError("device error in the grouped run")
+                ms = statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+                out[f"cg{cg}_{name}"] = round(flops / (ms * 1e-3) / 1e12, 1)
+        finally:
+            pts.gemm_destroy(h)
+    h = pts.gemm_create(dev, None)
+    try:
+        out["auto_cta_group"] = int(pts.gemm_query_grouped(h, lst, wl.BF16, 1).cta_group)
+    finally:
+        pts.gemm_destroy(h)
+    out["note"] = f"median of {reps} back-to-back grouped launches; TFLOP/s over all {len(probs)} problems"
     return out
 
 
@@ -654,6 +698,9 @@ def main():
                     help="only the 8192^3 measurement (for profiling it), restricted by --cta-group, --scheds "
                          "and --square-dtype; prints its numbers, not the benchmark line")
     ap.add_argument("--square-dtype", choices=["bf16", "e4m3"], default="bf16")
+    ap.add_argument("--grouped-only", action="store_true",
+                    help="only the grouped 64-problem measurement (for profiling it), restricted by --cta-group and "
+                         "--scheds; prints its numbers, not the benchmark line")
     args = ap.parse_args()
     if args.square_only:
         import persistent_tile_scheduled_gb300 as pts
@@ -661,6 +708,13 @@ def main():
         out = square_8192(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
                           scheds=tuple(args.scheds), dtype=args.square_dtype)
         print(json.dumps({f"square_8192_{args.square_dtype}": out}), flush=True)
+        return
+    if args.grouped_only:
+        import persistent_tile_scheduled_gb300 as pts
+        pts.load(build_if_missing=False)
+        out = grouped_vark(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
+                           scheds=tuple(args.scheds))
+        print(json.dumps({"bf16_grouped_vark": out}), flush=True)
         return
     if args.warmup < 3:
         log("warm-up raised to 3 steps")

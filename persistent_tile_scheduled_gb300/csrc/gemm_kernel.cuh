@@ -6,19 +6,19 @@
 // (128*CG) x 256 output tile at a time.  Warp roles:
 //   warp 0     producer: TMA loads of A and B k-blocks into an S-stage
 //              shared-memory ring guarded by full/empty mbarriers (one k-block
-//              per stage for a single CTA, two for a pair); on the leader CTA
-//              it is also the scheduler (static arithmetic or Cluster Launch
-//              Control): it takes units, splits each into its work items and
-//              publishes their ids into a small broadcast ring read by every
-//              other role
+//              per stage for a single CTA, two for a pair)
 //   warp 1     MMA issuer (the leader CTA's warp, lane 0 issuing): tcgen05.mma
 //              into one of two 256-column TMEM accumulators, so the epilogue
 //              of item i overlaps the mainloop of item i+1
 //   warps 2-5  epilogue: tcgen05.ld -> (scale) -> fp16/bf16 -> swizzled
 //              shared-memory staging -> TMA store; for a tile cut in two by
 //              the stream-K share, the fp32 partial fixup
-// The producer and MMA warps run their loops with all 32 lanes in step and
-// issue through predicated instructions from lane 0.
+//   warp 6     scheduler (the leader CTA's): static arithmetic or Cluster
+//              Launch Control; it takes units, splits each into its work
+//              items and publishes their ids into a small broadcast ring read
+//              by every other role, one item ahead of the producer
+// The producer, MMA and scheduler warps run their loops with all 32 lanes in
+// step and issue through predicated instructions from lane 0.
 //
 // Scheduling follows "Persistent Kernels with Cluster Launch Control": a
 // static scheduler derives later units in software (u, u+G, u+2G, ...); a CLC
@@ -52,6 +52,7 @@ enum : int32_t {
     WHERE_CLC = 7,          // scheduler waiting for a CLC response
     WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
     WHERE_FIXUP = 9,        // the second piece of a cut tile waiting for the first's partial
+    WHERE_STARTED = 10,     // scheduler waiting for the producer to start the item it published
 };
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
@@ -341,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_full0 = acc_empty0 + 16;             // + 8*r
     const uint32_t ring_empty0 = ring_full0 + 8 * kRing;     // + 8*r
     const uint32_t clc_bar = ring_empty0 + 8 * kRing;
-    const uint32_t clc_resp = (clc_bar + 8 + 15) & ~15u;
+    const uint32_t started_bar = clc_bar + 8;                // producer (leader) starts an item
+    const uint32_t clc_resp = (started_bar + 8 + 15) & ~15u;
     const uint32_t ring_w0 = clc_resp + 16;                  // + 4*r: work id
     const uint32_t ring_g0 = ring_w0 + 4 * kRing;            // + 4*r: its problem (grouped launch)
     const uint32_t tmem_slot = ring_g0 + 4 * kRing;
@@ -371,9 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(ring_full0 + 8 * r, 1);
-            mbar_init(ring_empty0 + 8 * r, CG == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps);
+            // readers: the producer, MMA and epilogue warps of the leader, the
+            // producer and epilogue warps of the peer
+            mbar_init(ring_empty0 + 8 * r, CG == 1 ? 2 + kEpiWarps : 3 + 2 * kEpiWarps);
         }
         mbar_init(clc_bar, 1);
+        mbar_init(started_bar, 1);
         st_shared_u32(abort_flag, 0u);
         fence_mbar_init();
     }
@@ -433,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work-id broadcast ring -------------------------------------------
     // Slot r holds the id of work item i (i % kRing == r), or -1 = no more,
-    // and the item's problem g.  Both are called by whole converged warps
-    // (producer, MMA) or by lane 0 of an epilogue warp; the slot writes and
-    // the arrivals happen in lane 0.
+    // and the item's problem g.  publish is called by the whole scheduler
+    // warp, ring_read by whole converged warps (producer, MMA) or by lane 0
+    // of an epilogue warp; the slot writes and the arrivals happen in lane 0.
     auto publish = [&](int i, int w, int g) -> bool {
         const int slot = i % kRing;
         if (i >= kRing && !ctl.wait_all(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
@@ -469,15 +474,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 0) {
-        // =========================== producer / scheduler ======================
+        // =============================== producer ==============================
         // All 32 lanes run this loop in step (every branch below is uniform
-        // across the warp); lane 0 issues the loads and the CLC requests.
+        // across the warp); lane 0 issues the loads.  Work items come from
+        // the broadcast ring; on the leader CTA, the producer tells the
+        // scheduler warp when it starts each one.
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
-        int maps_of = -1;   // the problem whose maps this thread has acquired (grouped launch)
-        auto load_tile = [&](const WorkTile &t) -> bool {
+        int maps_of = -1;   // grouped launch: the problem whose A and B maps this thread last acquired
+        // Load k-blocks [kb_from, kb_to) of work item t (kb_from is the
+        // item's first k-block or a stage boundary after it).
+        auto load_tile = [&](const WorkTile &t, int kb_from, int kb_to) -> bool {
             int ya, yb;
             const CUtensorMap *ma;
             const CUtensorMap *mb = boxes(t, ya, yb, ma);
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 maps_of = t.g;
             }
             // a stage holds KBS k-blocks (the last stage of an item may hold fewer)
-            for (int kb = t.kb_begin; kb < t.kb_end; kb += KBS) {
+            for (int kb = kb_from; kb < kb_to; kb += KBS) {
                 if (!ctl.wait_all(empty0 + 8 * stage, phase ^ 1u, WHERE_EMPTY)) return false;
                 const int nk = t.kb_end - kb < KBS ? t.kb_end - kb : KBS;
                 const uint32_t tx =
@@ -527,75 +536,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        bool clc_pending = false;
-        if (leader) {
-            // Units come from the scheduler; each is published as its pieces.
-            int u = cluster_id < p.num_units ? cluster_id : -1;
-            bool may_request = p.sched == SCHED_CLC;
-            uint32_t clc_phase = 0;
-            int i = 0;   // ring slot sequence
-            for (int n = 0; ok && u >= 0; ++n) {
-                if (may_request) {
-                    if ((p.debug_flags & DBG_CLC_STOP_AT) && n == p.fault_arg) {
-                        may_request = false;   // behave as if this request had failed
-                    } else {
-                        if (lane == 0) {
-                            fence_proxy_async_smem();   // earlier reads of the slot before the async write
-                            mbar_arrive_expect_tx(clc_bar, 16);
-                            clc_try_cancel(clc_resp, clc_bar);
-                        }
-                        __syncwarp();
-                        clc_pending = true;
-                    }
-                }
-                const int pieces = unit_items(u, p);
-                const int g = grouped ? group_of(u, p) : 0;   // (a grouped launch's units are tiles)
-                for (int j = 0; ok && j < pieces; ++j) {
-                    const int w = unit_item(u, j, pieces, p);
-                    ok = publish(i++, w, g) && load_tile(work_tile(w, g, p));
-                }
-                if (!ok) break;
-                int next = -1;
-                if (p.sched == SCHED_STATIC) {
-                    next = (u + num_clusters < p.num_units) ? u + num_clusters : -1;
-                } else if (clc_pending) {
-                    if (!ctl.wait_all(clc_bar, clc_phase, WHERE_CLC)) {
-                        ok = false;
-                        break;
-                    }
-                    clc_phase ^= 1u;
-                    clc_pending = false;
-                    // only lane 0 reads the response slot (it alone re-arms it)
-                    uint32_t x = 0, got = 0;
-                    if (lane == 0) got = clc_decode(clc_resp, x) ? 1u : 0u;
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    x = __shfl_sync(0xffffffffu, x, 0);
-                    if (got) {
-                        next = static_cast<int>(x / CG);
-                        if (next >= p.num_units) {   // cannot happen for a well-formed grid
-                            ctl.fail(WHERE_BAD_TILE);
-                            next = -1;
-                        }
-                    } else {
-                        may_request = false;   // a failed request is never repeated
-                    }
-                }
-                u = next;
+        for (int i = 0;; ++i) {
+            int w, g;
+            if (!ring_read(i, w, g, true)) {
+                ok = false;
+                break;
             }
-            if (ok) ok = publish(i, -1, 0);
-            if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
-        } else {
-            for (int i = 0;; ++i) {
-                int w, g;
-                if (!ring_read(i, w, g, true)) {
-                    ok = false;
-                    break;
-                }
-                if (w < 0) break;
-                if (!load_tile(work_tile(w, g, p))) {
-                    ok = false;
-                    break;
-                }
+            if (w < 0) break;
+            if (leader) mbar_arrive_if(one, started_bar);
+            const WorkTile t = work_tile(w, g, p);
+            if (!load_tile(t, t.kb_begin, t.kb_end)) {
+                ok = false;
+                break;
             }
         }
         if (!ok) {
@@ -674,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (last_stage >= 0) ctl.drain(empty0 + 8 * last_stage, last_phase, 10000000ull);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // ============================== epilogue ===============================
         const uint32_t e = warp - 2;          // staging buffer owner index
         const uint32_t q = warp & 3u;         // TMEM lane quarter this warp may access
@@ -886,6 +838,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         // CTA's shared memory goes away (their writes to C complete with the
         // grid)
         bulk_wait_read<0>();
+        __syncwarp();
+    } else if (warp == kSchedWarp) {
+        // ============================== scheduler ==============================
+        // The leader CTA's whole warp runs this loop in step; lane 0 makes
+        // the CLC requests.  It takes units (static arithmetic, CLC, or the
+        // cluster's own for the non-persistent grid), splits each into its
+        // work items and publishes them into the broadcast ring one at a
+        // time: item i + 1 only once the producer has started item i.  The
+        // next unit is claimed when the producer starts a unit's first item
+        // (as late as the producer's lead allows, so that CLC still balances
+        // the last tiles), and decoded while the producer loads: the
+        // producer never waits on the scheduling arithmetic.
+        if (leader) {
+            bool ok = true;
+            bool clc_pending = false;
+            bool may_request = p.sched == SCHED_CLC;
+            uint32_t clc_phase = 0;
+            int maps_of = -1;   // grouped launch: the problem whose maps this thread last acquired
+            // The unit after `cur` (-1: none): static arithmetic, or the
+            // answer to the CLC request made when `cur` started.  False on a
+            // failed wait.
+            auto next_unit = [&](int cur, int &next) -> bool {
+                next = -1;
+                if (p.sched == SCHED_STATIC) {
+                    next = (cur + num_clusters < p.num_units) ? cur + num_clusters : -1;
+                } else if (clc_pending) {
+                    if (!ctl.wait_all(clc_bar, clc_phase, WHERE_CLC)) return false;
+                    clc_phase ^= 1u;
+                    clc_pending = false;
+                    // only lane 0 reads the response slot (it alone re-arms it)
+                    uint32_t x = 0, got = 0;
+                    if (lane == 0) got = clc_decode(clc_resp, x) ? 1u : 0u;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    x = __shfl_sync(0xffffffffu, x, 0);
+                    if (got) {
+                        next = static_cast<int>(x / CG);
+                        if (next >= p.num_units) {   // cannot happen for a well-formed grid
+                            ctl.fail(WHERE_BAD_TILE);
+                            next = -1;
+                        }
+                    } else {
+                        may_request = false;   // a failed request is never repeated
+                    }
+                }
+                return true;
+            };
+            // Grouped launch: the next tile belongs to another problem, whose
+            // tensor maps and operands are not on chip yet.  Bring its maps
+            // (A and B, C) into the descriptor cache and its first stages'
+            // k-blocks (both CTAs' boxes) into L2 before the producer needs them.
+            auto warm = [&](const WorkTile &t) {
+                int ya, yb;
+                const CUtensorMap *ma;
+                const CUtensorMap *mb = boxes(t, ya, yb, ma);
+                const bool has_k = t.kb_end > t.kb_begin;   // (a problem with K = 0 has no A and B maps)
+                if (t.g != maps_of && has_k) {
+                    tmap_acquire(one, ma);
+                    tmap_acquire(one, mb);
+                    maps_of = t.g;
+                }
+                if (lane == 0) {
+                    if (has_k) {
+                        prefetch_tmap(ma);
+                        prefetch_tmap(mb);
+                    }
+                    prefetch_tmap(&p.groups[t.g].tmC);
+                }
+                __syncwarp();
+                const int kb_end = t.kb_end < t.kb_begin + S * KBS ? t.kb_end : t.kb_begin + S * KBS;
+                for (int kb = t.kb_begin; kb < kb_end; ++kb) {
+#pragma unroll
+                    for (int r = 0; r < CG; ++r) {
+                        tma_prefetch_2d(one, ma, kb * KELEMS, ya + r * kRowsPerCta);
+                        tma_prefetch_2d(one, mb, kb * KELEMS, yb + r * (t.n_len / CG));
+                    }
+                }
+            };
+            int u = cluster_id < p.num_units ? cluster_id : -1;
+            int g = grouped && u >= 0 ? group_of(u, p) : 0;   // (a grouped launch's units are tiles)
+            int i = 0;   // ring slot sequence = work items published
+            for (int n = 0; ok && u >= 0; ++n) {
+                const int pieces = unit_items(u, p);
+                for (int j = 0; ok && j < pieces; ++j) {
+                    ok = publish(i, unit_item(u, j, pieces, p), g)
+                         && ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED);
+                    ++i;
+                    if (ok && j == 0 && may_request) {
+                        // the producer has begun this unit: claim the one after it
+                        if ((p.debug_flags & DBG_CLC_STOP_AT) && n == p.fault_arg) {
+                            may_request = false;   // behave as if this request had failed
+                        } else {
+                            if (lane == 0) {
+                                fence_proxy_async_smem();   // earlier reads of the slot before the async write
+                                mbar_arrive_expect_tx(clc_bar, 16);
+                                clc_try_cancel(clc_resp, clc_bar);
+                            }
+                            __syncwarp();
+                            clc_pending = true;
+                        }
+                    }
+                }
+                int next = -1;
+                if (!ok || !next_unit(u, next)) {
+                    ok = false;
+                    break;
+                }
+                if (grouped && next >= 0) {
+                    g = group_of(next, p);
+                    warm(work_tile(unit_item(next, 0, 1, p), g, p));
+                }
+                u = next;
+            }
+            if (ok) publish(i, -1, 0);
+            if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
+        }
         __syncwarp();
     }
 

@@ -13,8 +13,9 @@ namespace pts {
 constexpr int kRowsPerCta = 128;
 constexpr int kTileN = 256;
 constexpr int kKBlockBytes = 128;
-constexpr int kThreads = 192;           // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreads = 224;           // warp 0 producer, warp 1 MMA, warps 2-5 epilogue, warp 6 scheduler
 constexpr int kEpiWarps = 4;
+constexpr int kSchedWarp = 2 + kEpiWarps;
 constexpr int kEpiChunkCols = 64;       // columns per epilogue TMA store (128 bytes of fp16/bf16)
 constexpr int kEpiRowsPerWarp = 32;
 constexpr int kEpiBufBytes = kEpiRowsPerWarp * kEpiChunkCols * 2;   // 4 KB
@@ -178,7 +179,7 @@ __host__ __device__ constexpr int epi_bytes() { return kEpiWarps * kEpiBufsPerWa
 __host__ __device__ constexpr int smem_bytes(int cg, int stages)
 {
     return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg)) + epi_bytes()
-           + 8 * (2 * kMaxStages + 4 + 2 * kRing + 1)    // mbarriers
+           + 8 * (2 * kMaxStages + 4 + 2 * kRing + 2)    // mbarriers
            + 16                                          // CLC response
            + 8 * kRing + 16;                             // ring payload, TMEM base, abort flag
 }
