@@ -571,33 +571,36 @@ def grouped_vark(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES
     ks = [p.K for p in probs]
     out = {"problems": len(probs), "M": probs[0].M, "N": probs[0].N, "K_min": min(ks), "K_max": max(ks),
            "K_mean": round(sum(ks) / len(ks), 1)}
+    arr = pts.gemm.group_array(lst)   # marshalled once: the timed loop makes only the C calls
     for cg in cgs:
-        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
-        try:
-            for si, name in enumerate(SCHED_NAMES):
-                if name not in scheds:
-                    continue
-                for _ in range(3):
-                    pts.gemm_run_grouped(h, lst, wl.BF16, si, stream)
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-                with torch.cuda.stream(stream):
-                    for r in range(reps):
-                        ev[r].record(stream)
-                        pts.gemm_run_grouped(h, lst, wl.BF16, si, stream)
-                    ev[reps].record(stream)
-                torch.cuda.synchronize()
-                if pts.gemm_check(h, stream)[0] != 0:
-                    raise RuntimeError("device error in the grouped run")
-                ms = statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
-                out[f"cg{cg}_{name}"] = round(flops / (ms * 1e-3) / 1e12, 1)
-        finally:
-            pts.gemm_destroy(h)
+        for order, suffix in ((1, ""), (2, "_given_order")):
+            h = pts.gemm_create(dev, pts.make_opts(cta_group=cg, group_order=order))
+            try:
+                for si, name in enumerate(SCHED_NAMES):
+                    if name not in scheds:
+                        continue
+                    for _ in range(3):
+                        pts.gemm_run_grouped(h, arr, wl.BF16, si, stream)
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                    with torch.cuda.stream(stream):
+                        for r in range(reps):
+                            ev[r].record(stream)
+                            pts.gemm_run_grouped(h, arr, wl.BF16, si, stream)
+                        ev[reps].record(stream)
+                    torch.cuda.synchronize()
+                    if pts.gemm_check(h, stream)[0] != 0:
+                        raise RuntimeError("device error in the grouped run")
+                    ms = statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+                    out[f"cg{cg}_{name}{suffix}"] = round(flops / (ms * 1e-3) / 1e12, 1)
+            finally:
+                pts.gemm_destroy(h)
     h = pts.gemm_create(dev, None)
     try:
         out["auto_cta_group"] = int(pts.gemm_query_grouped(h, lst, wl.BF16, 1).cta_group)
     finally:
         pts.gemm_destroy(h)
-    out["note"] = f"median of {reps} back-to-back grouped launches; TFLOP/s over all {len(probs)} problems"
+    out["note"] = (f"median of {reps} back-to-back grouped launches; TFLOP/s over all {len(probs)} problems; "
+                   "problems listed most k-blocks first (the default) or in the given order")
     return out
 
 

@@ -101,6 +101,9 @@ typedef struct gemm_opts {
     int epilogue;                   /* 0 = default (1); 1 = TMA stores from a swizzled shared-
                                        memory staging buffer; 2 = every lane stores its row's
                                        outputs straight from registers */
+    int group_order;                /* gemm_run_grouped's order of the problems in the work-id
+                                       list: 0 = default (1); 1 = most k-blocks first (stable:
+                                       equal K keep the given order); 2 = as given */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are numbered in grouped order (GROUP_SIZE_M tile-
@@ -143,8 +146,8 @@ typedef struct gemm_tile_record {
      * item's last store (leader CTA) */
     uint32_t t_mma_start, t_acc_full, t_stored;
     uint32_t kb_begin, kb_end;  /* k-block range of the item */
-    uint32_t group;    /* problem of the item in a grouped launch (0 otherwise); `tile` is then the
-                          tile index within that problem */
+    uint32_t group;    /* problem of the item in a grouped launch (its index in the caller's list;
+                          0 otherwise); `tile` is then the tile index within that problem */
 } gemm_tile_record_t;
 
 /* Launch shape chosen for a problem. */
@@ -239,13 +242,16 @@ typedef struct gemm_group_problem {
 #define GEMM_GROUPED_MAX_PROBLEMS 65536
 
 /* `count` independent GEMMs of one dtype in ONE launch.  The tiles of all
- * problems form one list of work ids (problem 0's tiles first, each problem's
- * in GROUP_SIZE_M-grouped order) that the scheduler hands out as it does one
- * problem's tiles; a tile costs time in proportion to its problem's K, so
- * the tiles differ in cost and a scheduler that hands out work as clusters
- * finish (CLC, or the hardware's for the non-persistent grid) can balance
- * what the static stride cannot ("Choosing between static and CLC
+ * problems form one list of work ids (problem by problem, each problem's
+ * tiles in GROUP_SIZE_M-grouped order) that the scheduler hands out as it
+ * does one problem's tiles; a tile costs time in proportion to its problem's
+ * K, so the tiles differ in cost and a scheduler that hands out work as
+ * clusters finish (CLC, or the hardware's for the non-persistent grid) can
+ * balance what the static stride cannot ("Choosing between static and CLC
  * scheduling": dynamic scheduling pays off when the work per tile varies).
+ * The problems are listed most k-blocks first (opts.group_order 1, the
+ * default; longest-processing-time-first list scheduling, so the last tiles
+ * handed out are the short ones) or in the given order (group_order 2).
  * No stream-K share and no column slices.  CTA group (cta_group 0): pairs
  * when the mean k-blocks per tile, weighted by output size, is at least 40.
  * The handle keeps the problem table (tensor maps and tile counts, 512 bytes

@@ -123,13 +123,20 @@ def record_slots(T: int, split: int = 1, sk_tiles: int = 0, sk_units: int = 0) -
     return T * split
 
 
-def grouped_items(problems, BM: int, BN: int, group_m: int) -> List[Tuple[int, int, int]]:
+def grouped_items(problems, BM: int, BN: int, group_m: int, kb=None) -> List[Tuple[int, int, int]]:
     """Work ids of a grouped launch (several independent GEMMs, one list of
-    tiles): ``(problem, tile-row, tile-col)`` per work id.  Problem 0's tiles
-    come first, each problem's in grouped order; a problem with M or N = 0
-    has no tiles.  ``problems``: sequence of (M, N)."""
+    tiles): ``(problem, tile-row, tile-col)`` per work id, problem by problem,
+    each problem's tiles in grouped order; a problem with M or N = 0 has no
+    tiles.  ``problems``: sequence of (M, N).  With ``kb`` (k-blocks per tile
+    of each problem) the problems are listed most k-blocks first, equal
+    counts in the given order (longest processing time first); without it,
+    in the given order."""
+    order = list(range(len(problems)))
+    if kb is not None:
+        order.sort(key=lambda g: -kb[g])   # list.sort is stable
     out = []
-    for g, (M, N) in enumerate(problems):
+    for g in order:
+        M, N = problems[g]
         if M == 0 or N == 0:
             continue
         Tm, Tn = tile_grid(M, N, BM, BN)

@@ -360,9 +360,11 @@ gemm_status_t check_group_problem(const gemm_group_problem_t &q, gemm_dtype_t dt
 }
 
 // Launch shape of a grouped launch, and (encode) its problem table: one
-// GroupDesc per problem, then the tile prefix sums group_start[0..count].
+// GroupDesc per problem in work-id order, then the tile prefix sums
+// group_start[0..count].
 struct GroupedPlan {
     Plan pl;
+    std::vector<int64_t> order;   // order[j] = the caller's index of the j-th problem of the work-id list
     std::vector<pts::GroupDesc> desc;
     std::vector<int32_t> start;
 };
@@ -387,13 +389,23 @@ gemm_status_t plan_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t c
     pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group
                                    : pts::choose_cta_group(w_sum > 0.0 ? int64_t(kb_sum / w_sum) : 0);
     const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
+    // work-id order of the problems: most k-blocks first (longest processing
+    // time first: the tiles handed out last, which decide how evenly the
+    // clusters finish, are the short ones), or as given
+    gp.order.resize(size_t(count));
+    for (int64_t g = 0; g < count; ++g) gp.order[size_t(g)] = g;
+    if (h->opts.group_order != 2)
+        std::stable_sort(gp.order.begin(), gp.order.end(), [&](int64_t a, int64_t b) {
+            return (q[a].K + kelems - 1) / kelems > (q[b].K + kelems - 1) / kelems;
+        });
     gp.start.assign(size_t(count) + 1, 0);
     int64_t tiles = 0;
-    for (int64_t g = 0; g < count; ++g) {
-        if (q[g].M > 0 && q[g].N > 0)
-            tiles += ((q[g].M + tile_m - 1) / tile_m) * ((q[g].N + pts::kTileN - 1) / pts::kTileN);
+    for (int64_t j = 0; j < count; ++j) {
+        const gemm_group_problem_t &x = q[gp.order[size_t(j)]];
+        if (x.M > 0 && x.N > 0)
+            tiles += ((x.M + tile_m - 1) / tile_m) * ((x.N + pts::kTileN - 1) / pts::kTileN);
         if (tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
-        gp.start[size_t(g) + 1] = static_cast<int32_t>(tiles);
+        gp.start[size_t(j) + 1] = static_cast<int32_t>(tiles);
     }
     pl.tiles_m = pl.tiles_n = 0;
     pl.tiles = tiles;
@@ -411,10 +423,11 @@ gemm_status_t plan_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t c
     gp.desc.resize(size_t(count));
     const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
-    for (int64_t g = 0; g < count; ++g) {
-        pts::GroupDesc &d = gp.desc[size_t(g)];
+    for (int64_t j = 0; j < count; ++j) {
+        pts::GroupDesc &d = gp.desc[size_t(j)];
         std::memset(&d, 0, sizeof(d));   // padding too: tables are compared byte for byte
-        const gemm_group_problem_t &x = q[g];
+        const gemm_group_problem_t &x = q[gp.order[size_t(j)]];
+        d.index = static_cast<int32_t>(gp.order[size_t(j)]);
         if (x.M == 0 || x.N == 0) continue;
         d.M = static_cast<int32_t>(x.M);
         d.N = static_cast<int32_t>(x.N);
@@ -578,6 +591,7 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
         return GEMM_ERR_INVALID_ARG;
     if (o.prefetch < -1 || o.prefetch > 64 || o.overlap_launch < -1 || o.overlap_launch > 0 || o.epilogue < 0 || o.epilogue > 2)
         return GEMM_ERR_INVALID_ARG;
+    if (o.group_order < 0 || o.group_order > 2) return GEMM_ERR_INVALID_ARG;
     if (o.split < 0 || o.split > 4 || o.split == 3 || o.split_k < -1 || o.split_k > 1
         || (o.split > 1 && o.split_k == 1))
         return GEMM_ERR_INVALID_ARG;

@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicAdd(&rec->visits, 1u);
                 if (leader) {
                     rec->tile = static_cast<uint32_t>(t.idx);
-                    rec->group = static_cast<uint32_t>(g);
+                    rec->group = grouped ? static_cast<uint32_t>(__ldg(&p.groups[g].index)) : 0u;
                     rec->n_off = static_cast<uint32_t>(t.n_off);
                     rec->n_len = static_cast<uint32_t>(t.n_len);
                     rec->kb_begin = static_cast<uint32_t>(t.kb_begin);

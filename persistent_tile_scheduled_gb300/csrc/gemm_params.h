@@ -50,6 +50,7 @@ struct GroupDesc {
     CUtensorMap tmA, tmB, tmC;
     int32_t M, N, num_kb, tiles_m, tiles_n;
     float out_scale;
+    int32_t index;   // the problem's position in the caller's list
 };
 static_assert(sizeof(GroupDesc) == 512, "problem table entry");
 

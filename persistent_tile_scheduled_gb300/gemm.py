@@ -32,7 +32,8 @@ class gemm_opts_t(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int), ("group_size_m", ctypes.c_int), ("stages", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("debug_flags", ctypes.c_uint), ("fault_arg", ctypes.c_int),
                 ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int), ("split_k", ctypes.c_int),
-                ("prefetch", ctypes.c_int), ("overlap_launch", ctypes.c_int), ("epilogue", ctypes.c_int)]
+                ("prefetch", ctypes.c_int), ("overlap_launch", ctypes.c_int), ("epilogue", ctypes.c_int),
+                ("group_order", ctypes.c_int)]
 
 
 class gemm_tile_record_t(ctypes.Structure):
@@ -144,9 +145,10 @@ def gemm_status_string(status: int) -> str:
 
 
 def make_opts(cta_group=0, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
-              timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0, epilogue=0) -> gemm_opts_t:
+              timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0, epilogue=0,
+              group_order=0) -> gemm_opts_t:
     return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split,
-                       split_k, prefetch, overlap_launch, epilogue)
+                       split_k, prefetch, overlap_launch, epilogue, group_order)
 
 
 def gemm_create(device: int = 0, opts: Optional[gemm_opts_t] = None) -> int:
@@ -178,26 +180,39 @@ def gemm_run_host_batch(h, problems, sched, stream=None) -> int:
                   "gemm_run_host_batch")
 
 
-def _group_array(problems):
-    arr = (gemm_group_problem_t * max(len(problems), 1))()
-    for i, q in enumerate(problems):
-        M, N, K, A, B, C = q[:6]
-        sa, sb = (q[6], q[7]) if len(q) > 6 else (1.0, 1.0)
-        arr[i] = gemm_group_problem_t(M, N, K, _ptr(A), _ptr(B), _ptr(C), float(sa), float(sb))
-    return arr
+class GroupArray:
+    """A problem list marshalled once into the C array gemm_run_grouped reads
+    (building it costs host time per problem; a loop over the same list can
+    reuse it)."""
+
+    def __init__(self, problems):
+        self.count = len(problems)
+        self.arr = (gemm_group_problem_t * max(self.count, 1))()
+        for i, q in enumerate(problems):
+            M, N, K, A, B, C = q[:6]
+            sa, sb = (q[6], q[7]) if len(q) > 6 else (1.0, 1.0)
+            self.arr[i] = gemm_group_problem_t(M, N, K, _ptr(A), _ptr(B), _ptr(C), float(sa), float(sb))
+
+
+def group_array(problems) -> GroupArray:
+    """problems: sequence of (M, N, K, A, B, C[, scale_a, scale_b]) with
+    device tensors or raw device addresses."""
+    return problems if isinstance(problems, GroupArray) else GroupArray(problems)
 
 
 def gemm_run_grouped(h, problems, dtype, sched, stream=None) -> int:
-    """problems: sequence of (M, N, K, A, B, C[, scale_a, scale_b]) with
-    device tensors or raw device addresses; one launch for all of them."""
-    return _check(load().gemm_run_grouped(h, _group_array(problems), len(problems), int(dtype), int(sched),
-                                          _stream(stream)), "gemm_run_grouped")
+    """problems: a GroupArray or a sequence as group_array() takes; one launch
+    for all of them."""
+    g = group_array(problems)
+    return _check(load().gemm_run_grouped(h, g.arr, g.count, int(dtype), int(sched), _stream(stream)),
+                  "gemm_run_grouped")
 
 
 def gemm_query_grouped(h, problems, dtype, sched) -> gemm_launch_info_t:
+    g = group_array(problems)
     info = gemm_launch_info_t()
-    _check(load().gemm_query_grouped(h, _group_array(problems), len(problems), int(dtype), int(sched),
-                                     ctypes.byref(info)), "gemm_query_grouped")
+    _check(load().gemm_query_grouped(h, g.arr, g.count, int(dtype), int(sched), ctypes.byref(info)),
+           "gemm_query_grouped")
     return info
 
 

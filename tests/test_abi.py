@@ -48,6 +48,8 @@ def test_calls_without_a_handle_are_rejected():
     assert lib.gemm_destroy(None) == g.GEMM_OK
     info = g.gemm_launch_info_t()
     assert lib.gemm_query(None, 8, 8, 8, 0, 0, ctypes.byref(info)) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_grouped(None, None, 0, 0, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_query_grouped(None, None, 0, 0, 0, ctypes.byref(info)) == g.GEMM_ERR_INVALID_ARG
 
 
 def test_bad_options_are_rejected_before_touching_a_device():
@@ -57,7 +59,7 @@ def test_bad_options_are_rejected_before_touching_a_device():
                 g.make_opts(group_size_m=-1), g.make_opts(debug_flags=0x80), g.make_opts(prefetch=-2),
                 g.make_opts(prefetch=65), g.make_opts(split=3), g.make_opts(split_k=2), g.make_opts(split_k=-2),
                 g.make_opts(split=2, split_k=1), g.make_opts(overlap_launch=1), g.make_opts(epilogue=3),
-                g.make_opts(max_clusters=-1)):
+                g.make_opts(max_clusters=-1), g.make_opts(group_order=3), g.make_opts(group_order=-1)):
         assert lib.gemm_create(ctypes.byref(h), 0, ctypes.byref(bad)) == g.GEMM_ERR_INVALID_ARG
         assert h.value is None
 

@@ -45,14 +45,15 @@ def _problems(xs, dev):
             for x, (A, B, C) in zip(xs, dev)]
 
 
-def _check_grouped_records(h, xs, info, sched, group_m=8):
+def _check_grouped_records(h, xs, info, sched, group_m=8, longest_first=True):
     cg = int(info.cta_group)
     W = int(info.work_items)
+    kelems = int(info.tile_k)
     st, recs, dev = pts.gemm_read_debug(h, W)
     assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
-    items = osched.grouped_items([(x.problem.M, x.problem.N) for x in xs], 128 * cg, 256, group_m)
+    kb = [-(-x.problem.K // kelems) for x in xs] if longest_first else None
+    items = osched.grouped_items([(x.problem.M, x.problem.N) for x in xs], 128 * cg, 256, group_m, kb)
     assert len(items) == W == int(info.tiles) == int(info.units)
-    kelems = int(info.tile_k)
     for w, (g, tm, tn) in enumerate(items):
         r = recs[w]
         p = xs[g].problem
@@ -117,6 +118,28 @@ def test_grouped_small_problems(handles, dtype, sched):
         assert torch.equal(C.view(torch.int16), C1.view(torch.int16)), p.name
 
 
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_grouped_given_order(sched):
+    """group_order 2: the problems' tiles in the caller's order."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    xs = _inputs([(256, 512, 64), (300, 264, 1024), (128, 256, 0), (512, 256, 512)], wl.BF16, 80)
+    dev = _device(xs)
+    probs = _problems(xs, dev)
+    h = pts.gemm_create(0, pts.make_opts(cta_group=2, group_order=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        pts.gemm_run_grouped(h, probs, wl.BF16, sched)
+        info = pts.gemm_query_grouped(h, probs, wl.BF16, sched)
+        _check_grouped_records(h, xs, info, sched, longest_first=False)
+        for x, (_, _, C) in zip(xs, dev):
+            if x.problem.K:
+                assert compare_full(x, C) <= TOL[wl.BF16]
+            else:
+                assert torch.count_nonzero(C).item() == 0
+    finally:
+        pts.gemm_destroy(h)
+
+
 def test_grouped_table_reuse_and_change(handles):
     """Lists X, Y, X, X (the last after new values in X's inputs) on one
     stream: an unchanged list reuses its table, a changed one gets the other
@@ -162,9 +185,9 @@ def test_grouped_invalid_arguments(handles):
     good = (128, 256, 64, A, B, C)
 
     def status(probs, dtype=wl.BF16, sched=pts.GEMM_SCHED_STATIC, count=None):
-        arr = pts.gemm._group_array(probs)
-        n = len(probs) if count is None else count
-        return lib.gemm_run_grouped(h, arr, n, dtype, sched, None)
+        g = pts.gemm.group_array(probs)
+        n = g.count if count is None else count
+        return lib.gemm_run_grouped(h, g.arr, n, dtype, sched, None)
 
     bad = pts.gemm.GEMM_ERR_INVALID_ARG
     assert status([good]) == 0
@@ -187,7 +210,7 @@ def test_grouped_invalid_arguments(handles):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         g.capture_begin()
-        st = lib.gemm_run_grouped(h, pts.gemm._group_array([good]), 1, wl.BF16, 1, ctypes.c_void_p(s.cuda_stream))
+        st = lib.gemm_run_grouped(h, pts.gemm.group_array([good]).arr, 1, wl.BF16, 1, ctypes.c_void_p(s.cuda_stream))
         g.capture_end()
     assert st == bad
     torch.cuda.synchronize()

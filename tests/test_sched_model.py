@@ -194,6 +194,13 @@ def test_grouped_items_hand_worked():
                    (0, 2, 0), (0, 2, 1), (0, 2, 2), (2, 0, 0)]
 
 
+def test_grouped_items_longest_first_hand_worked():
+    """Three one-tile problems with 2, 5 and 5 k-blocks and one with 3: the
+    5s first in their given order, then the 3, then the 2."""
+    got = sm.grouped_items([(1, 8), (1, 8), (1, 8), (1, 8)], 128, 256, 8, kb=[2, 5, 5, 3])
+    assert got == [(1, 0, 0), (2, 0, 0), (3, 0, 0), (0, 0, 0)]
+
+
 @pytest.mark.parametrize("seed", range(5))
 def test_grouped_items_cover_every_problem_tile_once(seed):
     rng = random.Random(seed)
