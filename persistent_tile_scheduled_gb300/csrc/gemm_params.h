@@ -109,8 +109,10 @@ constexpr int kSkMaxParts = 2;       // pieces per tile
 // Use it when it saves each cluster at least this many k-blocks' time.  The
 // price, measured on GB300 (fp16 4096^2, CTA pairs): a writer's epilogue
 // takes ~4 us longer than a plain one and a reader's ~4.5 us; hidden behind a
-// long next tile, but not behind a short one.  Break-even was near 14
-// k-blocks saved (K = 2048: 20 saved, 2 us gained; K = 4096: 40 saved, 7 us).
+// long next tile, but not behind a short one.  Break-even is between 15 and
+// 18 k-blocks saved (cold inputs, with vs without: 24 k-blocks per tile, 15
+// saved: 41.6-41.9 vs 41.1 us; 28 per tile, 18 saved: 45.4-45.6 vs
+// 45.8-46.0; 40 per tile, 25 saved: 57.4 vs 59.8-60.5).
 constexpr int kSkMinSavedKb = 16;
 
 __host__ __device__ inline int64_t sk_unit_begin(int64_t c, int64_t L, int64_t U) { return c * L / U; }
@@ -140,12 +142,13 @@ inline int64_t choose_stream_k(int64_t tiles, int64_t resident, int64_t num_kb, 
 
 // CTA group when the caller leaves it to the library.  CTA pairs (cta_group
 // 2) load a third less per SM for the same MMA work, so their mainloop runs
-// faster under full load, but a pair costs 3-5 us more per launch to start,
-// fill and finish.  Measured on GB300 on fp16 4096^2 with cold inputs (eight
-// buffer sets in turn), single vs pair per launch: K = 1024 32.1 vs 34.7 us,
-// K = 2048 52.3 vs 53.2, K = 2560 61.7 vs 61.8, K = 3072 70.8 vs 69.9.  So
-// pairs from 40 k-blocks per tile.
-constexpr int kPairMinKb = 40;
+// faster under full load, but a pair costs more per launch to start, fill
+// and finish.  Measured on GB300 on fp16 4096^2 with cold inputs (eight
+// buffer sets in turn), single vs pair per launch, without the stream-K
+// share: K = 768 27.0 vs 27.5-27.8 us, K = 1024 31.9-32.1 vs 31.9-32.3,
+// K = 1280 37.0-37.2 vs 36.4-36.5, K = 1536 42.1 vs 41.1.  So pairs from 18
+// k-blocks per tile.
+constexpr int kPairMinKb = 18;
 
 inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
 

@@ -225,15 +225,15 @@ def test_automatic_stream_k_share():
 
 
 def test_automatic_cta_group():
-    """CTA pairs from 40 k-blocks per tile, single CTAs below."""
+    """CTA pairs from 18 k-blocks per tile, single CTAs below."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=0))
     try:
         assert pts.gemm_query(h, 4096, 4096, 512, pts.GEMM_F16, 1).cta_group == 1      # 8 k-blocks
-        assert pts.gemm_query(h, 4096, 4096, 2496, pts.GEMM_F16, 1).cta_group == 1     # 39
-        assert pts.gemm_query(h, 4096, 4096, 2560, pts.GEMM_F16, 1).cta_group == 2     # 40
+        assert pts.gemm_query(h, 4096, 4096, 1088, pts.GEMM_F16, 1).cta_group == 1     # 17
+        assert pts.gemm_query(h, 4096, 4096, 1096, pts.GEMM_F16, 1).cta_group == 2     # 18 (a partial one)
         assert pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_BF16, 1).cta_group == 2    # 128
-        assert pts.gemm_query(h, 8192, 8192, 4096, pts.GEMM_E4M3, 1).cta_group == 1    # 32 (128-wide k-blocks)
-        assert pts.gemm_query(h, 8192, 8192, 8192, pts.GEMM_E4M3, 1).cta_group == 2    # 64
+        assert pts.gemm_query(h, 8192, 8192, 2176, pts.GEMM_E4M3, 1).cta_group == 1    # 17 (128-wide k-blocks)
+        assert pts.gemm_query(h, 8192, 8192, 2304, pts.GEMM_E4M3, 1).cta_group == 2    # 18
         x = wl.custom(640, 1000, 8192, wl.BF16, "normal_sqrtk", 12)
         C = run_device(h, x, pts.GEMM_SCHED_CLC)
         assert pts.gemm_check(h)[0] == 0
@@ -331,7 +331,7 @@ def test_bench_configuration_sampled(K):
     try:
         x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
         info = pts.gemm_query(h, 4096, 4096, K, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.cta_group == (2 if K // 64 >= 40 else 1)
+        assert info.cta_group == (2 if K // 64 >= 18 else 1)
         for sched in SCHEDS:
             _run_checked(h, x, sched, full=False)
     finally:
