@@ -503,6 +503,7 @@ def extra_configs(pts, dev, stream):
         out["concurrent_" + pa.name + "+" + pb.name] = conc
         out["half_occupied"] = half_occupied(pts, dev, stream)
         out["bf16_grouped_vark"] = grouped_vark(pts, dev, stream)
+        out["fp16_4096_ksweep_one_grouped_launch"] = sweep_as_grouped(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
     out["note"] = ("library's CTA group per GEMM (pairs from 18 k-blocks per tile); median of back-to-back "
@@ -601,6 +602,40 @@ def grouped_vark(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES
         pts.gemm_destroy(h)
     out["note"] = (f"median of {reps} back-to-back grouped launches; TFLOP/s over all {len(probs)} problems; "
                    "problems listed most k-blocks first (the default) or in the given order")
+    return out
+
+
+def sweep_as_grouped(pts, dev, stream, reps=10):
+    """The 32 GEMMs of the fp16 K sweep (M = N = 4096, K = 128..4096) as ONE
+    grouped launch per scheduler, library defaults: no launch boundary, so no
+    per-GEMM start-up, fill and tail (the headline times them as 32 launches,
+    as the pages' sweeps do)."""
+    probs = wl.fp16_4096_ksweep()
+    ins = [device_inputs(p, 9000 + i) for i, p in enumerate(probs)]
+    Cs = [torch.empty(p.M, p.N, dtype=torch.float16, device="cuda") for p in probs]
+    arr = pts.gemm.group_array([(p.M, p.N, p.K, A, B, C) for p, (A, B, _, _), C in zip(probs, ins, Cs)])
+    flops = sum(gemm_flops(p.M, p.N, p.K) for p in probs)
+    out = {}
+    h = pts.gemm_create(dev, None)
+    try:
+        out["cta_group"] = int(pts.gemm_query_grouped(h, arr, wl.F16, 1).cta_group)
+        for si, name in enumerate(SCHED_NAMES):
+            for _ in range(3):
+                pts.gemm_run_grouped(h, arr, wl.F16, si, stream)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+            with torch.cuda.stream(stream):
+                for r in range(reps):
+                    ev[r].record(stream)
+                    pts.gemm_run_grouped(h, arr, wl.F16, si, stream)
+                ev[reps].record(stream)
+            torch.cuda.synchronize()
+            if pts.gemm_check(h, stream)[0] != 0:
+                raise RuntimeError("device error in the grouped sweep")
+            ms = statistics.median(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+            out[name] = round(flops / (ms * 1e-3) / 1e12, 1)
+    finally:
+        pts.gemm_destroy(h)
+    out["note"] = f"median of {reps} launches; TFLOP/s over the 32 GEMMs; most k-blocks first"
     return out
 
 
