@@ -67,6 +67,16 @@ __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
     asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -142,9 +152,9 @@ __device__ __forceinline__ int group_of(int w, const GemmParams &p)
 //    whole tile sk_tiles + s - 3U.
 //  - With column slices (split 2 or 4): slice s % split of tile s / split.
 //  - Otherwise the whole tile s.
-//  - In a grouped launch: whole tile s - group_start[g] of problem g.
-// Tiles are numbered in grouped order (tile_of).
-__device__ __forceinline__ WorkTile work_tile(int s, int g, const GemmParams &p)
+// Tiles are numbered in grouped order (tile_of).  (A grouped launch's items
+// are decoded by the scheduler warp, which caches its problem table.)
+__device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
 {
     WorkTile t;
     int tile = s;
@@ -153,15 +163,7 @@ __device__ __forceinline__ WorkTile work_tile(int s, int g, const GemmParams &p)
     t.kb_begin = 0;
     t.kb_end = p.num_kb;
     t.ks = -1;
-    t.g = g;
-    if (p.num_groups > 0) {
-        const GroupDesc *d = p.groups + g;
-        const int tiles_n = __ldg(&d->tiles_n);
-        t.kb_end = __ldg(&d->num_kb);
-        tile_of(s - __ldg(p.group_start + g), __ldg(&d->tiles_m), tiles_n, p.group_m, t.tm, t.tn);
-        t.idx = t.tm * tiles_n + t.tn;
-        return t;
-    }
+    t.g = 0;
     if (p.sk_units > 0) {
         const int U = p.sk_units;
         if (s < kSkMaxPieces * U) {
@@ -344,9 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t clc_bar = ring_empty0 + 8 * kRing;
     const uint32_t started_bar = clc_bar + 8;                // producer (leader) starts an item
     const uint32_t clc_resp = (started_bar + 8 + 15) & ~15u;
-    const uint32_t ring_w0 = clc_resp + 16;                  // + 4*r: work id
-    const uint32_t ring_g0 = ring_w0 + 4 * kRing;            // + 4*r: its problem (grouped launch)
-    const uint32_t tmem_slot = ring_g0 + 4 * kRing;
+    const uint32_t ring0 = clc_resp + 16;                    // + 4*kRingWords*r: a decoded work item
+    const uint32_t tmem_slot = ring0 + 4 * kRingWords * kRing;
     const uint32_t abort_flag = tmem_slot + 4;
 
     const uint32_t warp = threadIdx.x >> 5;
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (Not in a grouped launch, whose problem table is read only after the wait.)
     pdl_launch_dependents();
     if (warp == 0 && cluster_id < p.num_units && !grouped) {
-        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), 0, p);
+        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), p);
         int ya, yb;
         const CUtensorMap *ma;
         const CUtensorMap *mb = boxes(t0, ya, yb, ma);
@@ -436,36 +437,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait();
 
-    // ---- work-id broadcast ring -------------------------------------------
-    // Slot r holds the id of work item i (i % kRing == r), or -1 = no more,
-    // and the item's problem g.  publish is called by the whole scheduler
-    // warp, ring_read by whole converged warps (producer, MMA) or by lane 0
-    // of an epilogue warp; the slot writes and the arrivals happen in lane 0.
-    auto publish = [&](int i, int w, int g) -> bool {
+    // ---- work-item broadcast ring -----------------------------------------
+    // Slot r holds work item i (i % kRing == r), decoded: its id w (the
+    // record slot; -1 = no more) and its WorkTile.  publish is called by the
+    // whole scheduler warp, ring_read by whole converged warps (producer, MMA)
+    // or by lane 0 of an epilogue warp; the slot writes and the arrivals
+    // happen in lane 0.
+    auto publish = [&](int i, int w, const WorkTile &t) -> bool {
         const int slot = i % kRing;
         if (i >= kRing && !ctl.wait_all(ring_empty0 + 8 * slot, ((i / kRing) & 1) ^ 1, WHERE_RING_EMPTY))
             return false;
         if (lane == 0) {
-            st_shared_u32(ring_w0 + 4 * slot, static_cast<uint32_t>(w));
-            st_shared_u32(ring_g0 + 4 * slot, static_cast<uint32_t>(g));
-            if constexpr (CG == 2) {
-                st_cluster_u32(mapa(ring_w0 + 4 * slot, 1u), static_cast<uint32_t>(w));
-                st_cluster_u32(mapa(ring_g0 + 4 * slot, 1u), static_cast<uint32_t>(g));
-                mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
+            const uint32_t a = ring0 + 4 * kRingWords * slot;
+            const uint32_t v[12] = {static_cast<uint32_t>(w),        static_cast<uint32_t>(t.g),
+                                    static_cast<uint32_t>(t.tm),     static_cast<uint32_t>(t.tn),
+                                    static_cast<uint32_t>(t.n_off),  static_cast<uint32_t>(t.n_len),
+                                    static_cast<uint32_t>(t.kb_begin), static_cast<uint32_t>(t.kb_end),
+                                    static_cast<uint32_t>(t.ks),     static_cast<uint32_t>(t.idx), 0u, 0u};
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                st_shared_v4(a + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                if constexpr (CG == 2)
+                    st_cluster_v4(mapa(a + 16 * q, 1u), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
+            if constexpr (CG == 2) mbar_arrive_cluster(mapa(ring_full0 + 8 * slot, 1u));
             mbar_arrive(ring_full0 + 8 * slot);
         }
         __syncwarp();
         return true;
     };
-    auto ring_read = [&](int i, int &w, int &g, bool whole_warp) -> bool {
+    auto ring_read = [&](int i, int &w, WorkTile &t, bool whole_warp) -> bool {
         const int slot = i % kRing;
         const uint32_t par = (i / kRing) & 1;
         if (!(whole_warp ? ctl.wait_all(ring_full0 + 8 * slot, par, WHERE_RING_FULL)
                          : ctl.wait(ring_full0 + 8 * slot, par, WHERE_RING_FULL)))
             return false;
-        w = static_cast<int>(ld_shared_u32(ring_w0 + 4 * slot));
-        g = static_cast<int>(ld_shared_u32(ring_g0 + 4 * slot));
+        const uint32_t a = ring0 + 4 * kRingWords * slot;
+        const uint4 v0 = ld_shared_v4(a), v1 = ld_shared_v4(a + 16), v2 = ld_shared_v4(a + 32);
+        w = static_cast<int>(v0.x);
+        t.g = static_cast<int>(v0.y);
+        t.tm = static_cast<int>(v0.z);
+        t.tn = static_cast<int>(v0.w);
+        t.n_off = static_cast<int>(v1.x);
+        t.n_len = static_cast<int>(v1.y);
+        t.kb_begin = static_cast<int>(v1.z);
+        t.kb_end = static_cast<int>(v1.w);
+        t.ks = static_cast<int>(v2.x);
+        t.idx = static_cast<int>(v2.y);
         if (CG == 2 && !leader)
             mbar_arrive_cluster_if(one, mapa(ring_empty0 + 8 * slot, 0u));
         else
@@ -537,14 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         for (int i = 0;; ++i) {
-            int w, g;
-            if (!ring_read(i, w, g, true)) {
+            int w;
+            WorkTile t;
+            if (!ring_read(i, w, t, true)) {
                 ok = false;
                 break;
             }
             if (w < 0) break;
             if (leader) mbar_arrive_if(one, started_bar);
-            const WorkTile t = work_tile(w, g, p);
             if (!load_tile(t, t.kb_begin, t.kb_end)) {
                 ok = false;
                 break;
@@ -579,13 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_stage = -1;
             uint32_t last_phase = 0;
             for (int i = 0;; ++i) {
-                int w, g;
-                if (!ring_read(i, w, g, true) || w < 0) break;
+                int w;
+                WorkTile t;
+                if (!ring_read(i, w, t, true) || w < 0) break;
                 if (!ctl.wait_all(acc_empty0 + 8 * acc, acc_phase ^ 1u, WHERE_ACC_EMPTY)) break;
                 tc_fence_after();
                 if (p.records != nullptr && lane == 0)
                     p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
-                const WorkTile t = work_tile(w, g, p);
                 const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
                 bool ok = true;
@@ -636,14 +654,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t nstore = 0;
         int maps_of = -1;   // the problem whose C map this warp's lane 0 has acquired (grouped launch)
         for (int i = 0;; ++i) {
-            int w = 0, g = 0;
+            int w = 0;
+            WorkTile t{};
             int ok = 1;
-            if (lane == 0) ok = ring_read(i, w, g, false) ? 1 : 0;
+            if (lane == 0) ok = ring_read(i, w, t, false) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             w = __shfl_sync(0xffffffffu, w, 0);
-            g = __shfl_sync(0xffffffffu, g, 0);
             if (!ok || w < 0) break;
-            const WorkTile t = work_tile(w, g, p);
+            t.g = __shfl_sync(0xffffffffu, t.g, 0);
+            t.tm = __shfl_sync(0xffffffffu, t.tm, 0);
+            t.tn = __shfl_sync(0xffffffffu, t.tn, 0);
+            t.n_off = __shfl_sync(0xffffffffu, t.n_off, 0);
+            t.n_len = __shfl_sync(0xffffffffu, t.n_len, 0);
+            t.kb_begin = __shfl_sync(0xffffffffu, t.kb_begin, 0);
+            t.kb_end = __shfl_sync(0xffffffffu, t.kb_end, 0);
+            t.ks = __shfl_sync(0xffffffffu, t.ks, 0);
+            t.idx = __shfl_sync(0xffffffffu, t.idx, 0);
+            const int g = t.g;
             // the item's output: its problem's C map, sizes and scale
             const CUtensorMap *mc = &tmC;
             int cM = p.M, cN = p.N;
@@ -915,14 +942,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             };
+            // Grouped launch: the problem of the last tile decoded, its tiles
+            // [gc_lo, gc_hi) and sizes, so that a tile of the same problem (or
+            // of the next one) costs no search and no table read.
+            int gc = -1, gc_lo = 0, gc_hi = 0, gc_tm = 0, gc_tn = 0, gc_kb = 0;
+            auto item_of = [&](int w) -> WorkTile {
+                if (!grouped) return work_tile(w, p);
+                if (w < gc_lo || w >= gc_hi) {
+                    int g;
+                    if (gc >= 0 && w >= gc_hi && gc + 1 < p.num_groups && w < __ldg(p.group_start + gc + 2))
+                        g = gc + 1;
+                    else
+                        g = group_of(w, p);
+                    const GroupDesc *d = p.groups + g;
+                    gc = g;
+                    gc_lo = __ldg(p.group_start + g);
+                    gc_hi = __ldg(p.group_start + g + 1);
+                    gc_tm = __ldg(&d->tiles_m);
+                    gc_tn = __ldg(&d->tiles_n);
+                    gc_kb = __ldg(&d->num_kb);
+                }
+                WorkTile t;
+                t.g = gc;
+                t.n_off = 0;
+                t.n_len = kTileN;
+                t.kb_begin = 0;
+                t.kb_end = gc_kb;
+                t.ks = -1;
+                tile_of(w - gc_lo, gc_tm, gc_tn, p.group_m, t.tm, t.tn);
+                t.idx = t.tm * gc_tn + t.tn;
+                return t;
+            };
+            // Only CLC waits for the producer before going on: its next claim
+            // must not come earlier than one item ahead.  Static units are
+            // fixed, so that scheduler runs as far ahead as the ring allows.
+            const bool pace = p.sched == SCHED_CLC;
             int u = cluster_id < p.num_units ? cluster_id : -1;
-            int g = grouped && u >= 0 ? group_of(u, p) : 0;   // (a grouped launch's units are tiles)
             int i = 0;   // ring slot sequence = work items published
             for (int n = 0; ok && u >= 0; ++n) {
                 const int pieces = unit_items(u, p);
                 for (int j = 0; ok && j < pieces; ++j) {
-                    ok = publish(i, unit_item(u, j, pieces, p), g)
-                         && ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED);
+                    const int w = unit_item(u, j, pieces, p);
+                    ok = publish(i, w, item_of(w))
+                         && (!pace || ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED));
                     ++i;
                     if (ok && j == 0 && may_request) {
                         // the producer has begun this unit: claim the one after it
@@ -944,13 +1006,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (grouped && next >= 0) {
-                    g = group_of(next, p);
-                    warm(work_tile(unit_item(next, 0, 1, p), g, p));
-                }
+                if (grouped && next >= 0) warm(item_of(next));   // (a grouped launch's units are tiles)
                 u = next;
             }
-            if (ok) publish(i, -1, 0);
+            if (ok) publish(i, -1, WorkTile{});
             if (clc_pending) ctl.drain(clc_bar, clc_phase, 10000000ull);
         }
         __syncwarp();

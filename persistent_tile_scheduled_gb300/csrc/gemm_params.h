@@ -20,7 +20,8 @@ constexpr int kEpiChunkCols = 64;       // columns per epilogue TMA store (128 b
 constexpr int kEpiRowsPerWarp = 32;
 constexpr int kEpiBufBytes = kEpiRowsPerWarp * kEpiChunkCols * 2;   // 4 KB
 constexpr int kEpiBufsPerWarp = 2;
-constexpr int kRing = 4;                // depth of the tile-id broadcast ring
+constexpr int kRing = 4;                // depth of the work-item broadcast ring
+constexpr int kRingWords = 12;          // 32-bit words per ring slot (a decoded work item)
 constexpr int kTmemCols = 512;          // two 256-column accumulators
 constexpr int kMaxStages = 8;
 constexpr int kDefaultPrefetchKb = 0;   // L2 prefetch of the operand loads: off (it costs more L2
@@ -185,7 +186,7 @@ __host__ __device__ constexpr int smem_bytes(int cg, int stages)
     return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg)) + epi_bytes()
            + 8 * (2 * kMaxStages + 4 + 2 * kRing + 2)    // mbarriers
            + 16                                          // CLC response
-           + 8 * kRing + 16;                             // ring payload, TMEM base, abort flag
+           + 4 * kRingWords * kRing + 16;                // ring payload, TMEM base, abort flag
 }
 
 }  // namespace pts
