@@ -15,8 +15,8 @@
 //              the stream-K share, the fp32 partial fixup
 //   warp 6     scheduler (the leader CTA's): static arithmetic or Cluster
 //              Launch Control; it takes units, splits each into its work
-//              items and publishes their ids into a small broadcast ring read
-//              by every other role, one item ahead of the producer
+//              items, decodes them and publishes them into a small broadcast
+//              ring read by every other role
 // The producer, MMA and scheduler warps run their loops with all 32 lanes in
 // step and issue through predicated instructions from lane 0.
 //
@@ -871,12 +871,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The leader CTA's whole warp runs this loop in step; lane 0 makes
         // the CLC requests.  It takes units (static arithmetic, CLC, or the
         // cluster's own for the non-persistent grid), splits each into its
-        // work items and publishes them into the broadcast ring one at a
-        // time: item i + 1 only once the producer has started item i.  The
-        // next unit is claimed when the producer starts a unit's first item
-        // (as late as the producer's lead allows, so that CLC still balances
-        // the last tiles), and decoded while the producer loads: the
-        // producer never waits on the scheduling arithmetic.
+        // work items, decodes them and publishes them into the broadcast
+        // ring, so no other warp does scheduling or decoding work.  With CLC
+        // it publishes item i + 1 only once the producer has started item i,
+        // and claims the next unit when the producer starts a unit's first
+        // item (as late as the producer's lead allows, so that CLC still
+        // balances the last tiles); the unit is decoded while the producer
+        // loads.  The static scheduler's units are fixed, so it runs as far
+        // ahead as the ring allows.
         if (leader) {
             bool ok = true;
             bool clc_pending = false;
