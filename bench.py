@@ -40,7 +40,7 @@ WORKLOAD = ("fp16 GEMM M=N=4096, K=128..4096 step 128 (32 GEMMs per step), A,B ~
             "fp32 accumulate, fp16 C, row-major A, column-major B")
 SCHED_NAMES = ["nonpersistent", "static", "clc"]
 TILE_DESC = {0: "128x256x64 per CTA; the library's CTA group per GEMM: single CTAs (tcgen05 cta_group::1) "
-                "below 18 k-blocks per tile (K < 1089), CTA pairs (one 256x256 cta_group::2 MMA sharing B) "
+                "below 14 k-blocks per tile (K <= 832), CTA pairs (one 256x256 cta_group::2 MMA sharing B) "
                 "from there",
              1: "128x256x64 per CTA (tcgen05 cta_group::1)",
              2: "128x256x64 per CTA; CTA pairs run one 256x256 tcgen05 cta_group::2 MMA and share B"}
@@ -506,7 +506,7 @@ def extra_configs(pts, dev, stream):
         out["fp16_4096_ksweep_one_grouped_launch"] = sweep_as_grouped(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
-    out["note"] = ("library's CTA group per GEMM (pairs from 18 k-blocks per tile); median of back-to-back "
+    out["note"] = ("library's CTA group per GEMM (pairs from 14 k-blocks per tile); median of back-to-back "
                    "launches; inputs generated on the GPU from seeded generators (parity for these shapes is in "
                    "the tests)")
     return out
@@ -725,7 +725,7 @@ def main():
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
-                    help="0 = the library's choice per GEMM (single CTAs below 18 k-blocks per tile)")
+                    help="0 = the library's choice per GEMM (single CTAs below 14 k-blocks per tile)")
     ap.add_argument("--split-k", type=int, default=0, choices=[0, 1, -1],
                     help="stream-K share of the last waves: 0 = the library's choice, 1 = always, -1 = never")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],

@@ -77,7 +77,7 @@ typedef enum {
 
 typedef struct gemm_opts {
     int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair);
-                                       0 = per call: pairs when a tile has >= 18 k-blocks */
+                                       0 = per call: pairs when a tile has >= 14 k-blocks */
     int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
     int stages;                     /* shared-memory ring depth in stages (a stage holds one
                                        k-block for single CTAs, two for CTA pairs); 0 = the
@@ -253,7 +253,7 @@ typedef struct gemm_group_problem {
  * default; longest-processing-time-first list scheduling, so the last tiles
  * handed out are the short ones) or in the given order (group_order 2).
  * No stream-K share and no column slices.  CTA group (cta_group 0): pairs
- * when the mean k-blocks per tile, weighted by output size, is at least 18.
+ * when the mean k-blocks per tile, weighted by output size, is at least 14.
  * The handle keeps the problem table (tensor maps and tile counts, 512 bytes
  * per problem) in device memory it owns, in two slots: a call with the same
  * problems as the previous one reuses its table; a different list is copied

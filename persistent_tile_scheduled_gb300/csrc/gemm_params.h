@@ -146,10 +146,10 @@ inline int64_t choose_stream_k(int64_t tiles, int64_t resident, int64_t num_kb, 
 // faster under full load, but a pair costs more per launch to start, fill
 // and finish.  Measured on GB300 on fp16 4096^2 with cold inputs (eight
 // buffer sets in turn), single vs pair per launch, without the stream-K
-// share: K = 768 27.0 vs 27.5-27.8 us, K = 1024 31.9-32.1 vs 31.9-32.3,
-// K = 1280 37.0-37.2 vs 36.4-36.5, K = 1536 42.1 vs 41.1.  So pairs from 18
-// k-blocks per tile.
-constexpr int kPairMinKb = 18;
+// share: K = 640 22.9-23.1 vs 24.3-24.5 us, K = 768 25.5 vs 25.7, K = 896
+// 27.8-28.3 vs 27.4-27.5, K = 1152 33.1-33.2 vs 32.7-32.8.  So pairs from
+// 14 k-blocks per tile.
+constexpr int kPairMinKb = 14;
 
 inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
 

@@ -225,15 +225,15 @@ def test_automatic_stream_k_share():
 
 
 def test_automatic_cta_group():
-    """CTA pairs from 18 k-blocks per tile, single CTAs below."""
+    """CTA pairs from 14 k-blocks per tile, single CTAs below."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=0))
     try:
         assert pts.gemm_query(h, 4096, 4096, 512, pts.GEMM_F16, 1).cta_group == 1      # 8 k-blocks
-        assert pts.gemm_query(h, 4096, 4096, 1088, pts.GEMM_F16, 1).cta_group == 1     # 17
-        assert pts.gemm_query(h, 4096, 4096, 1096, pts.GEMM_F16, 1).cta_group == 2     # 18 (a partial one)
+        assert pts.gemm_query(h, 4096, 4096, 832, pts.GEMM_F16, 1).cta_group == 1      # 13
+        assert pts.gemm_query(h, 4096, 4096, 840, pts.GEMM_F16, 1).cta_group == 2      # 14 (a partial one)
         assert pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_BF16, 1).cta_group == 2    # 128
-        assert pts.gemm_query(h, 8192, 8192, 2176, pts.GEMM_E4M3, 1).cta_group == 1    # 17 (128-wide k-blocks)
-        assert pts.gemm_query(h, 8192, 8192, 2304, pts.GEMM_E4M3, 1).cta_group == 2    # 18
+        assert pts.gemm_query(h, 8192, 8192, 1664, pts.GEMM_E4M3, 1).cta_group == 1    # 13 (128-wide k-blocks)
+        assert pts.gemm_query(h, 8192, 8192, 1792, pts.GEMM_E4M3, 1).cta_group == 2    # 14
         x = wl.custom(640, 1000, 8192, wl.BF16, "normal_sqrtk", 12)
         C = run_device(h, x, pts.GEMM_SCHED_CLC)
         assert pts.gemm_check(h)[0] == 0
@@ -331,7 +331,7 @@ def test_bench_configuration_sampled(K):
     try:
         x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
         info = pts.gemm_query(h, 4096, 4096, K, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
-        assert info.cta_group == (2 if K // 64 >= 18 else 1)
+        assert info.cta_group == (2 if K // 64 >= 14 else 1)
         for sched in SCHEDS:
             _run_checked(h, x, sched, full=False)
     finally:
