@@ -10,8 +10,8 @@
  * The output is cut into tiles (one tile per CTA, or per CTA pair with
  * cta_group 2); a scheduler hands the tiles to CTAs:
  *   - non-persistent: one CTA (pair) per tile, the hardware block scheduler
- *     assigns them ("question about persistent kernel concept": "allocating
- *     a thread block for each tile");
+ *     assigns them (the question of "question about persistent kernel
+ *     concept": one thread block per tile);
  *   - static: a grid sized to the resident capacity of the SMs, each CTA
  *     derives its later tiles in software ("Persistent Kernels with Cluster
  *     Launch Control", first paragraph; "Choosing between static and CLC

@@ -2,8 +2,8 @@
 
 The model states what each scheduler must do; these tests check it against
 hand-worked orders, closed forms of the grouped order at its extremes, and the
-coverage invariant ("Neither mode creates additional independent work at the
-tail of a grid": every tile is done exactly once).
+coverage invariant: neither scheduler adds or drops work ("Choosing between
+static and CLC scheduling"), so every tile is done exactly once.
 """
 import json
 import os
