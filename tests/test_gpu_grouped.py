@@ -14,6 +14,7 @@ import torch
 
 import persistent_tile_scheduled_gb300 as pts
 import workloads as wl
+from oracle import gemm as og
 from oracle import sched as osched
 
 from helpers import TOL, compare_full, compare_sampled
@@ -236,5 +237,42 @@ def test_grouped_workload_sampled(sched):
         for i in pick:
             err = compare_sampled(xs[i], dev[i][2], int(info.tile_m), 256, seed=i)
             assert err <= TOL[wl.BF16], f"{xs[i].problem.name}: rel err {err}"
+    finally:
+        pts.gemm_destroy(h)
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_grouped_three_thousand_small_problems(sched):
+    """3000 small ragged problems (some empty, some with K = 0) in one launch:
+    the problem search takes several rounds and the scheduler's cached
+    problem changes at nearly every tile.  Every C against the oracle, the
+    records exactly."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    rng = np.random.default_rng(5)
+    shapes = []
+    for _ in range(3000):
+        M = int(rng.choice([0, 1, 37, 128, 129, 300]))
+        N = int(rng.choice([8, 64, 256, 264]))
+        K = int(rng.choice([0, 8, 64, 200]))
+        shapes.append((M, N, K))
+    xs = _inputs(shapes, wl.BF16, 20000)
+    dev = _device(xs)
+    probs = pts.gemm.group_array(_problems(xs, dev))
+    h = pts.gemm_create(0, pts.make_opts(cta_group=1, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        pts.gemm_run_grouped(h, probs, wl.BF16, sched)
+        info = pts.gemm_query_grouped(h, probs, wl.BF16, sched)
+        _check_grouped_records(h, xs, info, sched)
+        for x, (A, B, C) in zip(xs, dev):
+            p = x.problem
+            if p.M == 0:
+                continue
+            if p.K == 0:
+                assert torch.count_nonzero(C).item() == 0
+                continue
+            ref, ref_abs = og.gemm(p.M, p.N, p.K, x.bits("A"), x.bits("B"), p.dtype, nthreads=1)
+            err = og.rel_err(C.double().cpu().numpy(), ref, ref_abs, og.OUT_UNIT_ROUNDOFF[og.BF16])
+            assert err <= TOL[wl.BF16], f"{p.name}: rel err {err}"
     finally:
         pts.gemm_destroy(h)
