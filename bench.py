@@ -415,12 +415,16 @@ def device_inputs(p, seed):
         a = torch.randn(p.M, p.K, device="cuda", generator=g)
         b = torch.randn(p.N, p.K, device="cuda", generator=g)
         sa, sb = 448.0 / float(a.abs().max()), 448.0 / float(b.abs().max())
-        return ((a * sa).clamp(-448, 448).to(torch.float8_e4m3fn), (b * sb).clamp(-448, 448).to(torch.float8_e4m3fn),
-                sa, sb)
+        out = ((a * sa).clamp(-448, 448).to(torch.float8_e4m3fn), (b * sb).clamp(-448, 448).to(torch.float8_e4m3fn),
+               sa, sb)
+        torch.cuda.synchronize()   # drawn on the default stream; the GEMMs run on others
+        return out
     td = torch.float16 if p.dtype == wl.F16 else torch.bfloat16
     s = 1.0 / math.sqrt(p.K)
-    return ((torch.randn(p.M, p.K, device="cuda", generator=g) * s).to(td),
-            (torch.randn(p.N, p.K, device="cuda", generator=g) * s).to(td), 1.0, 1.0)
+    out = ((torch.randn(p.M, p.K, device="cuda", generator=g) * s).to(td),
+           (torch.randn(p.N, p.K, device="cuda", generator=g) * s).to(td), 1.0, 1.0)
+    torch.cuda.synchronize()   # drawn on the default stream; the GEMMs run on others
+    return out
 
 
 def time_one(pts, h, p, A, B, C, sa, sb, sched, stream, reps):
@@ -639,6 +643,38 @@ def sweep_as_grouped(pts, dev, stream, reps=10):
     return out
 
 
+def config_points(pts, dev, stream):
+    """One GEMM per configuration point, static scheduler, library defaults,
+    each launched twice (a warm-up, then the measured one): fp16 512^3, fp16
+    4096^2 x {128, 1024, 4096}, bf16 8192^2 x {1024, 4096, 8192}, e4m3 8192^3
+    and the three tail shapes.  For profiling every point with one ncu
+    command; prints each point's event time of the second launch."""
+    probs = (wl.fp16_512() + wl.fp16_4096_ksweep([128, 1024, 4096]) + wl.bf16_8192_ksweep([1024, 4096, 8192])
+             + wl.e4m3_8192() + wl.bf16_tail())
+    out = {}
+    h = pts.gemm_create(dev, None)
+    try:
+        for i, p in enumerate(probs):
+            A, B, sa, sb = device_inputs(p, 9500 + i)
+            C = torch.empty(p.M, p.N, dtype=wl.output_torch_dtype(p.dtype), device="cuda")
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            with torch.cuda.stream(stream):
+                pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, pts.GEMM_SCHED_STATIC, sa, sb, stream)
+                ev[0].record(stream)
+                pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, pts.GEMM_SCHED_STATIC, sa, sb, stream)
+                ev[1].record(stream)
+            torch.cuda.synchronize()
+            if pts.gemm_check(h, stream)[0] != 0:
+                raise RuntimeError(f"device error in {p.name}")
+            ms = ev[0].elapsed_time(ev[1])
+            out[p.name] = {"us": round(ms * 1e3, 1), "tflops": round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1),
+                           "cta_group": int(pts.gemm_query(h, p.M, p.N, p.K, p.dtype, 1).cta_group)}
+            del A, B, C
+    finally:
+        pts.gemm_destroy(h)
+    return out
+
+
 def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES), dtype="bf16"):
     """bf16 (or e4m3) 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
     p = wl.bf16_8192_ksweep([8192])[0] if dtype == "bf16" else wl.e4m3_8192()[0]
@@ -736,6 +772,9 @@ def main():
                     help="only the 8192^3 measurement (for profiling it), restricted by --cta-group, --scheds "
                          "and --square-dtype; prints its numbers, not the benchmark line")
     ap.add_argument("--square-dtype", choices=["bf16", "e4m3"], default="bf16")
+    ap.add_argument("--points", action="store_true",
+                    help="only one GEMM per configuration point, twice each (for profiling them); prints their "
+                         "times, not the benchmark line")
     ap.add_argument("--grouped-only", action="store_true",
                     help="only the grouped 64-problem measurement (for profiling it), restricted by --cta-group and "
                          "--scheds; prints its numbers, not the benchmark line")
@@ -746,6 +785,11 @@ def main():
         out = square_8192(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
                           scheds=tuple(args.scheds), dtype=args.square_dtype)
         print(json.dumps({f"square_8192_{args.square_dtype}": out}), flush=True)
+        return
+    if args.points:
+        import persistent_tile_scheduled_gb300 as pts
+        pts.load(build_if_missing=False)
+        print(json.dumps({"config_points": config_points(pts, 0, torch.cuda.Stream())}), flush=True)
         return
     if args.grouped_only:
         import persistent_tile_scheduled_gb300 as pts
