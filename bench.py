@@ -324,6 +324,12 @@ def run_ours(args, dist, rank, world, local):
     line = finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step)
     if extras is not None:
         line["other_configs"] = extras
+    if args.square and rank == 0:
+        # context for the tensor peak (the roofline keeps the denominator above): the
+        # library's MMA-only probe, FLOP per SM clock and the aggregate at the clock it ran at
+        line["peaks"]["tensor_probe"] = {
+            name: pts.gemm_tensor_peak_probe(local, dt, 2, 100000)
+            for name, dt in (("bf16", wl.BF16), ("e4m3", wl.E4M3))}
     return line
 
 

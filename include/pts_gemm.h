@@ -271,6 +271,21 @@ gemm_status_t gemm_run_grouped(gemm_handle_t h, const gemm_group_problem_t *prob
 gemm_status_t gemm_query_grouped(gemm_handle_t h, const gemm_group_problem_t *problems, int64_t count,
                                  gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info);
 
+/* ---- tensor-pipe peak probe (a measurement aid, not a GEMM) -------------
+ * Every SM (cta_group 1) or SM pair (cta_group 2) issues `mmas` back-to-back
+ * tcgen05.mma of one k-step of the GEMM's tile (128 x 256 per CTA, 256 x 256
+ * per pair; K = 16 for fp16/bf16, 32 for e4m3) on finite operands already in
+ * shared memory: no loads, stores or epilogue, so only the tensor pipe limits
+ * it.  It measures the dense FLOP per SM clock that the GEMM's "% of tensor
+ * peak" assumes ("Persistent Kernels with Cluster Launch Control" names the
+ * tcgen05 2-SM MMA; the rate is not on the pages).  Outputs: the median over
+ * SMs of FLOP per SM clock, the aggregate FLOP/s over all SMs (TFLOP/s) and
+ * the median SM clock it ran at (GHz).  mmas in [1, 2^20]; synchronous; the
+ * device is made current.  GEMM_ERR_UNSUPPORTED off compute capability 10.3,
+ * GEMM_ERR_TIMEOUT if the MMAs did not complete within 2 s. */
+gemm_status_t gemm_tensor_peak_probe(int device, gemm_dtype_t dtype, int cta_group, int64_t mmas,
+                                     double *flop_per_clk_per_sm, double *tflops, double *sm_ghz);
+
 /* Launch shape gemm_run would use (no GPU work).  Same argument rules. */
 gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                          gemm_dtype_t dtype, gemm_sched_t sched, gemm_launch_info_t *info);

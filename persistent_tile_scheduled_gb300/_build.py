@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libpts_gemm.so")
-UNITS = ["gemm_cg1.cu", "gemm_cg2.cu", "gemm_api.cu", "gemm_noalloc.cu"]
+UNITS = ["gemm_cg1.cu", "gemm_cg2.cu", "gemm_api.cu", "gemm_noalloc.cu", "peak_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

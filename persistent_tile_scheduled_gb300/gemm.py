@@ -23,7 +23,7 @@ GEMM_DEBUG_FAULT_SKIP_TMA = 0x4
 
 EXPORTED = ("gemm_create", "gemm_run", "gemm_run_host", "gemm_query", "gemm_check",
             "gemm_read_debug", "gemm_destroy", "gemm_status_string", "gemm_run_noalloc",
-            "gemm_run_host_batch", "gemm_run_grouped", "gemm_query_grouped")
+            "gemm_run_host_batch", "gemm_run_grouped", "gemm_query_grouped", "gemm_tensor_peak_probe")
 GEMM_NOALLOC_MAX_WORK_ITEMS = 16384
 GEMM_GROUPED_MAX_PROBLEMS = 65536
 
@@ -112,6 +112,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int, f32, f32,
                                      ctypes.c_int, vp, ctypes.POINTER(ctypes.c_int)]
     lib.gemm_run_noalloc.restype = st
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.gemm_tensor_peak_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, dp, dp, dp]
+    lib.gemm_tensor_peak_probe.restype = st
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -247,6 +250,14 @@ def gemm_run_noalloc(M, N, K, A, B, C, dtype, sched, scale_a=1.0, scale_b=1.0, c
                                  float(scale_b), int(cta_group), _stream(stream),
                                  ctypes.byref(dev) if check else None)
     return st, dev.value
+
+
+def gemm_tensor_peak_probe(device, dtype, cta_group, mmas=20000) -> dict:
+    """The tensor-pipe peak probe: {"flop_per_clk_per_sm", "tflops", "sm_ghz"}."""
+    f, t, g = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(load().gemm_tensor_peak_probe(int(device), int(dtype), int(cta_group), int(mmas), ctypes.byref(f),
+                                         ctypes.byref(t), ctypes.byref(g)), "gemm_tensor_peak_probe")
+    return {"flop_per_clk_per_sm": f.value, "tflops": t.value, "sm_ghz": g.value}
 
 
 def gemm_destroy(h) -> int:

@@ -405,3 +405,13 @@ def test_wait_time_out_is_reported_and_the_context_survives(cg, sched):
         assert compare_full(x, C) <= TOL[wl.BF16]
     finally:
         pts.gemm_destroy(h)
+
+
+@pytest.mark.parametrize("dtype,per_clk", [(wl.F16, 8192), (wl.BF16, 8192), (wl.E4M3, 16384)])
+@pytest.mark.parametrize("cg", [1, 2])
+def test_tensor_peak_probe_pins_the_per_sm_rate(dtype, per_clk, cg):
+    """The dense rate the '% of tensor peak' figures assume: 8192 FLOP per SM
+    clock for fp16/bf16 and 16384 for e4m3 (measured by an MMA-only loop)."""
+    r = pts.gemm_tensor_peak_probe(0, dtype, cg, 20000)
+    assert 0.85 * per_clk <= r["flop_per_clk_per_sm"] <= 1.02 * per_clk, r
+    assert 0.5 < r["sm_ghz"] < 2.2, r
