@@ -1,8 +1,8 @@
 """Build the CUDA library libpts_gemm.so in-tree with nvcc for sm_103a.
 
-Four translation units (the 1-SM kernels, the 2-SM kernels, the C ABI and
-the allocation-free entry point) are compiled in parallel, then linked with
-the static CUDA runtime.  Nothing is rebuilt when the library is newer than
+Five translation units (the 1-SM kernels, the 2-SM kernels, the C ABI, the
+allocation-free entry point and the tensor-pipe peak probe) are compiled in
+parallel, then linked with the static CUDA runtime.  Nothing is rebuilt when the library is newer than
 every source file.
 """
 from __future__ import annotations
