@@ -318,7 +318,7 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
  * nothing: no cudaMalloc, no cudaFree, no host heap.  The kernel's scratch --
  * a 4-word device status block and one gemm_tile_record_t per work item (the
  * coverage counters) -- lives in a file-scope __device__ array of
- * 256 + 48 * GEMM_NOALLOC_MAX_WORK_ITEMS bytes (768.25 KiB) that every GPU which
+ * 256 + 52 * GEMM_NOALLOC_MAX_WORK_ITEMS bytes (832.25 KiB) that every GPU which
  * loads the library holds until the process exits.
  *   - Problems with more than GEMM_NOALLOC_MAX_WORK_ITEMS work items are
  *     rejected with GEMM_ERR_INVALID_ARG before anything is launched (work

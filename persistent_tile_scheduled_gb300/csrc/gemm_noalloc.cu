@@ -28,7 +28,7 @@ constexpr size_t kScratchBytes =
 }  // namespace
 
 // Scratch of every call: [0, 256) status block, then one record per work item.
-// Every GPU that loads this library holds it (kScratchBytes = 768.25 KiB)
+// Every GPU that loads this library holds it (kScratchBytes = 832.25 KiB)
 // until the process exits.  Calls share it; calls that overlap on the GPU race.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
