@@ -1,0 +1,117 @@
+"""The launch plan's host-side rules (csrc/gemm_params.h), compiled for the
+host and checked on the CPU: the stream-K partition helpers against the
+scheduler model (oracle/sched.py, which writes the partition out k-block by
+k-block), and the thresholds and shared-memory budget the launcher uses."""
+import json
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+from oracle import sched as sm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "persistent_tile_scheduled_gb300", "csrc")
+
+CASES = [(5, 3, 4), (7, 3, 1), (104, 76, 64), (256, 76, 64), (300, 152, 5), (31, 16, 9), (1024, 76, 128),
+         (28, 28, 3), (77, 76, 2)]
+
+PROGRAM = r"""
+#include <cstdio>
+#include "gemm_params.h"
+using namespace pts;
+int main() {
+    const long long cases[][3] = {%CASES%};
+    printf("{\"cases\": [");
+    for (unsigned i = 0; i < sizeof(cases) / sizeof(cases[0]); ++i) {
+        const long long T = cases[i][0], G = cases[i][1], kb = cases[i][2];
+        const long long sk1 = choose_stream_k(T, G, kb, 1), sk0 = choose_stream_k(T, G, kb, 0),
+                        skn = choose_stream_k(T, G, kb, -1);
+        printf("%s{\"T\": %lld, \"G\": %lld, \"kb\": %lld, \"sk_force\": %lld, \"sk_auto\": %lld, \"sk_never\": %lld",
+               i ? ", " : "", T, G, kb, sk1, sk0, skn);
+        const long long L = sk1 * kb;
+        printf(", \"begin\": [");
+        for (long long c = 0; sk1 && c < G; ++c) printf("%s%lld", c ? ", " : "", (long long)sk_unit_begin(c, L, G));
+        printf("], \"pieces\": [");
+        for (long long c = 0; sk1 && c < G; ++c) printf("%s%d", c ? ", " : "", sk_pieces(c, L, G, kb));
+        printf("], \"owner\": [");
+        for (long long x = 0; x < L; ++x) printf("%s%lld", x ? ", " : "", (long long)sk_unit_of(x, L, G));
+        printf("]}");
+    }
+    printf("], \"split\": [");
+    const long long sp[][2] = {{8, 152}, {38, 152}, {39, 152}, {76, 152}, {77, 152}, {151, 152}, {152, 152}, {500, 152}};
+    for (unsigned i = 0; i < sizeof(sp) / sizeof(sp[0]); ++i)
+        printf("%s[%lld, %lld, %d]", i ? ", " : "", sp[i][0], sp[i][1], choose_split(sp[i][0], sp[i][1]));
+    printf("], \"cta_group\": [");
+    for (int kb = 1; kb <= 40; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb));
+    printf("], \"pair_min_kb\": %d, \"sk_min_saved_kb\": %d", kPairMinKb, kSkMinSavedKb);
+    printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]}\n", kb_per_stage(1), kb_per_stage(2),
+           smem_bytes(1, 4), smem_bytes(2, 3), smem_bytes(1, 5));
+    return 0;
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def plan():
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc is needed to compile the host program")
+    src = PROGRAM.replace("%CASES%", ", ".join("{%d, %d, %d}" % c for c in CASES))
+    with tempfile.TemporaryDirectory() as d:
+        cu, exe = os.path.join(d, "plan.cu"), os.path.join(d, "plan")
+        open(cu, "w").write(src)
+        subprocess.run([nvcc, "-std=c++17", "-I", CSRC, cu, "-o", exe], check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    return json.loads(out)
+
+
+def test_stream_k_partition_matches_the_model(plan):
+    for case in plan["cases"]:
+        T, G, kb, sk = case["T"], case["G"], case["kb"], case["sk_force"]
+        R = T % G
+        assert sk == (R + G if T >= G and R else 0), case
+        assert case["sk_never"] == 0
+        if not sk:
+            continue
+        units = sm.work_units(T, num_kb=kb, sk_tiles=sk, sk_units=G)
+        L = sk * kb
+        for c in range(G):
+            items = units[c]
+            assert case["pieces"][c] == len(items), (case, c)
+            # the unit's first k-block of the region: its last-run piece is its first tile
+            t, k0 = items[-1][1], items[-1][4]
+            assert case["begin"][c] == t * kb + k0, (case, c)
+        owner = [None] * L
+        for c in range(G):
+            for _, t, _, _, k0, k1 in units[c]:
+                for k in range(k0, k1):
+                    owner[t * kb + k] = c
+        assert case["owner"] == owner, case
+
+
+def test_stream_k_is_used_only_when_it_saves_enough(plan):
+    m = plan["sk_min_saved_kb"]
+    for case in plan["cases"]:
+        T, G, kb = case["T"], case["G"], case["kb"]
+        R = T % G
+        want = case["sk_force"] if (case["sk_force"] and kb * (G - R) >= m * G) else 0
+        assert case["sk_auto"] == want, case
+
+
+def test_slices_and_cta_group_thresholds(plan):
+    for tiles, resident, split in plan["split"]:
+        want = 1 if tiles >= resident else (4 if 4 * tiles <= resident else (2 if 2 * tiles <= resident else 1))
+        assert split == want, (tiles, resident)
+    k = plan["pair_min_kb"]
+    assert plan["cta_group"] == [2 if kb >= k else 1 for kb in range(1, 41)]
+
+
+def test_shared_memory_budget(plan):
+    single, pair, five = plan["smem"]
+    assert plan["kb_per_stage"] == [1, 2]
+    # the default rings (4 single-CTA stages, 3 pair stages) fit the 227 KB a CTA may use; a
+    # fifth single-CTA stage does not
+    assert single <= 232448 and pair <= 232448 and five > 232448
