@@ -118,3 +118,15 @@ def test_no_cpu_fallback_in_the_package():
                 text = open(os.path.join(dirpath, f)).read()
                 for banned in ("oracle", "matmul", " @ ", "torch.mm", "einsum"):
                     assert banned not in text, (f, banned)
+
+
+def test_group_problem_marshalling():
+    """The binding packs (M, N, K, A, B, C[, scale_a, scale_b]) into the C
+    struct field by field; raw addresses pass through unchanged."""
+    arr = g.group_array([(3, 8, 16, 0x1000, 0x2000, 0x3000), (0, 64, 0, 0, 0, 0x4000, 2.0, 0.5)])
+    assert arr.count == 2
+    a, b = arr.arr[0], arr.arr[1]
+    assert (a.M, a.N, a.K, a.A, a.B, a.C, a.scale_a, a.scale_b) == (3, 8, 16, 0x1000, 0x2000, 0x3000, 1.0, 1.0)
+    assert (b.M, b.N, b.K, b.A, b.B, b.C, b.scale_a, b.scale_b) == (0, 64, 0, None, None, 0x4000, 2.0, 0.5)
+    assert g.group_array(arr) is arr
+    assert g.group_array([]).count == 0

@@ -285,3 +285,19 @@ def test_e4m3_inputs_hit_max():
     b = og.decode_np(x.bits("B"), og.E4M3)
     assert np.abs(a).max() == 448.0 and np.abs(b).max() == 448.0
     assert np.isfinite(a).all() and np.isfinite(b).all()
+
+
+def test_grouped_workload_recipe():
+    """64 bf16 problems of 1024 x 1024, K log-uniform in [256, 8192] as
+    multiples of 8, drawn the same way every time; problem i seeded 6001 + i."""
+    ps, qs = wl.bf16_grouped_vark(), wl.bf16_grouped_vark()
+    assert ps == qs and len(ps) == 64
+    ks = [p.K for p in ps]
+    assert all(p.M == 1024 and p.N == 1024 and p.dtype == wl.BF16 and p.dist == "normal_sqrtk" for p in ps)
+    assert all(k % 8 == 0 and 256 <= k <= 8192 for k in ks)
+    assert [p.seed for p in ps] == list(range(6001, 6065))
+    # log-uniform: about as many problems below the geometric midpoint 2^10.5 as above it
+    below = sum(k < 2 ** 10.5 for k in ks)
+    assert 20 <= below <= 44
+    assert max(ks) / min(ks) > 16   # tile costs differ by more than an order of magnitude
+
