@@ -212,3 +212,40 @@ def test_grouped_items_cover_every_problem_tile_once(seed):
     # problems in order, each a contiguous run
     gs = [g for g, _, _ in items]
     assert gs == sorted(gs)
+
+
+def test_grouped_workload_model_predicts_clc_ahead_of_static():
+    """The 64-problem grouped workload in the scheduler model (CTA pairs: 16
+    tiles per problem, 76 resident clusters, a tile costing its k-blocks
+    plus 6): the static stride finishes last, CLC's first-come order ends
+    near the even split, and listing the problems most k-blocks first brings
+    both closer to it."""
+    import workloads as wl
+    ps = wl.bf16_grouped_vark()
+    G = 76
+
+    def costs(order):
+        return [-(-ps[g].K // 64) + 6 for g in order for _ in range(16)]
+
+    def static_makespan(c):
+        load = [0.0] * G
+        for w, x in enumerate(c):
+            load[w % G] += x
+        return max(load)
+
+    def clc_makespan(c):
+        events, _, _ = sm.clc_replay(len(c), G, cost=lambda w: float(c[w]))
+        end = {}
+        # replay order: a cluster's tiles run back to back, so its finish is the sum of its costs
+        for w, cluster, _ in events:
+            end[cluster] = end.get(cluster, 0.0) + c[w]
+        return max(end.values())
+
+    given = list(range(len(ps)))
+    longest = sorted(given, key=lambda g: -ps[g].K)
+    even = sum(costs(given)) / G
+    st, cl = static_makespan(costs(given)), clc_makespan(costs(given))
+    st_l, cl_l = static_makespan(costs(longest)), clc_makespan(costs(longest))
+    assert st > cl > even and st_l > cl_l >= even
+    assert cl_l < cl and st_l < st
+    assert cl < 1.1 * even and cl_l < 1.02 * even and st > 1.2 * even
