@@ -131,6 +131,19 @@ def profile_traffic():
     return d.get("dram_bytes_per_launch_k4096"), d.get("launch")
 
 
+def profile_value(name, key):
+    """A per-launch figure from a committed ncu summary (profiles/<name>),
+    only if that capture was taken on the kernel sources as they are now."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_sources_sha256_16") != kernel_hash():
+        return None
+    return d.get(key)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -192,15 +205,21 @@ def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
 
-def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_graph=True):
+def sweep_pass(pts, h, bufs, problems, sched, stream):
+    """One step: the sweep's GEMMs, one gemm_run launch each, in K order, on
+    `stream` (also what a captured step holds)."""
+    for p, (A, B, C) in zip(problems, bufs):
+        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+
+
+def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_graph=False):
     """Warm-up, then `steps` timed passes over the sweep (events only at step
-    boundaries, so consecutive GEMMs may overlap their launches), then one
+    boundaries, so consecutive GEMMs may overlap their launches), then three
     extra passes with an event between GEMMs for the per-K breakdown.  With
-    use_graph the 32 launches of a pass are captured once in a CUDA graph and
+    use_graph the launches of a pass are captured once in a CUDA graph and
     each step replays it (the same kernels, without the host launch cost)."""
     def one_pass():
-        for p, (A, B, C) in zip(problems, bufs):
-            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
+        sweep_pass(pts, h, bufs, problems, sched, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -317,11 +336,21 @@ def run_ours(args, dist, rank, world, local):
         e2e = None
         if args.e2e:
             e2e = end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream)
-        extra = square_8192(pts, local, stream) if args.square and rank == 0 else None
+        peaks, peaks_src = load_peaks()
+        target = target_8192(pts, local, stream, peaks, peaks_src) if args.square and rank == 0 else None
+        small = small_points(pts, local, stream, peaks) if args.extras and rank == 0 else None
+        sweep8 = bf16_8192_sweep(pts, local, stream, peaks) if args.extras and rank == 0 else None
         extras = extra_configs(pts, local, stream) if args.extras and rank == 0 else None
     finally:
         pts.gemm_destroy(h)
-    line = finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step)
+    line = finish(args, per_sched, problems, world, clocks, e2e, None, rank, xs, flops_step)
+    if target is not None:
+        line["bf16_8192_cubed"] = target
+    if small is not None:
+        line["fp16_512"] = small.pop("fp16_512")
+        line["fp16_4096_small_k"] = small
+    if sweep8 is not None:
+        line["bf16_8192_ksweep"] = sweep8
     if extras is not None:
         line["other_configs"] = extras
     if args.square and rank == 0:
@@ -331,6 +360,161 @@ def run_ours(args, dist, rank, world, local):
             name: pts.gemm_tensor_peak_probe(local, dt, 2, 100000)
             for name, dt in (("bf16", wl.BF16), ("e4m3", wl.E4M3))}
     return line
+
+
+def point_roofline(p, ms, peaks):
+    """Roofline of one GEMM: attainable = min(dense tensor peak, I * HBM
+    bandwidth) with I = 2MNK / (compulsory bytes e*(MK + NK) + 2MN); e4m3 runs
+    at twice the bf16 tensor rate."""
+    tensor = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
+    hbm = peak_value(peaks, "hbm_gbs", "hbm_GBs")
+    fl = gemm_flops(p.M, p.N, p.K)
+    e = 1.0 if p.dtype == wl.E4M3 else 2.0
+    q = e * (p.M * p.K + p.N * p.K) + 2.0 * p.M * p.N
+    if not tensor or not hbm:
+        return {"tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
+    t_peak = tensor * (2.0 if p.dtype == wl.E4M3 else 1.0)
+    attain = min(t_peak, fl / q * hbm * 1e-3)
+    got = fl / (ms * 1e-3) / 1e12
+    return {"tflops": round(got, 1), "bound": "tensor" if attain == t_peak else "hbm",
+            "attainable_tflops": round(attain, 1), "frac": round(got / attain, 3)}
+
+
+def time_launches(pts, h, p, A, B, C, sa, sb, sched, stream, reps, flush=None):
+    """Median CUDA-event time (ms) of one gemm_run launch: back to back on the
+    same buffers, or, with `flush` (a buffer larger than L2), each launch
+    after the flush buffer was overwritten so that it starts with a cold L2."""
+    for _ in range(3):
+        pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, sa, sb, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            if flush is not None:
+                flush.zero_()
+            e0.record(stream)
+            pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, sa, sb, stream)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    if pts.gemm_check(h, stream)[0] != 0:
+        raise RuntimeError(f"device error in {p.name}")
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+
+
+def target_8192(pts, dev, stream, peaks, peaks_src, reps=10):
+    """bf16 M = N = K = 8192 (the largest point of the bf16 sweep) per
+    scheduler with the library's defaults (CTA pairs at this K), each a median
+    of back-to-back launches on 268 MB of A and B (above the 129 MB L2); its
+    own clock record and roofline.  Single CTAs and pairs forced are listed
+    too."""
+    p = wl.bf16_8192_ksweep([8192])[0]
+    A, B, sa, sb = device_inputs(p, 3000 + 8192)
+    C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+    out = {"workload": "bf16 GEMM M=N=K=8192, A,B ~ N(0,1)/sqrt(K), fp32 accumulate, bf16 C"}
+    h = pts.gemm_create(dev, None)
+    sampler = ClockSampler(dev)
+    try:
+        out["cta_group"] = int(pts.gemm_query(h, p.M, p.N, p.K, p.dtype, 1).cta_group)
+        sampler.__enter__()
+        t0 = time.time()
+        for si, name in enumerate(SCHED_NAMES):
+            ms = time_launches(pts, h, p, A, B, C, sa, sb, si, stream, reps)
+            out[name] = round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1)
+            out[name + "_ms"] = round(ms, 4)
+        t1 = time.time()
+        sampler.__exit__(None, None, None)
+        out["clocks"] = sampler.summary(t0, t1)
+    finally:
+        pts.gemm_destroy(h)
+    for cg in (1, 2):
+        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
+        try:
+            for si, name in enumerate(SCHED_NAMES):
+                ms = time_launches(pts, h, p, A, B, C, sa, sb, si, stream, 5)
+                out[f"cg{cg}_{name}"] = round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1)
+        finally:
+            pts.gemm_destroy(h)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tensor = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
+    mhz_max = peak_value(peaks, "sm_max_mhz") or 2070.0
+    theo = sms * 8192 * mhz_max * 1e6 / 1e12      # dense FLOP per SM clock pinned by the probe test
+    mhz = out["clocks"].get("sm_mhz")
+    best = max(out["static"], out["clc"])
+    traffic = profile_value("gemm_kernel_bf16_8192.json", "dram_bytes_per_launch")
+    out["roofline"] = {
+        "bound": "tensor", "achieved": out["static"], "peak": tensor, "unit": UNIT,
+        "frac": round(out["static"] / tensor, 4) if tensor else None,
+        "traffic": traffic, "peak_source": f"{peaks_src} bf16 dense, burst",
+        "achieved_def": "2*8192^3 / median CUDA-event time of one launch, static scheduler, library defaults",
+        "theoretical_tflops_at_max_clock": round(theo, 1),
+        "frac_of_theoretical": round(out["static"] / theo, 4),
+        "frac_of_theoretical_at_sampled_clock": (round(out["static"] / (sms * 8192 * mhz * 1e6 / 1e12), 4)
+                                                 if mhz else None),
+        "best_persistent_frac_of_theoretical": round(best / theo, 4),
+    }
+    out["persistent_ahead"] = min(out["static"], out["clc"]) > out["nonpersistent"]
+    del A, B, C
+    return out
+
+
+def small_points(pts, dev, stream, peaks, reps=20):
+    """fp16 512^3 (U[-1,1], 8 tiles) and the small-K end of the fp16 4096
+    sweep, per scheduler, library defaults: back to back on the same buffers
+    (the data stays in L2 between launches) and with L2 flushed before every
+    launch (a 256 MB buffer overwritten; not timed)."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    h = pts.gemm_create(dev, None)
+    try:
+        for p in wl.fp16_512() + wl.fp16_4096_ksweep([128, 256, 384, 512]):
+            x = wl.make_inputs(p)
+            A, B = x.A.cuda(), x.B.cuda()
+            C = torch.empty(p.M, p.N, dtype=torch.float16, device="cuda")
+            torch.cuda.synchronize()
+            row = {"M": p.M, "N": p.N, "K": p.K,
+                   "cta_group": int(pts.gemm_query(h, p.M, p.N, p.K, p.dtype, 1).cta_group)}
+            for si, name in enumerate(SCHED_NAMES):
+                warm = time_launches(pts, h, p, A, B, C, 1.0, 1.0, si, stream, reps)
+                cold = time_launches(pts, h, p, A, B, C, 1.0, 1.0, si, stream, reps, flush=flush)
+                row[name] = {"us": round(warm * 1e3, 2), "l2_flushed_us": round(cold * 1e3, 2),
+                             **point_roofline(p, warm, peaks),
+                             "l2_flushed": point_roofline(p, cold, peaks)}
+            out[p.name if p.name == "fp16_512" else f"K{p.K}"] = row
+            del A, B, C
+    finally:
+        pts.gemm_destroy(h)
+    del flush
+    out["note"] = (f"median of {reps} launches per scheduler; 'us' back to back on the same buffers, "
+                   "'l2_flushed_us' each launch after a 256 MB buffer was overwritten (L2 is 129 MB)")
+    return out
+
+
+def bf16_8192_sweep(pts, dev, stream, peaks, reps=5):
+    """The bf16 M = N = 8192 sweep, K = 256..8192 step 256 (32 GEMMs), per
+    scheduler, library defaults: TFLOP/s per K (median of back-to-back
+    launches) and its fraction of the point's roofline."""
+    h = pts.gemm_create(dev, None)
+    out = {"K": [], "attainable_tflops": []}
+    try:
+        for i, p in enumerate(wl.bf16_8192_ksweep()):
+            A, B, sa, sb = device_inputs(p, 6000 + i)
+            C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+            out["K"].append(p.K)
+            for si, name in enumerate(SCHED_NAMES):
+                ms = time_launches(pts, h, p, A, B, C, sa, sb, si, stream, reps)
+                r = point_roofline(p, ms, peaks)
+                out.setdefault(name, []).append(r["tflops"])
+                out.setdefault(name + "_frac", []).append(r.get("frac"))
+            out["attainable_tflops"].append(r.get("attainable_tflops"))
+            del A, B, C
+    finally:
+        pts.gemm_destroy(h)
+    for name in SCHED_NAMES:
+        out[name + "_mean"] = round(sum(out[name]) / len(out[name]), 1)
+    out["persistent_ahead_at_every_K"] = all(
+        min(s_, c_) > n_ for s_, c_, n_ in zip(out["static"], out["clc"], out["nonpersistent"]))
+    out["note"] = (f"median of {reps} back-to-back launches per K; inputs drawn on the GPU from seeded "
+                   "generators (parity for these shapes is in the tests)")
+    return out
 
 
 def end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream):
@@ -390,7 +574,8 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
         "data": "synthetic (seeded N(0,1)/sqrt(K), rounded to fp16)",
         "config": {"workload": WORKLOAD, "tile": TILE_DESC[args.cta_group], "group_size_m": 8,
                    "cta_group": args.cta_group, "split_k": args.split_k, "sched": HEADLINE,
-                   "launch": "CUDA graph of the 32 gemm_run launches per step" if args.graph else "eager",
+                   "launch": ("CUDA graph of the 32 gemm_run launches per step" if args.graph
+                              else "32 gemm_run calls per step, launched one by one"),
                    "l2": "no flush: one step's 32 distinct A,B,C sets (2.1 GB) exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_tensor_peak": round(achieved / tensor_peak, 4) if tensor_peak else None,
@@ -449,24 +634,12 @@ def time_one(pts, h, p, A, B, C, sa, sb, sched, stream, reps):
 
 
 def extra_configs(pts, dev, stream):
-    """The other workloads, TFLOP/s per scheduler: the whole bf16 8192 sweep,
-    e4m3 8192^3, the tail shapes, and two GEMMs at once on two streams."""
+    """The other workloads, TFLOP/s per scheduler: e4m3 8192^3, the tail
+    shapes, two GEMMs at once on two streams, the half-occupied GPU and the
+    grouped launches."""
     out = {}
     h = pts.gemm_create(dev, pts.make_opts(cta_group=0))
     try:
-        # bf16 M = N = 8192, every K of the sweep (one K at a time, inputs freed after)
-        sweep = {"K": []}
-        for i, p in enumerate(wl.bf16_8192_ksweep()):
-            A, B, sa, sb = device_inputs(p, 6000 + i)
-            C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
-            sweep["K"].append(p.K)
-            for si, name in enumerate(SCHED_NAMES):
-                ms = time_one(pts, h, p, A, B, C, sa, sb, si, stream, 5)
-                sweep.setdefault(name, []).append(round(gemm_flops(p.M, p.N, p.K) / (ms * 1e-3) / 1e12, 1))
-            del A, B, C
-        sweep["persistent_ahead_at_every_K"] = all(
-            min(s_, c_) > n_ for s_, c_, n_ in zip(sweep["static"], sweep["clc"], sweep["nonpersistent"]))
-        out["bf16_8192_ksweep"] = sweep
         probs = wl.e4m3_8192() + wl.bf16_tail()
         for i, p in enumerate(probs):
             A, B, sa, sb = device_inputs(p, 7000 + i)
@@ -772,8 +945,9 @@ def main():
                     help="stream-K share of the last waves: 0 = the library's choice, 1 = always, -1 = never")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],
                     help="0 default, 1 TMA stores through shared memory, 2 direct stores from registers")
-    ap.add_argument("--no-graph", dest="graph", action="store_false",
-                    help="launch the 32 GEMMs of a step one by one instead of replaying a CUDA graph")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the 32 launches of a step in a CUDA graph and replay it (default: every step "
+                         "launches them one by one with gemm_run)")
     ap.add_argument("--square-only", action="store_true",
                     help="only the 8192^3 measurement (for profiling it), restricted by --cta-group, --scheds "
                          "and --square-dtype; prints its numbers, not the benchmark line")

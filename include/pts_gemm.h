@@ -185,7 +185,13 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
  * M, N, K < 2^31.  M == 0 or N == 0 launches nothing; K == 0 writes zeros.
  * scale_a, scale_b: e4m3 per-tensor scales (> 0, finite); ignored otherwise.
  * Returns after the launch; device-side errors (wait time-outs) are read with
- * gemm_check or gemm_read_debug. */
+ * gemm_check or gemm_read_debug.
+ * CUDA graphs: a gemm_run launch may be captured and the graph replayed any
+ * number of times.  Each launch leaves the stream-K claim counters and ready
+ * flags it used at zero, so a replay starts exactly like a fresh launch.
+ * The workspace is grown (cudaMalloc, cudaMemset) by the first call that
+ * needs more than the handle holds, which a capturing stream does not allow:
+ * make one call of the same shape before capturing. */
 gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        const void *A, const void *B, void *C,
                        gemm_dtype_t dtype, gemm_sched_t sched,
@@ -292,7 +298,9 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
 
 /* Synchronise `stream`, read and clear the device status block.
  * device_status (may be NULL) receives the raw first error word (0 = none).
- * Returns GEMM_ERR_TIMEOUT if a device wait timed out since the last check. */
+ * Returns GEMM_ERR_TIMEOUT if a device wait timed out since the last check.
+ * After an error it also zeroes the handle's stream-K claim counters and
+ * ready flags, which a launch that stopped early may have left set. */
 gemm_status_t gemm_check(gemm_handle_t h, void *stream, int *device_status);
 
 /* After a run with GEMM_DEBUG_RECORDS: synchronise `stream`, copy the
@@ -327,6 +335,8 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
  *   - The first call on a device does a one-time set-up on that device (the
  *     scratch array's device address via cudaGetSymbolAddress, kernel
  *     attributes, occupancy); make that first call before any stream capture.
+ *     Only a set-up that succeeds is kept: if it fails, that call returns
+ *     the error and the next call on the device tries the set-up again.
  *   - Every call clears the status block and its work items' records with a
  *     cudaMemsetAsync on `stream`, then launches on `stream`.
  *   - All calls share the one scratch array, which keeps the last call's

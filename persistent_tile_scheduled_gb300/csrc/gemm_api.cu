@@ -49,9 +49,8 @@ struct gemm_ctx {
     size_t host_bufs_cap = 0;
     float *d_ws_partial = nullptr;            // stream-K fixup workspace
     size_t ws_partial_cap = 0;                // bytes
-    uint32_t *d_ws_sync = nullptr;            // stream-K claim counters / ready flags
+    uint32_t *d_ws_sync = nullptr;            // stream-K claim counters / ready flags (zero between launches)
     size_t ws_sync_cap = 0;                   // bytes
-    uint32_t epoch = 0;                       // launch number for the fixup counters (1 .. 2^29 - 1)
     // gemm_run_host_batch: staging slots (A | B | C each), copy streams and events
     void *d_slot[kBatchSlots] = {};
     size_t slot_cap = 0;
@@ -273,8 +272,6 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
             h->ws_sync_cap = need_s;
         }
     }
-    h->epoch = h->epoch % 0x1FFFFFFFu + 1u;
-
     // Each map is copied out of the cache at once: a later lookup in this same
     // call may reuse the cache slot an earlier map came from.
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
@@ -310,7 +307,6 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.split = pl.split;
     p.sk_tiles = static_cast<int32_t>(pl.sk_tiles);
     p.sk_units = static_cast<int32_t>(pl.sk_units);
-    p.epoch = h->epoch;
     p.ws_partial = pl.sk_units > 0 ? h->d_ws_partial : nullptr;
     p.ws_sync = pl.sk_units > 0 ? h->d_ws_sync : nullptr;
     p.num_units = static_cast<int32_t>(pl.units);
@@ -557,6 +553,11 @@ gemm_status_t read_status(gemm_ctx *h, cudaStream_t stream, int *device_status)
     if (cudaMemcpy(s, h->d_status, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
         return cuda_fail(cudaErrorUnknown);
     if (s[0] != 0 && cudaMemset(h->d_status, 0, sizeof(s)) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    // A launch that stopped on an error may have left stream-K claim counters
+    // or ready flags set (a completed launch leaves them at zero): clear them
+    // so that the next launch starts clean.
+    if (s[0] != 0 && h->d_ws_sync != nullptr && cudaMemset(h->d_ws_sync, 0, h->ws_sync_cap) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
     if (device_status) *device_status = s[0] == 0 ? 0 : (s[0] << 24) | ((s[1] & 0xff) << 16) | (s[2] & 0xffff);
     return s[0] == pts::DEV_ERR_TIMEOUT ? GEMM_ERR_TIMEOUT : GEMM_OK;
 }

@@ -216,27 +216,17 @@ __device__ __forceinline__ int unit_item(int u, int j, int pieces, const GemmPar
 // Stream-K fixup, per (cut tile, CTA of the pair, epilogue warp): the warp's
 // 32 rows of the tile are reduced independently of the other warps, so no
 // warp ever waits for another warp of its CTA.  Sync words: [0] claim counter
-// (epoch << 3 | pieces claimed), [1] ready flag of the partial slot (the
-// epoch of the launch that filled it).  A cut tile has kSkMaxParts pieces and
-// kSkMaxParts - 1 partial slots.
+// (pieces claimed so far), [1 .. kSkMaxParts - 1] ready flags of the partial
+// slots (1 = filled).  A cut tile has kSkMaxParts pieces and kSkMaxParts - 1
+// partial slots.  Every launch finds the words at zero and leaves them at
+// zero: the last piece to claim, once it has seen every flag raised, is the
+// only one of the launch still to touch them and resets them.  Nothing the
+// host passes in tags them, so a launch captured in a CUDA graph and replayed
+// behaves exactly like a fresh one.  (A launch that stops on a device error
+// may leave them set; reading that error through the handle clears them.)
 // Partial slot layout: float4 index (chunk * 16 + g) * 32 + lane, so every
 // warp-wide access is 512 contiguous bytes.
 constexpr int kPartialFloat4PerWarp = kEpiRowsPerWarp * kTileN / 4;
-
-// Claim the next part number of this launch (epoch); 0 when the counter still
-// holds an earlier launch's value.
-__device__ __forceinline__ uint32_t fixup_claim(uint32_t *cnt, uint32_t epoch)
-{
-    uint32_t old = atomicAdd(cnt, 0u);
-    for (;;) {
-        const bool fresh = (old >> 3) != epoch;
-        const uint32_t mine = fresh ? 0u : (old & 7u);
-        const uint32_t next = fresh ? ((epoch << 3) | 1u) : old + 1u;
-        const uint32_t prev = atomicCAS(cnt, old, next);
-        if (prev == old) return mine;
-        old = prev;
-    }
-}
 
 struct WaitCtl {
     uint32_t abort_addr;       // this CTA's abort flag (shared::cta)
@@ -570,7 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) {
             // Stopped early: let the loads already issued land before the
-            // CTA can exit (bounded; the pair's loads signal the leader).
+            // CTA can exit (bounded).  The leader drains the full barriers of
+            // its last stages, on which both CTAs' loads of those stages
+            // complete.  The peer may have issued a stage the leader never
+            // armed (the leader stopped first): that load completes on a
+            // leader barrier whose phase can no longer finish, so nothing can
+            // be waited on for it, and the peer instead lets a bounded 1 ms
+            // pass, far longer than any load takes, before it goes on to the
+            // teardown barrier.
             if (CG == 1 || leader) {
                 const long long n = issued < S ? issued : S;
                 for (long long j = 0; j < n; ++j) {
@@ -578,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ctl.drain(full0 + 8 * static_cast<int>(g % S), static_cast<uint32_t>((g / S) & 1),
                               10000000ull);
                 }
-            } else {
+            } else if (issued > 0) {
                 const uint64_t t0 = globaltimer_ns();
                 while (globaltimer_ns() - t0 < 1000000ull) {
                 }
@@ -730,23 +727,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 partials = reinterpret_cast<const float4 *>(p.ws_partial)
                            + unit * (nparts - 1) * kPartialFloat4PerWarp;
                 uint32_t mine = 0;
-                if (lane == 0) mine = fixup_claim(sync, p.epoch);
+                if (lane == 0) mine = atomicAdd(sync, 1u);
                 part = static_cast<int>(__shfl_sync(0xffffffffu, mine, 0));
                 if (part == nparts - 1) {
+                    uint32_t seen = 1u;
                     if (lane == 0) {
-                        for (int sl = 0; sl < nparts - 1; ++sl) {
+                        for (int sl = 0; sl < nparts - 1 && seen; ++sl) {
                             const uint64_t t0 = globaltimer_ns();
-                            while (ld_acquire_gpu(sync + 1 + sl) != p.epoch) {
-                                if (ld_shared_u32(abort_flag)) break;
+                            while (ld_acquire_gpu(sync + 1 + sl) == 0u) {
+                                if (ld_shared_u32(abort_flag)) {
+                                    seen = 0u;
+                                    break;
+                                }
                                 if (globaltimer_ns() - t0 > p.timeout_ns) {
                                     ctl.fail(WHERE_FIXUP);
+                                    seen = 0u;
                                     break;
                                 }
                             }
                         }
                     }
-                    __syncwarp();
+                    seen = __shfl_sync(0xffffffffu, seen, 0);
+                    // every lane acquires the raised flags itself before reading the partials
                     for (int sl = 0; sl < nparts - 1; ++sl) (void)ld_acquire_gpu(sync + 1 + sl);
+                    __syncwarp();
+                    // Every other piece has claimed and raised its flag: no one
+                    // else touches these words again in this launch, so they go
+                    // back to zero for the next one (which starts only after
+                    // this grid has completed).
+                    if (lane == 0 && seen) {
+                        for (int sl = 0; sl < nparts - 1; ++sl) sync[1 + sl] = 0u;
+                        sync[0] = 0u;
+                    }
                 }
             }
             const bool write_partial = part >= 0 && part < nparts - 1;
@@ -853,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // publish this part: every lane's stores, then the flag (release)
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(sync + 1 + part, p.epoch);
+                if (lane == 0) st_release_gpu(sync + 1 + part, 1u);
             }
             if (rec != nullptr && leader) rec->t_stored = static_cast<uint32_t>(globaltimer_ns());
             if (++acc == 2) {

@@ -37,8 +37,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
-    bool ready = false;
-    gemm_status_t error = GEMM_OK;     // set-up failure, returned by every later call
+    bool ready = false;                // set only once the whole set-up has succeeded
     unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int max_smem = 0;
     int stages[2] = {0, 0};
@@ -51,54 +50,56 @@ std::mutex g_setup_mutex;
 DeviceSetup g_setup[kMaxDevices];
 
 // Once per device, with that device current: scratch address, kernel
-// attributes, resident-cluster counts and the tensor-map encoder.
-const DeviceSetup *setup_device(int dev)
+// attributes, resident-cluster counts and the tensor-map encoder.  A set-up
+// that fails is not remembered: the error goes to this call's caller and the
+// next call on the device tries again from the start.
+gemm_status_t setup_device(int dev, const DeviceSetup **out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     DeviceSetup &s = g_setup[dev];
-    if (s.ready) return &s;
-    s.ready = true;
+    *out = &s;
+    if (s.ready) return GEMM_OK;
+    DeviceSetup n;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess
         || cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess
-        || cudaDeviceGetAttribute(&s.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
-        s.error = GEMM_ERR_CUDA;
-        return &s;
+        || cudaDeviceGetAttribute(&n.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
     }
-    if (major != 10 || minor != 3) {
-        s.error = GEMM_ERR_UNSUPPORTED;
-        return &s;
-    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
     void *addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
-        s.error = GEMM_ERR_CUDA;
-        return &s;
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
     }
-    s.scratch = static_cast<unsigned char *>(addr);
+    n.scratch = static_cast<unsigned char *>(addr);
     cudaDriverEntryPointQueryResult q;
     void *fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess
         || q != cudaDriverEntryPointSuccess || fn == nullptr) {
-        s.error = GEMM_ERR_CUDA;
-        return &s;
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
     }
-    s.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    n.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     for (int cg = 1; cg <= 2; ++cg) {
         int st = pts::kMaxStages;
-        while (st > 2 && pts::smem_bytes(cg, st) > s.max_smem) --st;
-        s.stages[cg - 1] = st;
-        s.smem[cg - 1] = pts::smem_bytes(cg, st);
+        while (st > 2 && pts::smem_bytes(cg, st) > n.max_smem) --st;
+        n.stages[cg - 1] = st;
+        n.smem[cg - 1] = pts::smem_bytes(cg, st);
         for (int kind = 0; kind < 3; ++kind) {
             pts::KernelOps ops = cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind);
-            if (ops.set_smem(s.max_smem) != cudaSuccess
-                || ops.max_active_clusters(s.smem[cg - 1], &s.clusters[kind][cg - 1]) != cudaSuccess
-                || s.clusters[kind][cg - 1] < 1) {
-                s.error = GEMM_ERR_CUDA;
-                return &s;
+            if (ops.set_smem(n.max_smem) != cudaSuccess
+                || ops.max_active_clusters(n.smem[cg - 1], &n.clusters[kind][cg - 1]) != cudaSuccess
+                || n.clusters[kind][cg - 1] < 1) {
+                (void)cudaGetLastError();
+                return GEMM_ERR_CUDA;
             }
         }
     }
-    return &s;
+    n.ready = true;
+    s = n;
+    return GEMM_OK;
 }
 
 bool encode_2d(const DeviceSetup *s, CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols,
@@ -155,8 +156,9 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     const int64_t tiles = tiles_m * tiles_n;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(cudaErrorInvalidDevice);
-    const DeviceSetup *s = setup_device(dev);
-    if (s->error != GEMM_OK) return s->error;
+    const DeviceSetup *s = nullptr;
+    const gemm_status_t setup = setup_device(dev, &s);
+    if (setup != GEMM_OK) return setup;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int ci = cta_group - 1;
     const int64_t resident = s->clusters[dtype][ci];
@@ -190,7 +192,6 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.split = split;
     p.sk_tiles = 0;   // no stream-K share: its fixup workspace would not fit a modest static array
     p.sk_units = 0;
-    p.epoch = 1;
     p.ws_partial = nullptr;
     p.ws_sync = nullptr;
     p.num_units = static_cast<int32_t>(work);

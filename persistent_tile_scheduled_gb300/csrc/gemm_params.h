@@ -63,7 +63,6 @@ struct GemmParams {
     int32_t split;              // column slices per tile (1, 2 or 4); 1 when sk_units > 0
     int32_t sk_tiles;           // tiles of the stream-K region (the first in grouped order); 0 = none
     int32_t sk_units;           // units sharing the region's k-blocks (0 = none)
-    uint32_t epoch;             // launch number (29 bits, never 0) tagging the fixup counters and flags
     int32_t num_units;          // work ids the schedulers hand out
     int32_t num_work;           // work items (record slots); see work_tile()
     int32_t group_m;            // GROUP_SIZE_M
@@ -78,7 +77,8 @@ struct GemmParams {
     uint64_t timeout_ns;
     int32_t *status;            // 4 ints
     float *ws_partial;          // stream-K partial accumulators (fixup workspace), or null
-    uint32_t *ws_sync;          // stream-K claim counters and ready flags, 4 words per (tile, CTA, warp)
+    uint32_t *ws_sync;          // stream-K claim counters and ready flags, 4 words per (tile, CTA, warp);
+                                // zero between launches (each launch resets what it used)
     TileRecord *records;        // num_work entries, or null
     // Grouped launch (num_groups > 0): work id w is tile w - group_start[g] of
     // problem g, where group_start[g] <= w < group_start[g + 1], numbered in

@@ -31,10 +31,35 @@ def out_u(dtype: int) -> float:
     return og.OUT_UNIT_ROUNDOFF[og.F16 if dtype == wl.F16 else og.BF16]
 
 
-def compare_full(x: wl.Inputs, C: torch.Tensor):
+# Error distribution of every parity comparison of the session (reported at
+# the end of the run; written as JSON to $PTS_PARITY_REPORT when that is set).
+PARITY_LOG = []
+
+
+def record_parity(what: str, p, got, ref, ref_abs):
+    """Log one comparison: the plain metric (no output-rounding allowance),
+    the one the tests bound (with it), and percentiles of the per-element
+    normalised error |C - C_ref| / (s * sum_k |a||b|)."""
+    got = np.asarray(got, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    ref_abs = np.asarray(ref_abs, np.float64).ravel()
+    nz = ref_abs != 0
+    e = np.abs(got[nz] - ref[nz]) / ref_abs[nz] if nz.any() else np.zeros(1)
+    PARITY_LOG.append({
+        "what": what, "dtype": wl.DTYPE_NAMES[p.dtype], "M": p.M, "N": p.N, "K": p.K, "elements": int(got.size),
+        "plain_max": og.rel_err(got, ref, ref_abs, 0.0),
+        "bounded_max": og.rel_err(got, ref, ref_abs, out_u(p.dtype)),
+        "p50": float(np.percentile(e, 50)), "p99": float(np.percentile(e, 99)),
+        "p999": float(np.percentile(e, 99.9)),
+    })
+
+
+def compare_full(x: wl.Inputs, C: torch.Tensor, what: str = "full"):
     p = x.problem
     ref, ref_abs = og.gemm(p.M, p.N, p.K, x.bits("A"), x.bits("B"), p.dtype, dequant(x))
-    return og.rel_err(C.double().cpu().numpy(), ref, ref_abs, out_u(p.dtype))
+    got = C.double().cpu().numpy()
+    record_parity(what, p, got, ref, ref_abs)
+    return og.rel_err(got, ref, ref_abs, out_u(p.dtype))
 
 
 def sample_positions(M, N, tile_m, tile_n, n_random=4096, seed=0):
@@ -53,11 +78,12 @@ def sample_positions(M, N, tile_m, tile_n, n_random=4096, seed=0):
     return np.concatenate(ii).astype(np.int64), np.concatenate(jj).astype(np.int64)
 
 
-def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, seed=0):
+def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, seed=0, what: str = "sampled"):
     p = x.problem
     ii, jj = sample_positions(p.M, p.N, tile_m, tile_n, seed=seed)
     ref, ref_abs = og.gemm_sampled(p.M, p.N, p.K, x.bits("A"), x.bits("B"), p.dtype, ii, jj, dequant(x))
     got = C.double().cpu().numpy()[ii, jj]
+    record_parity(what, p, got, ref, ref_abs)
     return og.rel_err(got, ref, ref_abs, out_u(p.dtype))
 
 
