@@ -104,6 +104,21 @@ typedef struct gemm_opts {
     int group_order;                /* gemm_run_grouped's order of the problems in the work-id
                                        list: 0 = default (1); 1 = most k-blocks first (stable:
                                        equal K keep the given order); 2 = as given */
+    int tile_n;                     /* output tile columns of gemm_run: 0 = per call (128 for the
+                                       non-persistent scheduler when a tile has <= 4 k-blocks and
+                                       cta_group is 0, else 256);
+                                       256 = the wide tile (one CTA, or CTA pair, per SM);
+                                       128 = the narrow tile: 128 x 128 per CTA, single CTAs,
+                                       two resident per SM (needs cta_group 0 or 1); no stream-K
+                                       share and no column quarters (split 4) with it.
+                                       gemm_run_grouped and gemm_run_noalloc use the wide tile. */
+    int clc_depth;                  /* GEMM_SCHED_CLC: how far ahead of the producer a cluster
+                                       claims work.  1 = the next unit is claimed when the producer
+                                       starts the current one; 2 = one unit earlier (the response
+                                       then has a whole unit to arrive in, but every cluster holds
+                                       one more claimed unit at the end of the grid).  Requests
+                                       stay one at a time either way: the next is issued only after
+                                       the previous one was seen to succeed.  0 = default (1). */
 } gemm_opts_t;
 
 /* Work items.  Output tiles are numbered in grouped order (GROUP_SIZE_M tile-
@@ -167,6 +182,7 @@ typedef struct gemm_launch_info {
     int64_t sk_units;               /* units sharing it (the resident clusters G) */
     int64_t work_items;             /* work items = record slots (gemm_read_debug's n_work) */
     int64_t units;                  /* units the schedulers hand out */
+    int ctas_per_sm;                /* CTAs the kernel keeps resident per SM (1 wide, 2 narrow) */
 } gemm_launch_info_t;
 
 typedef struct gemm_ctx *gemm_handle_t;

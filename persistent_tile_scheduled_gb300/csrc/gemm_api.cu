@@ -68,9 +68,10 @@ struct gemm_ctx {
     cudaEvent_t ev_tab[kGroupSlots] = {};
     int tab_cur = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    bool smem_set[3][2] = {};
-    int occ_smem[3][2] = {};                  // smem the cached occupancy was computed for
-    int occ_clusters[3][2] = {};
+    // per dtype and kernel variant (0: wide tile, single CTAs; 1: wide, pairs; 2: narrow tile)
+    bool smem_set[3][3] = {};
+    int occ_smem[3][3] = {};                  // smem the cached occupancy was computed for
+    int occ_clusters[3][3] = {};
     MapEntry maps[kMapCache];
 };
 
@@ -118,10 +119,17 @@ const CUtensorMap *get_map(gemm_ctx *h, const void *ptr, uint64_t rows, uint64_t
     return &m.map;
 }
 
-pts::KernelOps ops_for(int kind, int cg) { return cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind); }
+// Kernel variant: 0 wide tile, single CTAs; 1 wide tile, CTA pairs; 2 narrow tile.
+int variant_of(int cg, int bn) { return bn == pts::kTileNNarrow ? 2 : cg - 1; }
+
+pts::KernelOps ops_for(int kind, int cg, int bn)
+{
+    if (bn == pts::kTileNNarrow) return pts::kernel_ops_narrow(kind);
+    return cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind);
+}
 
 struct Plan {
-    int cg, stages, smem;
+    int cg, bn = pts::kTileN, stages, smem;
     int64_t tiles_m, tiles_n, tiles;
     int split;               // column slices per tile (1, 2 or 4)
     int64_t sk_tiles;        // stream-K region: its tiles and units (0 = none)
@@ -131,6 +139,7 @@ struct Plan {
     int64_t work;            // work items (record slots)
     int64_t grid_ctas;
     int max_active_clusters;
+    int ctas_per_sm;
 };
 
 
@@ -145,20 +154,23 @@ gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, g
     return GEMM_OK;
 }
 
-// Ring depth, shared memory and resident clusters of the kernel for pl.cg.
+// Ring depth, shared memory and resident clusters of the kernel for pl.cg
+// and pl.bn.
 gemm_status_t kernel_shape(gemm_ctx *h, gemm_dtype_t dtype, Plan &pl)
 {
     int stages = h->opts.stages;
-    if (stages == 0) {   // the deepest ring that fits
+    if (stages == 0 && pl.bn == pts::kTileNNarrow) {
+        stages = pts::kNarrowStages;   // the ring that lets two CTAs share an SM
+    } else if (stages == 0) {          // the deepest ring that fits
         stages = pts::kMaxStages;
-        while (stages > 2 && pts::smem_bytes(pl.cg, stages) > h->max_smem_optin) --stages;
+        while (stages > 2 && pts::smem_bytes(pl.cg, stages, pl.bn) > h->max_smem_optin) --stages;
     }
     pl.stages = stages;
-    pl.smem = pts::smem_bytes(pl.cg, stages);
+    pl.smem = pts::smem_bytes(pl.cg, stages, pl.bn);
     if (pl.smem > h->max_smem_optin) return GEMM_ERR_INVALID_ARG;
     const int kind = static_cast<int>(dtype);
-    const int ci = pl.cg - 1;
-    pts::KernelOps ops = ops_for(kind, pl.cg);
+    const int ci = variant_of(pl.cg, pl.bn);
+    pts::KernelOps ops = ops_for(kind, pl.cg, pl.bn);
     if (!h->smem_set[kind][ci]) {
         if (ops.set_smem(h->max_smem_optin) != cudaSuccess) return cuda_fail(cudaErrorInvalidValue);
         h->smem_set[kind][ci] = true;
@@ -171,6 +183,7 @@ gemm_status_t kernel_shape(gemm_ctx *h, gemm_dtype_t dtype, Plan &pl)
     }
     pl.max_active_clusters = h->occ_clusters[kind][ci];
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
+    pl.ctas_per_sm = static_cast<int>((int64_t(pl.max_active_clusters) * pl.cg + h->sm_count - 1) / h->sm_count);
     return GEMM_OK;
 }
 
@@ -186,20 +199,31 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
 {
     const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
     pl.num_kb = (K + kelems - 1) / kelems;
-    pl.cg = h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb);
+    // tile width: the narrow tile (two CTAs per SM) for short tiles when the
+    // caller leaves the shape to the library and forces nothing it lacks
+    // (the stream-K share, column quarters)
+    const bool forced_wide_only = h->opts.split_k == 1 || h->opts.split == 4;
+    pl.bn = h->opts.tile_n != 0 ? h->opts.tile_n
+                                : (forced_wide_only ? pts::kTileN
+                                                    : pts::choose_tile_n(pl.num_kb, h->opts.cta_group, int(sched)));
+    pl.cg = pl.bn == pts::kTileNNarrow ? 1
+                                        : (h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb));
     const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
     pl.tiles_m = (M + tile_m - 1) / tile_m;
-    pl.tiles_n = (N + pts::kTileN - 1) / pts::kTileN;
+    pl.tiles_n = (N + pl.bn - 1) / pl.bn;
     pl.tiles = pl.tiles_m * pl.tiles_n;
     if (pl.tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = kernel_shape(h, dtype, pl);
     if (st != GEMM_OK) return st;
     int64_t resident = resident_clusters(h, pl);
-    // column slices for a problem smaller than one wave (or forced, for testing)
+    // column slices for a problem smaller than one wave (or forced, for
+    // testing); the narrow tile is cut in halves at most (64-column slices)
     pl.split = h->opts.split > 0 ? h->opts.split : pts::choose_split(pl.tiles, resident);
+    if (pl.bn == pts::kTileNNarrow && pl.split > 2) pl.split = 2;
     pl.sk_tiles = 0;
     pl.sk_units = 0;
-    if (pl.split == 1 && (pl.sk_tiles = pts::choose_stream_k(pl.tiles, resident, pl.num_kb, h->opts.split_k)) > 0)
+    if (pl.bn == pts::kTileN && pl.split == 1
+        && (pl.sk_tiles = pts::choose_stream_k(pl.tiles, resident, pl.num_kb, h->opts.split_k)) > 0)
         pl.sk_units = resident;
     pl.units = pl.sk_units > 0 ? pl.sk_units + pl.tiles - pl.sk_tiles : pl.tiles * pl.split;
     pl.work = pl.sk_units > 0 ? pts::kSkMaxPieces * pl.sk_units + pl.tiles - pl.sk_tiles : pl.units;
@@ -275,7 +299,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     // Each map is copied out of the cache at once: a later lookup in this same
     // call may reuse the cache slot an earlier map came from.
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
-    const uint32_t brows = uint32_t(pts::kTileN / pl.cg);
+    const uint32_t brows = uint32_t(pl.bn / pl.cg);
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
     const bool slices = pl.split > 1;
     CUtensorMap ma, mb0, mb_slice, mc;
@@ -316,6 +340,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.stages = pl.stages;
     p.prefetch_kb = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
     p.epi_direct = h->opts.epilogue == 2 ? 1 : 0;
+    p.clc_lead = h->opts.clc_depth;
     p.c_ptr = C;
     p.out_scale = out_scale;
     p.debug_flags = h->opts.debug_flags;
@@ -329,8 +354,9 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     h->last_sk_units = pl.sk_units;
     h->last_num_kb = pl.num_kb;
 
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg).launch(ma, mb, mc, p, static_cast<int>(pl.grid_ctas),
-                                                                   pl.smem, stream, h->opts.overlap_launch >= 0);
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn)
+                        .launch(ma, mb, mc, p, static_cast<int>(pl.grid_ctas), pl.smem, stream,
+                                h->opts.overlap_launch >= 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return cuda_fail(cudaGetLastError());
 }
@@ -515,6 +541,7 @@ gemm_status_t launch_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t
     p.sched = static_cast<int32_t>(sched);
     p.stages = pl.stages;
     p.prefetch_kb = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
+    p.clc_lead = h->opts.clc_depth;
     p.out_scale = 1.0f;
     p.debug_flags = h->opts.debug_flags;
     p.fault_arg = h->opts.fault_arg;
@@ -535,7 +562,7 @@ gemm_status_t launch_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t
     const CUtensorMap *mb[3] = {&none, &none, &none};
     // A launch right after an upload does not overlap the previous grid: the
     // copy sits between them in the stream.
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg)
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn)
                         .launch(none, mb, none, p, static_cast<int>(pl.grid_ctas), pl.smem, stream,
                                 h->opts.overlap_launch >= 0 && !uploaded);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -595,6 +622,11 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.group_order < 0 || o.group_order > 2) return GEMM_ERR_INVALID_ARG;
     if (o.split < 0 || o.split > 4 || o.split == 3 || o.split_k < -1 || o.split_k > 1
         || (o.split > 1 && o.split_k == 1))
+        return GEMM_ERR_INVALID_ARG;
+    if (o.tile_n != 0 && o.tile_n != pts::kTileN && o.tile_n != pts::kTileNNarrow) return GEMM_ERR_INVALID_ARG;
+    if (o.clc_depth < 0 || o.clc_depth > 2) return GEMM_ERR_INVALID_ARG;
+    if (o.clc_depth == 0) o.clc_depth = pts::kDefaultClcLead;
+    if (o.tile_n == pts::kTileNNarrow && (o.cta_group == 2 || o.split == 4 || o.split_k == 1))
         return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
         return GEMM_ERR_INVALID_ARG;
@@ -793,10 +825,11 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     if (st != GEMM_OK) return st;
     std::memset(info, 0, sizeof(*info));
     info->tile_m = pts::kRowsPerCta * pl.cg;
-    info->tile_n = pts::kTileN;
+    info->tile_n = pl.bn;
     info->tile_k = dtype == GEMM_E4M3 ? 128 : 64;
     info->cta_group = pl.cg;
     info->stages = pl.stages;
+    info->ctas_per_sm = pl.ctas_per_sm;
     info->tiles_m = pl.tiles_m;
     info->tiles_n = pl.tiles_n;
     info->tiles = pl.tiles;
@@ -838,6 +871,7 @@ gemm_status_t gemm_query_grouped(gemm_handle_t h, const gemm_group_problem_t *pr
     info->tiles = pl.tiles;
     info->grid_ctas = pl.tiles == 0 ? 0 : pl.grid_ctas;
     info->max_active_clusters = pl.max_active_clusters;
+    info->ctas_per_sm = pl.ctas_per_sm;
     info->smem_bytes = pl.smem;
     info->threads = pts::kThreads;
     info->split = 1;

@@ -52,7 +52,7 @@ enum : int32_t {
     WHERE_CLC = 7,          // scheduler waiting for a CLC response
     WHERE_BAD_TILE = 8,     // a CLC response named a cluster outside the grid
     WHERE_FIXUP = 9,        // the second piece of a cut tile waiting for the first's partial
-    WHERE_STARTED = 10,     // scheduler waiting for the producer to start the item it published
+    WHERE_STARTED = 10,     // CLC scheduler waiting for the producer to start an item it published
 };
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
@@ -154,12 +154,13 @@ __device__ __forceinline__ int group_of(int w, const GemmParams &p)
 //  - Otherwise the whole tile s.
 // Tiles are numbered in grouped order (tile_of).  (A grouped launch's items
 // are decoded by the scheduler warp, which caches its problem table.)
+template <int BN>
 __device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
 {
     WorkTile t;
     int tile = s;
     t.n_off = 0;
-    t.n_len = kTileN;
+    t.n_len = BN;
     t.kb_begin = 0;
     t.kb_end = p.num_kb;
     t.ks = -1;
@@ -183,7 +184,7 @@ __device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
     } else if (p.split > 1) {
         tile = s / p.split;
         const int h = s - tile * p.split;
-        t.n_len = kTileN / p.split;
+        t.n_len = BN / p.split;
         t.n_off = h * t.n_len;
     }
     tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
@@ -277,6 +278,33 @@ struct WaitCtl {
         return all;
     }
 
+    // Wait until the shared word at `addr` holds at least `target` (a count
+    // another warp of this CTA raises), bounded like wait(); every lane of a
+    // converged warp polls and all get one answer.
+    __device__ bool wait_count_all(uint32_t addr, int target, int32_t where) const
+    {
+        bool mine = static_cast<int>(ld_shared_u32(addr)) >= target;
+        if (!mine) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t n = 1;; ++n) {
+                if (static_cast<int>(ld_shared_u32(addr)) >= target) {
+                    mine = true;
+                    break;
+                }
+                if ((n & 15u) == 0) {
+                    if (ld_shared_u32(abort_addr)) break;
+                    if (globaltimer_ns() - t0 > timeout_ns) {
+                        fail(where);
+                        break;
+                    }
+                }
+            }
+        }
+        const bool all = __all_sync(0xffffffffu, mine);
+        if (!all && mine && lane_id() == 0 && !ld_shared_u32(abort_addr)) fail(where);
+        return all;
+    }
+
     // Bounded wait used only while shutting down after an error: ignores the
     // abort flag, gives up silently after `limit_ns`.
     __device__ bool drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
@@ -305,18 +333,24 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits, fl
     }
 }
 
-template <int KIND, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KIND, int CG, int BN = kTileN>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB4,
                 const __grid_constant__ CUtensorMap tmC, const GemmParams p)
 {
-    // tmB / tmB2 / tmB4: B boxes of 256/CG, 128/CG and 64/CG rows, for whole
+    // BN: tile columns, 256 (the wide tile, one CTA per SM) or 128 (the
+    // narrow tile, single CTAs, two per SM; no stream-K share and no column
+    // quarters, so its epilogue holds fewer registers).
+    // tmB / tmB2 / tmB4: B boxes of BN/CG, BN/CG/2 and BN/CG/4 rows, for whole
     // tiles and for the column slices (halves, quarters) of a problem smaller
     // than one wave
+    static_assert(BN == kTileN || (BN == kTileNNarrow && CG == 1), "tile shape");
+    constexpr bool kStreamK = BN == kTileN;   // the stream-K fixup is built for the wide tile only
+    constexpr uint32_t kAccCols = 2 * BN;     // TMEM columns: two accumulators
     constexpr int KBS = kb_per_stage(CG);   // k-blocks per ring stage
     constexpr int SA = stage_bytes_a(CG);
-    constexpr int SB = stage_bytes_b(CG);
+    constexpr int SB = stage_bytes_b(CG, BN);
     constexpr int KELEMS = (KIND == 2) ? kKBlockBytes : kKBlockBytes / 2;   // K elements per k-block
 
     extern __shared__ uint8_t smem_raw[];
@@ -334,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_full0 = acc_empty0 + 16;             // + 8*r
     const uint32_t ring_empty0 = ring_full0 + 8 * kRing;     // + 8*r
     const uint32_t clc_bar = ring_empty0 + 8 * kRing;
-    const uint32_t started_bar = clc_bar + 8;                // producer (leader) starts an item
-    const uint32_t clc_resp = (started_bar + 8 + 15) & ~15u;
+    const uint32_t started_cnt = clc_bar + 8;                // items the (leader's) producer has started
+    const uint32_t clc_resp = (started_cnt + 8 + 15) & ~15u;
     const uint32_t ring0 = clc_resp + 16;                    // + 4*kRingWords*r: a decoded work item
     const uint32_t tmem_slot = ring0 + 4 * kRingWords * kRing;
     const uint32_t abort_flag = tmem_slot + 4;
@@ -369,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(ring_empty0 + 8 * r, CG == 1 ? 2 + kEpiWarps : 3 + 2 * kEpiWarps);
         }
         mbar_init(clc_bar, 1);
-        mbar_init(started_bar, 1);
+        st_shared_u32(started_cnt, 0u);
         st_shared_u32(abort_flag, 0u);
         fence_mbar_init();
     }
@@ -382,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc<CG>(tmem_slot, kTmemCols);
+        tmem_alloc<CG>(tmem_slot, kAccCols);
         tmem_relinquish<CG>();
     }
     tc_fence_before();
@@ -396,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // map of the item's column width (a grouped launch: its problem's maps).
     auto boxes = [&](const WorkTile &t, int &ya, int &yb, const CUtensorMap *&ma) -> const CUtensorMap * {
         ya = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta;
-        yb = t.tn * kTileN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
+        yb = t.tn * BN + t.n_off + static_cast<int>(rank) * (t.n_len / CG);
         if (grouped) {
             ma = &p.groups[t.g].tmA;
             return &p.groups[t.g].tmB;
         }
         ma = &tmA;
-        return t.n_len == kTileN ? &tmB : (t.n_len == kTileN / 2 ? &tmB2 : &tmB4);
+        return t.n_len == BN ? &tmB : (t.n_len == BN / 2 ? &tmB2 : &tmB4);
     };
 
     // Back-to-back launches: the set-up above may overlap the end of the
@@ -415,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (Not in a grouped launch, whose problem table is read only after the wait.)
     pdl_launch_dependents();
     if (warp == 0 && cluster_id < p.num_units && !grouped) {
-        const WorkTile t0 = work_tile(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), p);
+        const WorkTile t0 = work_tile<BN>(unit_item(cluster_id, 0, unit_items(cluster_id, p), p), p);
         int ya, yb;
         const CUtensorMap *ma;
         const CUtensorMap *mb = boxes(t0, ya, yb, ma);
@@ -552,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (w < 0) break;
-            if (leader) mbar_arrive_if(one, started_bar);
+            if (leader && lane == 0) st_shared_u32(started_cnt, static_cast<uint32_t>(i + 1));
             if (!load_tile(t, t.kb_begin, t.kb_end)) {
                 ok = false;
                 break;
@@ -602,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.records != nullptr && lane == 0)
                     p.records[w].t_mma_start = static_cast<uint32_t>(globaltimer_ns());
                 const uint32_t idesc = make_idesc<KIND, CG>(static_cast<uint32_t>(t.n_len));
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTileN);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
                 bool ok = true;
                 for (int kb = t.kb_begin; kb < t.kb_end; kb += KBS) {
                     if (!ctl.wait_all(full0 + 8 * stage, phase, WHERE_FULL)) {
@@ -708,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int row0 = t.tm * (kRowsPerCta * CG) + static_cast<int>(rank) * kRowsPerCta
                              + static_cast<int>(q) * kEpiRowsPerWarp;
-            const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * kTileN);
+            const uint32_t tbase = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN);
             const int chunks = t.n_len / kEpiChunkCols;
 
             // A stream-K piece of a cut tile: claim a part number for this
@@ -721,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int part = -1;
             uint32_t *sync = nullptr;
             const float4 *partials = nullptr;
-            if (t.ks >= 0) {
+            if (kStreamK && t.ks >= 0) {
                 const long long unit = (static_cast<long long>(t.ks) * CG + rank) * kEpiWarps + q;
                 sync = p.ws_sync + unit * 4;
                 partials = reinterpret_cast<const float4 *>(p.ws_partial)
@@ -773,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < 16; ++g) pa[g] = __ldcg(src + g * 32);
             }
 #pragma unroll
-            for (int c = 0; c < kTileN / kEpiChunkCols; ++c) {
+            for (int c = 0; c < BN / kEpiChunkCols; ++c) {
                 if (c >= chunks) break;
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(tbase + c * kEpiChunkCols, v0);
@@ -829,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[j] = pack2<KIND>(v0[2 * j], v0[2 * j + 1], oscale);
                     pk[16 + j] = pack2<KIND>(v1[2 * j], v1[2 * j + 1], oscale);
                 }
-                const int col = t.tn * kTileN + t.n_off + c * kEpiChunkCols;
+                const int col = t.tn * BN + t.n_off + c * kEpiChunkCols;
                 if (p.epi_direct) {
                     // this lane's row: 64 outputs = 8 x 16 bytes, straight to global
                     const int row = row0 + static_cast<int>(lane);
@@ -961,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // of the next one) costs no search and no table read.
             int gc = -1, gc_lo = 0, gc_hi = 0, gc_tm = 0, gc_tn = 0, gc_kb = 0;
             auto item_of = [&](int w) -> WorkTile {
-                if (!grouped) return work_tile(w, p);
+                if (!grouped) return work_tile<BN>(w, p);
                 if (w < gc_lo || w >= gc_hi) {
                     int g;
                     if (gc >= 0 && w >= gc_hi && gc + 1 < p.num_groups && w < __ldg(p.group_start + gc + 2))
@@ -979,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 WorkTile t;
                 t.g = gc;
                 t.n_off = 0;
-                t.n_len = kTileN;
+                t.n_len = BN;
                 t.kb_begin = 0;
                 t.kb_end = gc_kb;
                 t.ks = -1;
@@ -987,10 +1021,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t.idx = t.tm * gc_tn + t.tn;
                 return t;
             };
-            // Only CLC waits for the producer before going on: its next claim
-            // must not come earlier than one item ahead.  Static units are
+            // Only CLC waits for the producer before going on: it claims a unit
+            // when the producer starts the unit `lead` - 1 units earlier, so
+            // the producer finds the next `lead` - 1 units decoded in the ring
+            // (lead 1: the claim is made as the producer starts the unit
+            // before it; lead 2: one unit earlier, which hides a CLC response
+            // behind a whole unit even when units are short, but leaves each
+            // cluster holding one more claimed unit when the grid runs out).
+            // Claims stay one at a time: a request is issued only after the
+            // previous one's response was seen to succeed.  Static units are
             // fixed, so that scheduler runs as far ahead as the ring allows.
-            const bool pace = p.sched == SCHED_CLC;
+            const int lead = p.sched == SCHED_CLC ? p.clc_lead : 0;
             int u = cluster_id < p.num_units ? cluster_id : -1;
             int i = 0;   // ring slot sequence = work items published
             for (int n = 0; ok && u >= 0; ++n) {
@@ -998,10 +1039,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; ok && j < pieces; ++j) {
                     const int w = unit_item(u, j, pieces, p);
                     ok = publish(i, w, item_of(w))
-                         && (!pace || ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED));
+                         && (lead == 0 || ctl.wait_count_all(started_cnt, i + 2 - lead, WHERE_STARTED));
                     ++i;
                     if (ok && j == 0 && may_request) {
-                        // the producer has begun this unit: claim the one after it
+                        // the producer has begun the item `lead` - 1 before this one: claim the next unit
                         if ((p.debug_flags & DBG_CLC_STOP_AT) && n == p.fault_arg) {
                             may_request = false;   // behave as if this request had failed
                         } else {
@@ -1035,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CG == 2) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<CG>(tmem_base, kTmemCols);
+        tmem_dealloc<CG>(tmem_base, kAccCols);
     }
 }
 

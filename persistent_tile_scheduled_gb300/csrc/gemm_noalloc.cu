@@ -201,6 +201,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.stages = s->stages[ci];
     p.prefetch_kb = pts::kDefaultPrefetchKb;
     p.epi_direct = 0;
+    p.clc_lead = pts::kDefaultClcLead;
     p.c_ptr = C;
     p.out_scale = out_scale;
     p.debug_flags = pts::DBG_RECORDS;

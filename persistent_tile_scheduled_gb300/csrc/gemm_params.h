@@ -8,10 +8,13 @@
 namespace pts {
 
 // One CTA owns 128 rows of the output tile and its TMEM accumulator holds
-// 128 lanes x 256 fp32 columns.  A k-block is 128 bytes of K per row (64
-// fp16/bf16 or 128 e4m3 elements): one 128-byte swizzle atom row.
+// 128 lanes x 256 fp32 columns (the wide tile, one CTA per SM) or 128 lanes x
+// 128 columns (the narrow tile, whose smaller ring and accumulators let two
+// CTAs share an SM).  A k-block is 128 bytes of K per row (64 fp16/bf16 or
+// 128 e4m3 elements): one 128-byte swizzle atom row.
 constexpr int kRowsPerCta = 128;
-constexpr int kTileN = 256;
+constexpr int kTileN = 256;             // columns of the wide tile
+constexpr int kTileNNarrow = 128;       // columns of the narrow tile (single CTAs, two per SM)
 constexpr int kKBlockBytes = 128;
 constexpr int kThreads = 224;           // warp 0 producer, warp 1 MMA, warps 2-5 epilogue, warp 6 scheduler
 constexpr int kEpiWarps = 4;
@@ -22,8 +25,9 @@ constexpr int kEpiBufBytes = kEpiRowsPerWarp * kEpiChunkCols * 2;   // 4 KB
 constexpr int kEpiBufsPerWarp = 2;
 constexpr int kRing = 4;                // depth of the work-item broadcast ring
 constexpr int kRingWords = 12;          // 32-bit words per ring slot (a decoded work item)
-constexpr int kTmemCols = 512;          // two 256-column accumulators
+constexpr int kTmemCols = 512;          // two 256-column accumulators (the narrow tile: 2 x 128)
 constexpr int kMaxStages = 8;
+constexpr int kDefaultClcLead = 1;      // CLC claim depth when the caller leaves it to the library
 constexpr int kDefaultPrefetchKb = 0;   // L2 prefetch of the operand loads: off (it costs more L2
                                         // traffic than it saves in miss latency on GB300)
 
@@ -70,6 +74,7 @@ struct GemmParams {
     int32_t stages;
     int32_t prefetch_kb;        // L2 prefetch distance ahead of the operand loads, in k-blocks (0 = none)
     int32_t epi_direct;         // 1: the epilogue stores C rows straight from registers (no TMA store)
+    int32_t clc_lead;           // CLC: units claimed ahead of the producer (1 or 2)
     void *c_ptr;                // C (for the direct-store epilogue)
     float out_scale;            // 1, or 1/(scale_a*scale_b) for e4m3
     uint32_t debug_flags;
@@ -167,6 +172,44 @@ inline int choose_split(int64_t tiles, int64_t resident)
     return 1;
 }
 
+// CTAs per SM: the wide tile's ring and staging take nearly all of an SM's
+// shared memory; the narrow tile's fit twice (two stages of 32 KB, 32 KB of
+// epilogue staging, about 97 KB per CTA), and its accumulators take 256 of
+// the SM's 512 TMEM columns.  A second resident CTA gives the SM a second,
+// independent load -> MMA -> epilogue pipeline: while one CTA waits for its
+// operands or drains its output, the other computes.  That pays where tiles
+// are short (few k-blocks) and the per-tile latencies dominate; for long
+// tiles the narrow tile's two-stage ring and its 4/3 times higher operand
+// traffic per flop lose to the wide tile.  ("[Persistent] Performance on
+// 09-persistent-matmul on A100 worse than non-persistent": the best
+// persistent configuration there was 128x128x64 tiles with twice as many
+// programs as SMs.)
+//
+// Measured on GB300 (fp16 4096^2, 40 chained launches per point, microseconds
+// per launch; wide = 128 x 256 single CTAs, narrow = 128 x 128, two per SM):
+//   K     static wide / narrow   CLC wide / narrow   non-persistent wide / narrow
+//   128   11.8 / 11.8            12.9 / 11.8         23.5 / 20.8
+//   256   13.1 / 16.8            13.6 / 16.6         26.2 / 25.3
+//   512   19.5 / 24.2            19.4 / 24.1         31.5 / 32.7
+//   1024  29.6 / 38.9            29.7 / 39.0         41.9 / 47.0
+// The persistent grids gain nothing: at small K a launch is bound by the
+// latency of its operand loads, and the SM's operands in flight are what
+// sets the pace -- four 48 KB stages for the wide tile, 2 x 2 stages of 32 KB
+// for the narrow pair -- so the narrow tile ties at 2 k-blocks and loses
+// beyond.  The non-persistent grid, which starts a CTA per tile, gains from
+// two CTAs per SM up to 4 k-blocks.
+__host__ __device__ constexpr int ctas_per_sm(int bn) { return bn == kTileN ? 1 : 2; }
+constexpr int kNarrowStages = 2;
+// Narrow tiles when the caller leaves both the tile and the CTA group to the
+// library: for the non-persistent grid (sched 0) on tiles of at most this
+// many k-blocks.
+constexpr int kNarrowMaxKb = 4;
+
+inline int choose_tile_n(int64_t num_kb, int cta_group_opt, int sched)
+{
+    return (cta_group_opt == 0 && sched == SCHED_NONPERSISTENT && num_kb <= kNarrowMaxKb) ? kTileNNarrow : kTileN;
+}
+
 // K-blocks per ring stage.  A stage's fixed costs (its barrier waits, the
 // expect-tx arrival, the commit that frees it) are paid once per stage, so a
 // CTA pair, whose 32 KB k-blocks leave room for 3 stages of 2, takes 2 per
@@ -176,14 +219,17 @@ inline int choose_split(int64_t tiles, int64_t resident)
 // (K = 768: 26.6 vs 24.8 us).
 __host__ __device__ constexpr int kb_per_stage(int cg) { return cg == 2 ? 2 : 1; }
 __host__ __device__ constexpr int stage_bytes_a(int cg) { return kRowsPerCta * kKBlockBytes * kb_per_stage(cg); }
-__host__ __device__ constexpr int stage_bytes_b(int cg) { return (kTileN / cg) * kKBlockBytes * kb_per_stage(cg); }
+__host__ __device__ constexpr int stage_bytes_b(int cg, int bn = kTileN)
+{
+    return (bn / cg) * kKBlockBytes * kb_per_stage(cg);
+}
 __host__ __device__ constexpr int epi_bytes() { return kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes; }
 
-// Dynamic shared memory needed for `stages` stages (plus 1 KB for aligning
-// the base to the 1024-byte swizzle period).
-__host__ __device__ constexpr int smem_bytes(int cg, int stages)
+// Dynamic shared memory needed for `stages` stages of a tile `bn` columns
+// wide (plus 1 KB for aligning the base to the 1024-byte swizzle period).
+__host__ __device__ constexpr int smem_bytes(int cg, int stages, int bn = kTileN)
 {
-    return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg)) + epi_bytes()
+    return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg, bn)) + epi_bytes()
            + 8 * (2 * kMaxStages + 4 + 2 * kRing + 2)    // mbarriers
            + 16                                          // CLC response
            + 4 * kRingWords * kRing + 16;                // ring payload, TMEM base, abort flag

@@ -33,7 +33,7 @@ class gemm_opts_t(ctypes.Structure):
                 ("max_clusters", ctypes.c_int), ("debug_flags", ctypes.c_uint), ("fault_arg", ctypes.c_int),
                 ("timeout_ns", ctypes.c_ulonglong), ("split", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("prefetch", ctypes.c_int), ("overlap_launch", ctypes.c_int), ("epilogue", ctypes.c_int),
-                ("group_order", ctypes.c_int)]
+                ("group_order", ctypes.c_int), ("tile_n", ctypes.c_int), ("clc_depth", ctypes.c_int)]
 
 
 class gemm_tile_record_t(ctypes.Structure):
@@ -50,7 +50,8 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("tiles_n", ctypes.c_int64), ("tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64),
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
                 ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("sk_tiles", ctypes.c_int64),
-                ("sk_units", ctypes.c_int64), ("work_items", ctypes.c_int64), ("units", ctypes.c_int64)]
+                ("sk_units", ctypes.c_int64), ("work_items", ctypes.c_int64), ("units", ctypes.c_int64),
+                ("ctas_per_sm", ctypes.c_int)]
 
 
 class gemm_host_problem_t(ctypes.Structure):
@@ -149,9 +150,9 @@ def gemm_status_string(status: int) -> str:
 
 def make_opts(cta_group=0, group_size_m=8, stages=0, max_clusters=0, debug_flags=0, fault_arg=0,
               timeout_ns=0, split=0, split_k=0, prefetch=0, overlap_launch=0, epilogue=0,
-              group_order=0) -> gemm_opts_t:
+              group_order=0, tile_n=0, clc_depth=0) -> gemm_opts_t:
     return gemm_opts_t(cta_group, group_size_m, stages, max_clusters, debug_flags, fault_arg, timeout_ns, split,
-                       split_k, prefetch, overlap_launch, epilogue, group_order)
+                       split_k, prefetch, overlap_launch, epilogue, group_order, tile_n, clc_depth)
 
 
 def gemm_create(device: int = 0, opts: Optional[gemm_opts_t] = None) -> int:

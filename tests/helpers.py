@@ -90,10 +90,11 @@ def compare_sampled(x: wl.Inputs, C: torch.Tensor, tile_m: int, tile_n: int, see
 def check_records(records, info, sched: int, K: int, group_m: int = 8):
     """Per-work-item records against what the schedulers must do (bit-exact)."""
     T, Tm, Tn, cg = int(info.tiles), int(info.tiles_m), int(info.tiles_n), int(info.cta_group)
-    W, split = int(info.work_items), int(info.split)
+    W, split, BN = int(info.work_items), int(info.split), int(info.tile_n)
     G = int(info.grid_ctas) // cg
     num_kb = -(-int(K) // int(info.tile_k))
-    units = osched.work_units(T, split, num_kb=num_kb, sk_tiles=int(info.sk_tiles), sk_units=int(info.sk_units))
+    units = osched.work_units(T, split, tile_n=BN, num_kb=num_kb, sk_tiles=int(info.sk_tiles),
+                              sk_units=int(info.sk_units))
     assert len(units) == int(info.units)
     assert W == osched.record_slots(T, split, int(info.sk_tiles), int(info.sk_units))
     items = [it for u in units for it in u]
@@ -114,7 +115,7 @@ def check_records(records, info, sched: int, K: int, group_m: int = 8):
         cover[r.tile] |= cells
     # the items partition every tile (columns x k-blocks) exactly once
     assert sorted(cover) == list(range(T))
-    full = {(c, kb) for c in range(0, 256, 64) for kb in range(num_kb)}
+    full = {(c, kb) for c in range(0, BN, 64) for kb in range(num_kb)}
     assert all(cells == full for cells in cover.values())
     by_work = {it[0]: (records[it[0]].owner, records[it[0]].iter) for it in items}
     if sched == pts.GEMM_SCHED_STATIC:

@@ -85,8 +85,9 @@ def test_struct_layouts_match_the_header():
              offsetof(gemm_group_problem_t, scale_a), (size_t)GEMM_GROUPED_MAX_PROBLEMS);
       printf("%zu %zu %zu %zu\n", sizeof(gemm_launch_info_t), offsetof(gemm_launch_info_t, tiles_m),
              offsetof(gemm_launch_info_t, grid_ctas), offsetof(gemm_launch_info_t, threads));
-      printf("%zu %zu %zu\n", offsetof(gemm_launch_info_t, sk_tiles), offsetof(gemm_launch_info_t, work_items),
-             offsetof(gemm_launch_info_t, units));
+      printf("%zu %zu %zu %zu\n", offsetof(gemm_launch_info_t, sk_tiles), offsetof(gemm_launch_info_t, work_items),
+             offsetof(gemm_launch_info_t, units), offsetof(gemm_launch_info_t, ctas_per_sm));
+      printf("%zu %zu\n", offsetof(gemm_opts_t, tile_n), offsetof(gemm_opts_t, clc_depth));
       return 0;
     }
     """
@@ -105,7 +106,8 @@ def test_struct_layouts_match_the_header():
             ctypes.sizeof(g.gemm_launch_info_t), g.gemm_launch_info_t.tiles_m.offset,
             g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset,
             g.gemm_launch_info_t.sk_tiles.offset, g.gemm_launch_info_t.work_items.offset,
-            g.gemm_launch_info_t.units.offset]
+            g.gemm_launch_info_t.units.offset, g.gemm_launch_info_t.ctas_per_sm.offset,
+            g.gemm_opts_t.tile_n.offset, g.gemm_opts_t.clc_depth.offset]
     assert got == want
 
 

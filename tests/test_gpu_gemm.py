@@ -21,11 +21,16 @@ pytestmark = pytest.mark.gpu
 SCHEDS = [pts.GEMM_SCHED_NONPERSISTENT, pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC]
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["cg1", "cg2"])
+# the wide tile (128 x 256 per CTA) with single CTAs and with CTA pairs, and
+# the narrow tile (128 x 128 per CTA, two CTAs per SM)
+SHAPES = {"cg1": dict(cta_group=1), "cg2": dict(cta_group=2), "narrow": dict(cta_group=1, tile_n=128)}
+
+
+@pytest.fixture(scope="module", params=list(SHAPES), ids=list(SHAPES))
 def handle(request):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
-    h = pts.gemm_create(0, pts.make_opts(cta_group=request.param, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS, **SHAPES[request.param]))
     yield h, request.param
     pts.gemm_destroy(h)
 
@@ -291,6 +296,81 @@ def test_run_host_batch_matches_device_path(handle):
         assert torch.equal(w.view(torch.int16), q[5].view(torch.int16))
 
 
+# ------------------------------------------------------------- narrow tile
+
+def test_narrow_tile_keeps_two_ctas_per_sm():
+    """The narrow tile's ring, staging and accumulators fit twice per SM: the
+    static grid holds two CTAs per SM (twice as many programs as SMs)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128))
+    try:
+        for dt, K in ((wl.F16, 512), (wl.BF16, 256), (wl.E4M3, 1024)):
+            info = pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_STATIC)
+            assert (info.tile_m, info.tile_n, info.cta_group, info.ctas_per_sm) == (128, 128, 1, 2)
+            assert info.max_active_clusters == 2 * sms
+            assert info.grid_ctas == 2 * sms and info.tiles == 32 * 32 and info.split_k == 0
+            assert info.smem_bytes * 2 <= 228 * 1024
+    finally:
+        pts.gemm_destroy(h)
+
+
+def test_automatic_tile_choice():
+    """With the shape left to the library, the non-persistent grid takes the
+    narrow tile for tiles of at most 4 k-blocks; the persistent grids, and a
+    caller that fixes the CTA group, get the wide tile."""
+    h = pts.gemm_create(0, pts.make_opts())
+    h1 = pts.gemm_create(0, pts.make_opts(cta_group=1))
+    try:
+        for dt, K, narrow in ((wl.F16, 128, True), (wl.F16, 256, True), (wl.F16, 320, False),
+                              (wl.E4M3, 512, True), (wl.E4M3, 640, False), (wl.BF16, 4096, False)):
+            info = pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_NONPERSISTENT)
+            assert info.tile_n == (128 if narrow else 256), (dt, K)
+            for sched in (pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC):
+                assert pts.gemm_query(h, 4096, 4096, K, dt, sched).tile_n == 256
+            assert pts.gemm_query(h1, 4096, 4096, K, dt, pts.GEMM_SCHED_NONPERSISTENT).tile_n == 256
+    finally:
+        pts.gemm_destroy(h)
+        pts.gemm_destroy(h1)
+
+
+def test_narrow_tile_rejects_what_it_lacks():
+    for bad in (dict(tile_n=128, cta_group=2), dict(tile_n=128, split=4), dict(tile_n=128, split_k=1),
+                dict(tile_n=64)):
+        with pytest.raises(pts.GemmError):
+            pts.gemm_create(0, pts.make_opts(**bad))
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_narrow_tile_column_halves(sched):
+    """Sub-wave problems on the narrow tile are cut into 64-column halves."""
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, split=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 96, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("narrow", M, N, K, dt, dist, M + N + K + 2))
+            info = pts.gemm_query(h, M, N, K, dt, sched)
+            assert info.split == 2 and info.tile_n == 128
+            _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
+@pytest.mark.parametrize("K", [128, 256, 512])
+def test_narrow_tile_sweep_points_sampled(K):
+    """The fp16 4096 sweep's small-K end on the narrow tile, two CTAs per SM,
+    every scheduler (the library's plan for the non-persistent grid at K =
+    128 and 256)."""
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
+        for sched in SCHEDS:
+            info = pts.gemm_query(h, 4096, 4096, K, wl.F16, sched)
+            assert info.tile_n == 128 and info.ctas_per_sm == 2
+            _run_checked(h, x, sched, full=False)
+    finally:
+        pts.gemm_destroy(h)
+
+
 # ---------------------------------------------------------------- full sizes
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
@@ -353,6 +433,31 @@ def test_clc_injected_request_failure_keeps_coverage(stop_at):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("shape", list(SHAPES))
+@pytest.mark.parametrize("stop_at", [None, 0, 2])
+def test_clc_claiming_two_units_ahead(shape, stop_at):
+    """clc_depth 2: a cluster claims its next unit one unit earlier than with
+    depth 1 (still one request at a time).  Coverage stays exact, with and
+    without a request that behaves as failed, on ragged and multi-wave
+    problems, stream-K units included."""
+    flags = pts.GEMM_DEBUG_RECORDS | (pts.GEMM_DEBUG_CLC_STOP_AT if stop_at is not None else 0)
+    h = pts.gemm_create(0, pts.make_opts(clc_depth=2, debug_flags=flags, fault_arg=stop_at or 0, **SHAPES[shape]))
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (2048, 2048, 256, wl.F16), (1000, 1800, 2000, wl.BF16),
+                              (640, 1000, 512, wl.E4M3)]:
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("clc2", M, N, K, dt, dist, M + N + K + 5))
+            _run_checked(h, x, pts.GEMM_SCHED_CLC)
+    finally:
+        pts.gemm_destroy(h)
+
+
+def test_clc_depth_option_is_checked():
+    for bad in (-1, 3):
+        with pytest.raises(pts.GemmError):
+            pts.gemm_create(0, pts.make_opts(clc_depth=bad))
+
+
 def test_two_gemms_on_two_streams():
     """Two CLC GEMMs in flight at once on one GPU: both exact in coverage and
     within tolerance (the concurrency case CLC redistributes work for)."""
@@ -380,15 +485,15 @@ def test_two_gemms_on_two_streams():
 
 # ------------------------------------------------------------ bounded waits
 
-@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("shape", list(SHAPES))
 @pytest.mark.parametrize("sched", [pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC])
-def test_wait_time_out_is_reported_and_the_context_survives(cg, sched):
+def test_wait_time_out_is_reported_and_the_context_survives(shape, sched):
     """A stage load that never arrives makes the MMA warp's bounded wait run
     out: the launch reports GEMM_ERR_TIMEOUT (nothing traps, nothing hangs) and
     the next GEMM on the same context is exact."""
     x = wl.custom(512, 512, 1024, wl.BF16, "uniform", 2)
-    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, debug_flags=pts.GEMM_DEBUG_FAULT_SKIP_TMA,
-                                         fault_arg=5, timeout_ns=20_000_000))
+    h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_FAULT_SKIP_TMA, fault_arg=5,
+                                         timeout_ns=20_000_000, **SHAPES[shape]))
     try:
         run_device(h, x, sched)
         st, dev = pts.gemm_check(h)
@@ -398,7 +503,7 @@ def test_wait_time_out_is_reported_and_the_context_survives(cg, sched):
         assert pts.gemm_check(h)[0] == 0              # the status block was cleared
     finally:
         pts.gemm_destroy(h)
-    h = pts.gemm_create(0, pts.make_opts(cta_group=cg))
+    h = pts.gemm_create(0, pts.make_opts(**SHAPES[shape]))
     try:
         C = run_device(h, x, sched)
         assert pts.gemm_check(h)[0] == 0

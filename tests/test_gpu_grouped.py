@@ -241,8 +241,9 @@ def test_grouped_workload_sampled(sched):
         pts.gemm_destroy(h)
 
 
-@pytest.mark.parametrize("sched", SCHEDS)
-def test_grouped_three_thousand_small_problems(sched):
+@pytest.mark.parametrize("sched,clc_depth", [(pts.GEMM_SCHED_NONPERSISTENT, 0), (pts.GEMM_SCHED_STATIC, 0),
+                                             (pts.GEMM_SCHED_CLC, 1), (pts.GEMM_SCHED_CLC, 2)])
+def test_grouped_three_thousand_small_problems(sched, clc_depth):
     """3000 small ragged problems (some empty, some with K = 0) in one launch:
     the problem search takes several rounds and the scheduler's cached
     problem changes at nearly every tile.  Every C against the oracle, the
@@ -259,7 +260,7 @@ def test_grouped_three_thousand_small_problems(sched):
     xs = _inputs(shapes, wl.BF16, 20000)
     dev = _device(xs)
     probs = pts.gemm.group_array(_problems(xs, dev))
-    h = pts.gemm_create(0, pts.make_opts(cta_group=1, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    h = pts.gemm_create(0, pts.make_opts(cta_group=1, clc_depth=clc_depth, debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
         pts.gemm_run_grouped(h, probs, wl.BF16, sched)
         info = pts.gemm_query_grouped(h, probs, wl.BF16, sched)
