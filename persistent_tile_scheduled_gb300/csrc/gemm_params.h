@@ -113,13 +113,15 @@ constexpr int kPartialFloats = kRowsPerCta * kTileN;
 constexpr int kSkMaxPieces = 3;      // record slots per stream-K unit
 constexpr int kSkMaxParts = 2;       // pieces per tile
 // Use it when it saves each cluster at least this many k-blocks' time.  The
-// price, measured on GB300 (fp16 4096^2, CTA pairs): a writer's epilogue
-// takes ~4 us longer than a plain one and a reader's ~4.5 us; hidden behind a
-// long next tile, but not behind a short one.  Break-even is between 15 and
-// 18 k-blocks saved (cold inputs, with vs without: 24 k-blocks per tile, 15
-// saved: 41.6-41.9 vs 41.1 us; 28 per tile, 18 saved: 45.4-45.6 vs
-// 45.8-46.0; 40 per tile, 25 saved: 57.4 vs 59.8-60.5).
-constexpr int kSkMinSavedKb = 16;
+// price, measured on GB300 (fp16 4096^2, CTA pairs, per-item records): a
+// writer piece's epilogue takes 5.5-5.8 us against 1.1-1.5 us for a whole
+// tile (its 128 KB fp32 partial per CTA; staging that partial through shared
+// memory and bulk copies measured slower still, 6.9-7.7 us), a reader's
+// 3.5-4.7 us; hidden behind a long next tile, not behind a short one.
+// Chained launches, without / with the share: K = 1536 (24 k-blocks, 15 saved
+// per cluster) 38.2 / 38.8 us, K = 1792 (28, 18 saved) 42.5 / 43.2, K = 2048
+// (32, 20 saved) 48.7 / 48.1, K = 3072 68.6 / 64.8, K = 4096 91.2 / 84.2.
+constexpr int kSkMinSavedKb = 20;
 
 __host__ __device__ inline int64_t sk_unit_begin(int64_t c, int64_t L, int64_t U) { return c * L / U; }
 
