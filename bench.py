@@ -854,7 +854,7 @@ def config_points(pts, dev, stream):
     return out
 
 
-def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES), dtype="bf16"):
+def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES), dtype="bf16", group_m=8):
     """bf16 (or e4m3) 8192^3 per scheduler and CTA group (the >= 70 % of peak target)."""
     p = wl.bf16_8192_ksweep([8192])[0] if dtype == "bf16" else wl.e4m3_8192()[0]
     x = wl.make_inputs(p)
@@ -863,7 +863,7 @@ def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)
     C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
     out = {}
     for cg in cgs:
-        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg))
+        h = pts.gemm_create(dev, pts.make_opts(cta_group=cg, group_size_m=group_m))
         try:
             for si, name in enumerate(SCHED_NAMES):
                 if name not in scheds:
@@ -884,7 +884,8 @@ def square_8192(pts, dev, stream, reps=10, cgs=(1, 2), scheds=tuple(SCHED_NAMES)
         finally:
             pts.gemm_destroy(h)
     ab_mb = (A.numel() * A.element_size() + B.numel() * B.element_size()) / 1e6
-    out["note"] = f"median of {reps} back-to-back launches; A,B = {ab_mb:.0f} MB (L2 is 129 MB)"
+    out["note"] = (f"median of {reps} back-to-back launches; A,B = {ab_mb:.0f} MB (L2 is 129 MB); "
+                   f"GROUP_SIZE_M {group_m}")
     return out
 
 
@@ -952,6 +953,8 @@ def main():
                     help="only the 8192^3 measurement (for profiling it), restricted by --cta-group, --scheds "
                          "and --square-dtype; prints its numbers, not the benchmark line")
     ap.add_argument("--square-dtype", choices=["bf16", "e4m3"], default="bf16")
+    ap.add_argument("--group-size-m", type=int, default=8,
+                    help="with --square-only: tile-rows per group of the tile order (the library's default is 8)")
     ap.add_argument("--points", action="store_true",
                     help="only one GEMM per configuration point, twice each (for profiling them); prints their "
                          "times, not the benchmark line")
@@ -963,7 +966,7 @@ def main():
         import persistent_tile_scheduled_gb300 as pts
         pts.load(build_if_missing=False)
         out = square_8192(pts, 0, torch.cuda.Stream(), cgs=(args.cta_group,) if args.cta_group else (1, 2),
-                          scheds=tuple(args.scheds), dtype=args.square_dtype)
+                          scheds=tuple(args.scheds), dtype=args.square_dtype, group_m=args.group_size_m)
         print(json.dumps({f"square_8192_{args.square_dtype}": out}), flush=True)
         return
     if args.points:
