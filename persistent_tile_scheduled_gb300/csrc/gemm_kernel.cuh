@@ -368,11 +368,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
     const uint32_t ring_full0 = acc_empty0 + 16;             // + 8*r
     const uint32_t ring_empty0 = ring_full0 + 8 * kRing;     // + 8*r
     const uint32_t clc_bar = ring_empty0 + 8 * kRing;
-    const uint32_t started_cnt = clc_bar + 8;                // items the (leader's) producer has started
-    const uint32_t clc_resp = (started_cnt + 8 + 15) & ~15u;
+    const uint32_t started_bar = clc_bar + 8;                // producer (leader) starts an item
+    const uint32_t clc_resp = (started_bar + 8 + 15) & ~15u;
     const uint32_t ring0 = clc_resp + 16;                    // + 4*kRingWords*r: a decoded work item
     const uint32_t tmem_slot = ring0 + 4 * kRingWords * kRing;
     const uint32_t abort_flag = tmem_slot + 4;
+    const uint32_t started_cnt = tmem_slot + 8;              // items the (leader's) producer has started
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
@@ -403,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
             mbar_init(ring_empty0 + 8 * r, CG == 1 ? 2 + kEpiWarps : 3 + 2 * kEpiWarps);
         }
         mbar_init(clc_bar, 1);
+        mbar_init(started_bar, 1);
         st_shared_u32(started_cnt, 0u);
         st_shared_u32(abort_flag, 0u);
         fence_mbar_init();
@@ -586,7 +588,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
                 break;
             }
             if (w < 0) break;
-            if (leader && lane == 0) st_shared_u32(started_cnt, static_cast<uint32_t>(i + 1));
+            if (leader) {
+                mbar_arrive_if(one, started_bar);
+                if (lane == 0) st_shared_u32(started_cnt, static_cast<uint32_t>(i + 1));
+            }
             if (!load_tile(t, t.kb_begin, t.kb_end)) {
                 ok = false;
                 break;
@@ -1038,8 +1043,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
                 const int pieces = unit_items(u, p);
                 for (int j = 0; ok && j < pieces; ++j) {
                     const int w = unit_item(u, j, pieces, p);
+                    // Depth 1 waits for the producer to start item i on the started
+                    // barrier, whose phase parity is unambiguous there (the producer
+                    // cannot be past an item not yet published), and the hardware
+                    // may suspend the waiting warp.  Depth 2 lets the producer run a
+                    // further item ahead, past what a parity can tell apart, so it
+                    // waits on the started-item counter instead.
                     ok = publish(i, w, item_of(w))
-                         && (lead == 0 || ctl.wait_count_all(started_cnt, i + 2 - lead, WHERE_STARTED));
+                         && (lead == 0
+                             || (lead == 1 ? ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED)
+                                           : ctl.wait_count_all(started_cnt, i + 2 - lead, WHERE_STARTED)));
                     ++i;
                     if (ok && j == 0 && may_request) {
                         // the producer has begun the item `lead` - 1 before this one: claim the next unit

@@ -234,7 +234,7 @@ __host__ __device__ constexpr int smem_bytes(int cg, int stages, int bn = kTileN
     return 1024 + stages * (stage_bytes_a(cg) + stage_bytes_b(cg, bn)) + epi_bytes()
            + 8 * (2 * kMaxStages + 4 + 2 * kRing + 2)    // mbarriers
            + 16                                          // CLC response
-           + 4 * kRingWords * kRing + 16;                // ring payload, TMEM base, abort flag
+           + 4 * kRingWords * kRing + 16;                // ring payload, TMEM base, abort flag, started count
 }
 
 }  // namespace pts
