@@ -47,8 +47,19 @@ int main() {
     printf("], \"cta_group\": [");
     for (int kb = 1; kb <= 40; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb));
     printf("], \"pair_min_kb\": %d, \"sk_min_saved_kb\": %d", kPairMinKb, kSkMinSavedKb);
-    printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]}\n", kb_per_stage(1), kb_per_stage(2),
+    printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]", kb_per_stage(1), kb_per_stage(2),
            smem_bytes(1, 4), smem_bytes(2, 3), smem_bytes(1, 5));
+    printf(", \"narrow\": {\"smem\": %d, \"smem3\": %d, \"stages\": %d, \"per_sm\": [%d, %d], \"max_kb\": %d, \"tile\": [",
+           smem_bytes(1, kNarrowStages, kTileNNarrow), smem_bytes(1, 3, kTileNNarrow), kNarrowStages,
+           ctas_per_sm(kTileN), ctas_per_sm(kTileNNarrow), kNarrowMaxKb);
+    int first = 1;
+    for (int kb = 1; kb <= 10; ++kb)
+        for (int cg = 0; cg <= 2; ++cg)
+            for (int sched = 0; sched <= 2; ++sched) {
+                printf("%s[%d, %d, %d, %d]", first ? "" : ", ", kb, cg, sched, choose_tile_n(kb, cg, sched));
+                first = 0;
+            }
+    printf("]}}\n");
     return 0;
 }
 """
@@ -115,3 +126,17 @@ def test_shared_memory_budget(plan):
     # the default rings (4 single-CTA stages, 3 pair stages) fit the 227 KB a CTA may use; a
     # fifth single-CTA stage does not
     assert single <= 232448 and pair <= 232448 and five > 232448
+
+
+def test_narrow_tile_rules(plan):
+    """The narrow tile's ring, staging and barriers fit twice in an SM's 228 KB
+    with the 1 KB each CTA reserves (a third stage would not); the library picks
+    it only for the non-persistent grid, on tiles of at most 4 k-blocks, when
+    the CTA group is left to it."""
+    n = plan["narrow"]
+    assert n["stages"] == 2 and n["per_sm"] == [1, 2]
+    assert 2 * (n["smem"] + 1024) <= 233472 < 2 * (n["smem3"] + 1024)
+    assert n["max_kb"] == 4
+    for kb, cg, sched, tile in n["tile"]:
+        want = 128 if (cg == 0 and sched == 0 and kb <= 4) else 256
+        assert tile == want, (kb, cg, sched)
