@@ -508,8 +508,11 @@ def bf16_8192_sweep(pts, dev, stream, peaks, reps=5):
             del A, B, C
     finally:
         pts.gemm_destroy(h)
+    tensor = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
     for name in SCHED_NAMES:
         out[name + "_mean"] = round(sum(out[name]) / len(out[name]), 1)
+        if tensor:
+            out[name + "_pct_of_tensor_peak"] = [round(100.0 * t / tensor, 1) for t in out[name]]
     out["persistent_ahead_at_every_K"] = all(
         min(s_, c_) > n_ for s_, c_, n_ in zip(out["static"], out["clc"], out["nonpersistent"]))
     out["note"] = (f"median of {reps} back-to-back launches per K; inputs drawn on the GPU from seeded "
@@ -567,6 +570,12 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
                            "attainable_tflops": round(attain / 1e12, 1) if attain else None,
                            "frac": round(fl / (t * 1e-3) / attain, 3) if attain else None})
 
+    # the metric as named: TFLOP/s and % of the dense tensor peak vs K, per scheduler
+    # (isolated launches, an event between GEMMs)
+    if tensor_peak:
+        for v in per_sched.values():
+            v["per_k_pct_of_tensor_peak"] = [round(100.0 * t / tensor_peak, 1) for t in v["per_k_tflops_isolated"]]
+            v["pct_of_tensor_peak"] = round(100.0 * v["value"] / world / tensor_peak, 2)
     line = {
         "metric": METRIC, "value": round(head["value"], 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
