@@ -275,23 +275,52 @@ def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_g
     return total_ms, per_k, (t0, t1)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, else lscpu, else the machine type)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name") and ":" in line:
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name") and ":" in line:
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline_sample(problem, x, budget_s=10.0):
-    """The oracle as it stands on the host cores, on a bounded row sample."""
+    """The oracle as it stands on the host cores, on a bounded row sample: all
+    threads, and one thread on a smaller sample."""
     from oracle import gemm as og
     p = problem
     A, B = x.bits("A").reshape(-1), x.bits("B").reshape(-1)
-    rows, spent, flops = 1, 0.0, 0.0
-    while True:
-        t0 = time.perf_counter()
-        og.gemm(rows, p.N, p.K, A[: rows * p.K], B, p.dtype)
-        dt = time.perf_counter() - t0
-        spent, flops = dt, gemm_flops(rows, p.N, p.K)
-        if dt > budget_s / 4 or rows >= 512:
-            break
-        rows *= 4
-    return {"value": flops / spent / 1e12, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle",
+
+    def rate(nthreads, max_rows, budget):
+        rows, spent, flops = 1, 0.0, 0.0
+        while True:
+            t0 = time.perf_counter()
+            og.gemm(rows, p.N, p.K, A[: rows * p.K], B, p.dtype, nthreads=nthreads)
+            dt = time.perf_counter() - t0
+            spent, flops = dt, gemm_flops(rows, p.N, p.K)
+            if dt > budget / 4 or rows >= max_rows:
+                return flops / spent / 1e12, rows, spent
+            rows *= 4
+
+    v_all, rows, spent = rate(0, 512, budget_s)
+    v_one, rows1, spent1 = rate(1, 16, budget_s / 4)
+    return {"value": v_all, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of the M=N=4096, K={p.K} fp16 GEMM ({rows}x{p.N} outputs, "
-                      f"fp64 triple loop over all K), {spent:.1f} s"}
+                      f"fp64 triple loop over all K), {spent:.1f} s",
+            "single_thread": {"value": v_one, "unit": UNIT, "cores": 1,
+                              "sample": f"rows 0..{rows1 - 1} of the same GEMM, {spent1:.1f} s"},
+            "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_ours(args, dist, rank, world, local):
