@@ -314,6 +314,49 @@ def test_narrow_tile_keeps_two_ctas_per_sm():
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("sched", [pts.GEMM_SCHED_NONPERSISTENT, pts.GEMM_SCHED_CLC])
+def test_narrow_tile_runs_two_ctas_on_one_sm(sched):
+    """The hardware does co-schedule two narrow-tile CTAs per SM: in a launch
+    of one CTA per tile, the per-item records (SM id, MMA start and last store
+    times) show two CTAs active at once on every SM, and never three."""
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        x = wl.make_inputs(wl.fp16_4096_ksweep([512])[0])
+        p = x.problem
+        _run_checked(h, x, sched, full=False)
+        info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
+        run_device(h, x, sched)
+        st, recs, dev = pts.gemm_read_debug(h, int(info.work_items))
+        assert st == 0
+        ref = recs[0].t_mma_start
+
+        def rel(t):   # the records keep the low 32 bits of %globaltimer (ns)
+            return ((t - ref + (1 << 31)) & 0xFFFFFFFF) - (1 << 31)
+
+        spans = {}
+        for i in range(int(info.work_items)):
+            r = recs[i]
+            sm, t0, t1 = spans.get(r.owner, (r.smid, 1 << 40, -(1 << 40)))
+            spans[r.owner] = (sm, min(t0, rel(r.t_mma_start)), max(t1, rel(r.t_stored)))
+        per_sm = {}
+        for sm, t0, t1 in spans.values():
+            per_sm.setdefault(sm, []).append((t0, t1))
+        most = {}
+        for sm, iv in per_sm.items():
+            events = sorted([(t0, 1) for t0, _ in iv] + [(t1, -1) for _, t1 in iv], key=lambda e: (e[0], e[1]))
+            c = m = 0
+            for _, d in events:
+                c += d
+                m = max(m, c)
+            most[sm] = m
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert len(most) == sms
+        assert max(most.values()) == 2
+        assert sum(1 for m in most.values() if m == 2) >= sms * 3 // 4, most
+    finally:
+        pts.gemm_destroy(h)
+
+
 def test_automatic_tile_choice():
     """With the shape left to the library, the non-persistent grid takes the
     narrow tile for tiles of at most 4 k-blocks; the persistent grids, and a
