@@ -414,6 +414,29 @@ def test_narrow_tile_sweep_points_sampled(K):
         pts.gemm_destroy(h)
 
 
+# ------------------------------------------------------- long and skinny
+
+LONG = [(300, 264, 65536, wl.BF16), (1, 8, 8192, wl.F16), (8, 4096, 4096, wl.BF16), (4096, 8, 2048, wl.E4M3),
+        (129, 1032, 24576, wl.F16)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", LONG, ids=[f"{m}x{n}x{k}-{wl.DTYPE_NAMES[d]}" for m, n, k, d in LONG])
+def test_long_and_skinny_problems(shape):
+    """Library defaults on long accumulations (up to 1024 k-blocks per tile,
+    column slices below one wave) and on single-row, single-tile-column and
+    eight-column outputs, every scheduler, element by element."""
+    M, N, K, dt = shape
+    h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        dist = "normal" if dt == wl.E4M3 else "normal_sqrtk"
+        x = wl.make_inputs(wl.Problem("long", M, N, K, dt, dist, M + N + K))
+        for sched in SCHEDS:
+            _run_checked(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+
+
 # ---------------------------------------------------------------- full sizes
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
