@@ -578,6 +578,37 @@ def test_wait_time_out_is_reported_and_the_context_survives(shape, sched):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("sched", [pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC])
+def test_stream_k_state_is_cleared_after_a_device_error(sched):
+    """A stream-K launch that stops on a wait time-out leaves some cut tiles
+    claimed by one piece only (1000 x 1800 x 2000 on five clusters: every
+    producer withholds its 40th stage, after each unit's first piece of a cut
+    tile has claimed and before the piece that shares that tile).
+    gemm_check reports the time-out and zeroes the handle's claim counters and
+    ready flags, so the next stream-K launch on the same handle, whose cut
+    tiles use the same slots and whose producers stay below the withheld
+    stage, is exact."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=1, split_k=1, max_clusters=5, timeout_ns=20_000_000,
+                                         debug_flags=pts.GEMM_DEBUG_FAULT_SKIP_TMA, fault_arg=40))
+    try:
+        x1 = wl.custom(1000, 1800, 2000, wl.BF16, "uniform", 81)
+        info1 = pts.gemm_query(h, 1000, 1800, 2000, wl.BF16, sched)
+        assert info1.split_k == 1 and int(info1.sk_tiles) == 64 % 5 + 5
+        run_device(h, x1, sched)
+        st, dev = pts.gemm_check(h)
+        assert st == pts.gemm.GEMM_ERR_TIMEOUT, f"status {st}, device word {dev:#x}"
+        x2 = wl.custom(300, 520, 208, wl.BF16, "uniform", 82)
+        info2 = pts.gemm_query(h, 300, 520, 208, wl.BF16, sched)
+        assert info2.split_k == 1 and int(info2.sk_tiles) == 9     # every tile in the stream-K region
+        for _ in range(2):
+            C = run_device(h, x2, sched)
+            st, dev = pts.gemm_check(h)
+            assert st == 0, f"status {st}, device word {dev:#x}"
+            assert compare_full(x2, C) <= TOL[wl.BF16]
+    finally:
+        pts.gemm_destroy(h)
+
+
 @pytest.mark.parametrize("dtype,per_clk", [(wl.F16, 8192), (wl.BF16, 8192), (wl.E4M3, 16384)])
 @pytest.mark.parametrize("cg", [1, 2])
 def test_tensor_peak_probe_pins_the_per_sm_rate(dtype, per_clk, cg):
