@@ -71,16 +71,18 @@ def _check_positions(x, C, ii, jj, what):
 @pytest.mark.parametrize("sched", [pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC, pts.GEMM_SCHED_NONPERSISTENT])
 def test_captured_stream_k_gemm_replayed_three_times(cg, sched):
     """One fp16 4096^3 GEMM with the stream-K share, captured once and replayed
-    three times; C is overwritten with NaN before each replay, and every
-    replay must match the oracle on every cut tile."""
-    x = wl.make_inputs(wl.fp16_4096_ksweep([4096])[0])
-    p = x.problem
+    three times.  Before each replay the captured A and B buffers receive new
+    seeded inputs and C is overwritten with NaN, so a partial left over from an
+    earlier replay holds the wrong numbers; every replay must match its own
+    inputs' oracle on every cut tile."""
+    p = wl.fp16_4096_ksweep([4096])[0]
+    xs = [wl.make_inputs(wl.Problem(p.name, p.M, p.N, p.K, p.dtype, p.dist, p.seed + 100 * r)) for r in range(3)]
     h = pts.gemm_create(0, pts.make_opts(cta_group=cg, split_k=1))
     s = torch.cuda.Stream()
     try:
         info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
         assert info.split_k == 1
-        A, B = x.A.cuda(), x.B.cuda()
+        A, B = xs[0].A.cuda(), xs[0].B.cuda()
         C = torch.empty(p.M, p.N, dtype=torch.float16, device="cuda")
         torch.cuda.synchronize()
         pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, s)   # grows the workspace
@@ -90,8 +92,10 @@ def test_captured_stream_k_gemm_replayed_three_times(cg, sched):
             pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, s)
         ii, jj, ncut = cut_tile_positions(info, p.M, p.N, p.K)
         ri, rj = sample_positions(p.M, p.N, int(info.tile_m), int(info.tile_n), n_random=2048, seed=3)
-        for r in range(3):
+        for r, x in enumerate(xs):
             with torch.cuda.stream(s):
+                A.copy_(x.A, non_blocking=False)
+                B.copy_(x.B, non_blocking=False)
                 C.fill_(float("nan"))
                 g.replay()
             st, dev = pts.gemm_check(h, s)
@@ -104,31 +108,36 @@ def test_captured_stream_k_gemm_replayed_three_times(cg, sched):
 
 
 def test_graph_with_the_same_stream_k_gemm_twice():
-    """Two launches of one stream-K GEMM inside one graph (into two outputs):
-    the second launch of each replay starts from the counters the first left."""
-    x = wl.make_inputs(wl.fp16_4096_ksweep([2048])[0])
-    p = x.problem
+    """Two launches of one stream-K GEMM inside one graph, on two input sets
+    into two outputs: the second launch of each replay starts from the
+    counters the first left; new inputs before every replay."""
+    p = wl.fp16_4096_ksweep([2048])[0]
     h = pts.gemm_create(0, pts.make_opts(cta_group=2, split_k=1))
     s = torch.cuda.Stream()
     try:
         info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, pts.GEMM_SCHED_STATIC)
-        A, B = x.A.cuda(), x.B.cuda()
-        Cs = [torch.empty(p.M, p.N, dtype=torch.float16, device="cuda") for _ in range(2)]
+        sets = [[wl.make_inputs(wl.Problem(p.name, p.M, p.N, p.K, p.dtype, p.dist, p.seed + 10 * r + n))
+                 for n in range(2)] for r in range(2)]
+        dev = [(sets[0][n].A.cuda(), sets[0][n].B.cuda(), torch.empty(p.M, p.N, dtype=torch.float16, device="cuda"))
+               for n in range(2)]
         torch.cuda.synchronize()
-        pts.gemm_run(h, p.M, p.N, p.K, A, B, Cs[0], p.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s)
+        A0, B0, C0 = dev[0]
+        pts.gemm_run(h, p.M, p.N, p.K, A0, B0, C0, p.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s)
         assert pts.gemm_check(h, s)[0] == 0
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            for C in Cs:
+            for A, B, C in dev:
                 pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s)
         ii, jj, _ = cut_tile_positions(info, p.M, p.N, p.K)
         for r in range(2):
             with torch.cuda.stream(s):
-                for C in Cs:
+                for (A, B, C), x in zip(dev, sets[r]):
+                    A.copy_(x.A)
+                    B.copy_(x.B)
                     C.fill_(float("nan"))
                 g.replay()
             assert pts.gemm_check(h, s)[0] == 0
-            for n, C in enumerate(Cs):
+            for n, ((_, _, C), x) in enumerate(zip(dev, sets[r])):
                 _check_positions(x, C, ii, jj, f"replay {r}, launch {n}")
         del g
     finally:
@@ -169,8 +178,12 @@ def test_bench_step_replayed_matches_oracle():
             bench.sweep_pass(pts, h, bufs, problems, pts.GEMM_SCHED_STATIC, s)
         for r in range(2):
             with torch.cuda.stream(s):
-                for q, (_, _, C) in zip(problems, bufs):
+                for q, (A, B, C) in zip(problems, bufs):
                     if q.K in checked:
+                        if r > 0:   # new inputs, so that a stale partial would show
+                            xs[q.K] = wl.make_inputs(wl.Problem(q.name, q.M, q.N, q.K, q.dtype, q.dist, q.seed + 7 * r))
+                            A.copy_(xs[q.K].A)
+                            B.copy_(xs[q.K].B)
                         C.fill_(float("nan"))
                 g.replay()
             assert pts.gemm_check(h, s)[0] == 0
