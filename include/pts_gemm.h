@@ -108,9 +108,12 @@ typedef struct gemm_opts {
                                        non-persistent scheduler when a tile has <= 4 k-blocks and
                                        cta_group is 0, else 256);
                                        256 = the wide tile (one CTA, or CTA pair, per SM);
-                                       128 = the narrow tile: 128 x 128 per CTA, single CTAs,
-                                       two resident per SM (needs cta_group 0 or 1); no stream-K
-                                       share and no column quarters (split 4) with it.
+                                       128 = the narrow tile: 128 x 128 per CTA; with cta_group
+                                       0 or 1 single CTAs, two resident per SM; with cta_group 2
+                                       a 256 x 128 tile per CTA pair, one CTA per SM (a pair is
+                                       never given a second CTA per SM: where the hardware puts
+                                       the two CTAs of a pair then is not documented); no
+                                       stream-K share and no column quarters (split 4) with it.
                                        gemm_run_grouped and gemm_run_noalloc use the wide tile. */
     int clc_depth;                  /* GEMM_SCHED_CLC: how far ahead of the producer a cluster
                                        claims work.  1 = the next unit is claimed when the producer

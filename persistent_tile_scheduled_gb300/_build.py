@@ -1,8 +1,8 @@
 """Build the CUDA library libpts_gemm.so in-tree with nvcc for sm_103a.
 
-Six translation units (the wide-tile 1-SM kernels, the 2-SM kernels, the
-narrow-tile kernels, the C ABI, the allocation-free entry point and the
-tensor-pipe peak probe) are compiled in parallel, then linked with the static
+Seven translation units (the wide-tile 1-SM kernels, the 2-SM kernels, the
+narrow-tile 1-SM and 2-SM kernels, the C ABI, the allocation-free entry point
+and the tensor-pipe peak probe) are compiled in parallel, then linked with the static
 CUDA runtime.  Nothing is rebuilt when the library is newer than every source
 file.
 """
@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libpts_gemm.so")
-UNITS = ["gemm_cg1.cu", "gemm_cg2.cu", "gemm_narrow.cu", "gemm_api.cu", "gemm_noalloc.cu", "peak_probe.cu"]
+UNITS = ["gemm_cg1.cu", "gemm_cg2.cu", "gemm_narrow.cu", "gemm_narrow_cg2.cu", "gemm_api.cu", "gemm_noalloc.cu",
+         "peak_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

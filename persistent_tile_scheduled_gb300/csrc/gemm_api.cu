@@ -68,10 +68,11 @@ struct gemm_ctx {
     cudaEvent_t ev_tab[kGroupSlots] = {};
     int tab_cur = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    // per dtype and kernel variant (0: wide tile, single CTAs; 1: wide, pairs; 2: narrow tile)
-    bool smem_set[3][3] = {};
-    int occ_smem[3][3] = {};                  // smem the cached occupancy was computed for
-    int occ_clusters[3][3] = {};
+    // per dtype and kernel variant (0: wide tile, single CTAs; 1: wide, pairs; 2: narrow tile,
+    // single CTAs; 3: narrow tile, pairs)
+    bool smem_set[3][4] = {};
+    int occ_smem[3][4] = {};                  // smem the cached occupancy was computed for
+    int occ_clusters[3][4] = {};
     MapEntry maps[kMapCache];
 };
 
@@ -119,12 +120,13 @@ const CUtensorMap *get_map(gemm_ctx *h, const void *ptr, uint64_t rows, uint64_t
     return &m.map;
 }
 
-// Kernel variant: 0 wide tile, single CTAs; 1 wide tile, CTA pairs; 2 narrow tile.
-int variant_of(int cg, int bn) { return bn == pts::kTileNNarrow ? 2 : cg - 1; }
+// Kernel variant: 0 wide tile, single CTAs; 1 wide tile, CTA pairs; 2 narrow
+// tile, single CTAs; 3 narrow tile, CTA pairs.
+int variant_of(int cg, int bn) { return (bn == pts::kTileNNarrow ? 2 : 0) + cg - 1; }
 
 pts::KernelOps ops_for(int kind, int cg, int bn)
 {
-    if (bn == pts::kTileNNarrow) return pts::kernel_ops_narrow(kind);
+    if (bn == pts::kTileNNarrow) return cg == 2 ? pts::kernel_ops_narrow_cg2(kind) : pts::kernel_ops_narrow(kind);
     return cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind);
 }
 
@@ -159,7 +161,7 @@ gemm_status_t check_sizes(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, g
 gemm_status_t kernel_shape(gemm_ctx *h, gemm_dtype_t dtype, Plan &pl)
 {
     int stages = h->opts.stages;
-    if (stages == 0 && pl.bn == pts::kTileNNarrow) {
+    if (stages == 0 && pl.bn == pts::kTileNNarrow && pl.cg == 1) {
         stages = pts::kNarrowStages;   // the ring that lets two CTAs share an SM
     } else if (stages == 0) {          // the deepest ring that fits
         stages = pts::kMaxStages;
@@ -199,14 +201,15 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
 {
     const int64_t kelems = dtype == GEMM_E4M3 ? 128 : 64;
     pl.num_kb = (K + kelems - 1) / kelems;
-    // tile width: the narrow tile (two CTAs per SM) for short tiles when the
-    // caller leaves the shape to the library and forces nothing it lacks
-    // (the stream-K share, column quarters)
+    // tile width: the narrow tile (single CTAs, two per SM) for short tiles
+    // when the caller leaves the shape to the library and forces nothing it
+    // lacks (the stream-K share, column quarters); its pair form only when
+    // asked for (tile_n 128 with cta_group 2)
     const bool forced_wide_only = h->opts.split_k == 1 || h->opts.split == 4;
     pl.bn = h->opts.tile_n != 0 ? h->opts.tile_n
                                 : (forced_wide_only ? pts::kTileN
                                                     : pts::choose_tile_n(pl.num_kb, h->opts.cta_group, int(sched)));
-    pl.cg = pl.bn == pts::kTileNNarrow ? 1
+    pl.cg = pl.bn == pts::kTileNNarrow ? (h->opts.cta_group == 2 ? 2 : 1)
                                         : (h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb));
     const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
     pl.tiles_m = (M + tile_m - 1) / tile_m;
@@ -626,8 +629,7 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
     if (o.tile_n != 0 && o.tile_n != pts::kTileN && o.tile_n != pts::kTileNNarrow) return GEMM_ERR_INVALID_ARG;
     if (o.clc_depth < 0 || o.clc_depth > 2) return GEMM_ERR_INVALID_ARG;
     if (o.clc_depth == 0) o.clc_depth = pts::kDefaultClcLead;
-    if (o.tile_n == pts::kTileNNarrow && (o.cta_group == 2 || o.split == 4 || o.split_k == 1))
-        return GEMM_ERR_INVALID_ARG;
+    if (o.tile_n == pts::kTileNNarrow && (o.split == 4 || o.split_k == 1)) return GEMM_ERR_INVALID_ARG;
     if (o.debug_flags & ~(GEMM_DEBUG_RECORDS | GEMM_DEBUG_CLC_STOP_AT | GEMM_DEBUG_FAULT_SKIP_TMA))
         return GEMM_ERR_INVALID_ARG;
 

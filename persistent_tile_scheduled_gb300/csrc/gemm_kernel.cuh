@@ -3,7 +3,8 @@
 //   C[M x N] = A[M x K] . B[N x K]^T      (fp32 accumulation in TMEM)
 //
 // One CTA (CG = 1) or one CTA pair (CG = 2, tcgen05 cta_group::2) computes a
-// (128*CG) x 256 output tile at a time.  Warp roles:
+// (128*CG) x BN output tile at a time (BN = 256, or 128 for the narrow tile).
+// Warp roles:
 //   warp 0     producer: TMA loads of A and B k-blocks into an S-stage
 //              shared-memory ring guarded by full/empty mbarriers (one k-block
 //              per stage for a single CTA, two for a pair)
@@ -334,18 +335,19 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits, fl
 }
 
 template <int KIND, int CG, int BN = kTileN>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm(BN))
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(CG, BN))
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmB4,
                 const __grid_constant__ CUtensorMap tmC, const GemmParams p)
 {
     // BN: tile columns, 256 (the wide tile, one CTA per SM) or 128 (the
-    // narrow tile, single CTAs, two per SM; no stream-K share and no column
-    // quarters, so its epilogue holds fewer registers).
+    // narrow tile: single CTAs two per SM, or CTA pairs one per SM; no
+    // stream-K share and no column quarters, so its epilogue holds fewer
+    // registers).
     // tmB / tmB2 / tmB4: B boxes of BN/CG, BN/CG/2 and BN/CG/4 rows, for whole
     // tiles and for the column slices (halves, quarters) of a problem smaller
     // than one wave
-    static_assert(BN == kTileN || (BN == kTileNNarrow && CG == 1), "tile shape");
+    static_assert(BN == kTileN || BN == kTileNNarrow, "tile shape");
     constexpr bool kStreamK = BN == kTileN;   // the stream-K fixup is built for the wide tile only
     constexpr uint32_t kAccCols = 2 * BN;     // TMEM columns: two accumulators
     constexpr int KBS = kb_per_stage(CG);   // k-blocks per ring stage

@@ -21,8 +21,10 @@ struct KernelOps {
 // kind: 0 fp16, 1 bf16, 2 e4m3
 KernelOps kernel_ops_cg1(int kind);
 KernelOps kernel_ops_cg2(int kind);
-// the narrow tile (128 x 128 per CTA, single CTAs, two per SM)
+// the narrow tile: 128 x 128 per CTA, single CTAs, two per SM
 KernelOps kernel_ops_narrow(int kind);
+// the narrow tile as CTA pairs: 256 x 128 per pair, one CTA per SM
+KernelOps kernel_ops_narrow_cg2(int kind);
 cudaError_t launch_zero_fill(void *c, long long bytes, cudaStream_t stream);
 
 }  // namespace pts

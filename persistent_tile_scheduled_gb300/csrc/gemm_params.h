@@ -9,12 +9,13 @@ namespace pts {
 
 // One CTA owns 128 rows of the output tile and its TMEM accumulator holds
 // 128 lanes x 256 fp32 columns (the wide tile, one CTA per SM) or 128 lanes x
-// 128 columns (the narrow tile, whose smaller ring and accumulators let two
-// CTAs share an SM).  A k-block is 128 bytes of K per row (64 fp16/bf16 or
-// 128 e4m3 elements): one 128-byte swizzle atom row.
+// 128 columns (the narrow tile: single CTAs, whose smaller ring and
+// accumulators let two of them share an SM, or CTA pairs, 256 x 128 per pair,
+// one CTA per SM).  A k-block is 128 bytes of K per row (64 fp16/bf16 or 128
+// e4m3 elements): one 128-byte swizzle atom row.
 constexpr int kRowsPerCta = 128;
 constexpr int kTileN = 256;             // columns of the wide tile
-constexpr int kTileNNarrow = 128;       // columns of the narrow tile (single CTAs, two per SM)
+constexpr int kTileNNarrow = 128;       // columns of the narrow tile
 constexpr int kKBlockBytes = 128;
 constexpr int kThreads = 224;           // warp 0 producer, warp 1 MMA, warps 2-5 epilogue, warp 6 scheduler
 constexpr int kEpiWarps = 4;
@@ -200,8 +201,15 @@ inline int choose_split(int64_t tiles, int64_t resident)
 // for the narrow pair -- so the narrow tile ties at 2 k-blocks and loses
 // beyond.  The non-persistent grid, which starts a CTA per tile, gains from
 // two CTAs per SM up to 4 k-blocks.
-__host__ __device__ constexpr int ctas_per_sm(int bn) { return bn == kTileN ? 1 : 2; }
-constexpr int kNarrowStages = 2;
+//
+// The narrow tile also comes as a CTA pair (256 x 128 per pair, tcgen05
+// cta_group::2), but at one CTA per SM, with the deepest ring that fits: the
+// two CTAs of a pair then sit on two SMs by construction.  Nothing available
+// here documents where the hardware puts a pair's two CTAs when one SM could
+// hold both, and a pair's MMA cannot run with both on one SM, so pairs are
+// never given a second CTA per SM.
+__host__ __device__ constexpr int ctas_per_sm(int cg, int bn) { return (bn == kTileNNarrow && cg == 1) ? 2 : 1; }
+constexpr int kNarrowStages = 2;        // ring stages of the narrow single CTA
 // Narrow tiles when the caller leaves both the tile and the CTA group to the
 // library: for the non-persistent grid (sched 0) on tiles of at most this
 // many k-blocks.

@@ -61,7 +61,7 @@ def test_bad_options_are_rejected_before_touching_a_device():
                 g.make_opts(split=2, split_k=1), g.make_opts(overlap_launch=1), g.make_opts(overlap_launch=-2),
                 g.make_opts(epilogue=3), g.make_opts(max_clusters=-1), g.make_opts(group_order=3),
                 g.make_opts(group_order=-1), g.make_opts(tile_n=64), g.make_opts(tile_n=512),
-                g.make_opts(tile_n=128, cta_group=2), g.make_opts(tile_n=128, split=4),
+                g.make_opts(tile_n=128, split=4),
                 g.make_opts(tile_n=128, split_k=1), g.make_opts(clc_depth=3), g.make_opts(clc_depth=-1)):
         assert lib.gemm_create(ctypes.byref(h), 0, ctypes.byref(bad)) == g.GEMM_ERR_INVALID_ARG
         assert h.value is None

@@ -21,9 +21,11 @@ pytestmark = pytest.mark.gpu
 SCHEDS = [pts.GEMM_SCHED_NONPERSISTENT, pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC]
 
 
-# the wide tile (128 x 256 per CTA) with single CTAs and with CTA pairs, and
-# the narrow tile (128 x 128 per CTA, two CTAs per SM)
-SHAPES = {"cg1": dict(cta_group=1), "cg2": dict(cta_group=2), "narrow": dict(cta_group=1, tile_n=128)}
+# the wide tile (128 x 256 per CTA) with single CTAs and with CTA pairs, the
+# narrow tile (128 x 128 per CTA, two CTAs per SM) and its pair form (256 x 128
+# per CTA pair, one CTA per SM)
+SHAPES = {"cg1": dict(cta_group=1), "cg2": dict(cta_group=2), "narrow": dict(cta_group=1, tile_n=128),
+          "narrow_cg2": dict(cta_group=2, tile_n=128)}
 
 
 @pytest.fixture(scope="module", params=list(SHAPES), ids=list(SHAPES))
@@ -377,16 +379,41 @@ def test_automatic_tile_choice():
 
 
 def test_narrow_tile_rejects_what_it_lacks():
-    for bad in (dict(tile_n=128, cta_group=2), dict(tile_n=128, split=4), dict(tile_n=128, split_k=1),
+    for bad in (dict(tile_n=128, split=4), dict(tile_n=128, split_k=1), dict(tile_n=128, cta_group=2, split=4),
                 dict(tile_n=64)):
         with pytest.raises(pts.GemmError):
             pts.gemm_create(0, pts.make_opts(**bad))
 
 
+def test_narrow_pair_tile_shape():
+    """The narrow tile's pair form: 256 x 128 per CTA pair, one CTA per SM, a
+    ring of four two-k-block stages, so the static grid holds one pair per two
+    SMs; never chosen by the library on its own."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, cta_group=2))
+    h0 = pts.gemm_create(0, pts.make_opts())
+    try:
+        for dt, K in ((wl.F16, 512), (wl.BF16, 4096), (wl.E4M3, 1024)):
+            info = pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_STATIC)
+            assert (info.tile_m, info.tile_n, info.cta_group, info.ctas_per_sm) == (256, 128, 2, 1)
+            assert info.stages == 4 and info.max_active_clusters == sms // 2
+            assert info.grid_ctas == sms and info.tiles == 16 * 32 and info.split_k == 0
+            for sched in SCHEDS:
+                auto = pts.gemm_query(h0, 4096, 4096, K, dt, sched)
+                assert not (auto.tile_n == 128 and auto.cta_group == 2)
+        # below one wave: column halves at most
+        assert pts.gemm_query(h, 300, 520, 208, wl.BF16, pts.GEMM_SCHED_STATIC).split == 2
+    finally:
+        pts.gemm_destroy(h)
+        pts.gemm_destroy(h0)
+
+
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("sched", SCHEDS)
-def test_narrow_tile_column_halves(sched):
-    """Sub-wave problems on the narrow tile are cut into 64-column halves."""
-    h = pts.gemm_create(0, pts.make_opts(tile_n=128, split=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
+def test_narrow_tile_column_halves(sched, cg):
+    """Sub-wave problems on the narrow tile (and its pair form) are cut into
+    64-column halves."""
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, cta_group=cg, split=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
         for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 96, wl.E4M3)]:
             dist = "normal" if dt == wl.E4M3 else "uniform"
@@ -409,6 +436,22 @@ def test_narrow_tile_sweep_points_sampled(K):
         for sched in SCHEDS:
             info = pts.gemm_query(h, 4096, 4096, K, wl.F16, sched)
             assert info.tile_n == 128 and info.ctas_per_sm == 2
+            _run_checked(h, x, sched, full=False)
+    finally:
+        pts.gemm_destroy(h)
+
+
+@pytest.mark.parametrize("K", [512, 4096])
+def test_narrow_pair_tile_sweep_points_sampled(K):
+    """Full-size fp16 4096^2 points on the narrow tile's pair form (512 tiles
+    of 256 x 128 on 76 pairs), every scheduler, every work item's record
+    checked against the scheduler model."""
+    h = pts.gemm_create(0, pts.make_opts(tile_n=128, cta_group=2, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
+        for sched in SCHEDS:
+            info = pts.gemm_query(h, 4096, 4096, K, wl.F16, sched)
+            assert (info.tile_m, info.tile_n, info.cta_group) == (256, 128, 2)
             _run_checked(h, x, sched, full=False)
     finally:
         pts.gemm_destroy(h)

@@ -49,9 +49,11 @@ int main() {
     printf("], \"pair_min_kb\": %d, \"sk_min_saved_kb\": %d", kPairMinKb, kSkMinSavedKb);
     printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]", kb_per_stage(1), kb_per_stage(2),
            smem_bytes(1, 4), smem_bytes(2, 3), smem_bytes(1, 5));
-    printf(", \"narrow\": {\"smem\": %d, \"smem3\": %d, \"stages\": %d, \"per_sm\": [%d, %d], \"max_kb\": %d, \"tile\": [",
+    printf(", \"narrow\": {\"smem\": %d, \"smem3\": %d, \"stages\": %d, \"per_sm\": [%d, %d, %d, %d], "
+           "\"pair_smem\": [%d, %d], \"max_kb\": %d, \"tile\": [",
            smem_bytes(1, kNarrowStages, kTileNNarrow), smem_bytes(1, 3, kTileNNarrow), kNarrowStages,
-           ctas_per_sm(kTileN), ctas_per_sm(kTileNNarrow), kNarrowMaxKb);
+           ctas_per_sm(1, kTileN), ctas_per_sm(2, kTileN), ctas_per_sm(1, kTileNNarrow), ctas_per_sm(2, kTileNNarrow),
+           smem_bytes(2, 4, kTileNNarrow), smem_bytes(2, 5, kTileNNarrow), kNarrowMaxKb);
     int first = 1;
     for (int kb = 1; kb <= 10; ++kb)
         for (int cg = 0; cg <= 2; ++cg)
@@ -130,12 +132,18 @@ def test_shared_memory_budget(plan):
 
 def test_narrow_tile_rules(plan):
     """The narrow tile's ring, staging and barriers fit twice in an SM's 228 KB
-    with the 1 KB each CTA reserves (a third stage would not); the library picks
-    it only for the non-persistent grid, on tiles of at most 4 k-blocks, when
-    the CTA group is left to it."""
+    with the 1 KB each CTA reserves (a third stage would not); its pair form
+    runs one CTA per SM, with a ring of four two-k-block stages (48 KB each:
+    128 rows of A and 64 of B per k-block) in the 227 KB a CTA may use (a fifth
+    would not fit); the library picks the narrow tile only for the
+    non-persistent grid, on tiles of at most 4 k-blocks, when the CTA group is
+    left to it (so never the pair form)."""
     n = plan["narrow"]
-    assert n["stages"] == 2 and n["per_sm"] == [1, 2]
+    assert n["stages"] == 2 and n["per_sm"] == [1, 1, 2, 1]
     assert 2 * (n["smem"] + 1024) <= 233472 < 2 * (n["smem3"] + 1024)
+    four, five = n["pair_smem"]
+    assert four <= 232448 < five
+    assert five - four == 2 * (128 + 64) * 128
     assert n["max_kb"] == 4
     for kb, cg, sched, tile in n["tile"]:
         want = 128 if (cg == 0 and sched == 0 and kb <= 4) else 256
