@@ -295,31 +295,40 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def cpu_baseline_sample(problem, x, budget_s=10.0):
-    """The oracle as it stands on the host cores, on a bounded row sample: all
-    threads, and one thread on a smaller sample."""
+def cpu_baseline_sample(problems, xs, budget_s=10.0):
+    """The oracle as it stands on the host cores: on all threads, whole GEMMs of
+    the sweep, the largest K first, until `budget_s` seconds have been spent
+    (a bounded sample of the step's own work); on one thread, a row sample of
+    the largest-K GEMM."""
     from oracle import gemm as og
-    p = problem
+    order = sorted(range(len(problems)), key=lambda i: -problems[i].K)
+    spent, flops, done = 0.0, 0.0, []
+    for i in order:
+        p, x = problems[i], xs[i]
+        t0 = time.perf_counter()
+        og.gemm(p.M, p.N, p.K, x.bits("A").reshape(-1), x.bits("B").reshape(-1), p.dtype, nthreads=0)
+        spent += time.perf_counter() - t0
+        flops += gemm_flops(p.M, p.N, p.K)
+        done.append(p.K)
+        if spent >= budget_s:
+            break
+    p, x = problems[order[0]], xs[order[0]]
     A, B = x.bits("A").reshape(-1), x.bits("B").reshape(-1)
-
-    def rate(nthreads, max_rows, budget):
-        rows, spent, flops = 1, 0.0, 0.0
-        while True:
-            t0 = time.perf_counter()
-            og.gemm(rows, p.N, p.K, A[: rows * p.K], B, p.dtype, nthreads=nthreads)
-            dt = time.perf_counter() - t0
-            spent, flops = dt, gemm_flops(rows, p.N, p.K)
-            if dt > budget / 4 or rows >= max_rows:
-                return flops / spent / 1e12, rows, spent
-            rows *= 4
-
-    v_all, rows, spent = rate(0, 512, budget_s)
-    v_one, rows1, spent1 = rate(1, 16, budget_s / 4)
-    return {"value": v_all, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of the M=N=4096, K={p.K} fp16 GEMM ({rows}x{p.N} outputs, "
-                      f"fp64 triple loop over all K), {spent:.1f} s",
+    rows, spent1 = 1, 0.0
+    while True:   # one thread: rows 0..rows-1, growing until it takes a second or 16 rows
+        t0 = time.perf_counter()
+        og.gemm(rows, p.N, p.K, A[: rows * p.K], B, p.dtype, nthreads=1)
+        spent1 = time.perf_counter() - t0
+        if spent1 > 1.0 or rows >= 16:
+            break
+        rows *= 4
+    v_one = gemm_flops(rows, p.N, p.K) / spent1 / 1e12
+    ks = ", ".join(str(k) for k in done)
+    return {"value": flops / spent / 1e12, "unit": UNIT, "cores": og.max_threads(), "kind": "oracle",
+            "sample": f"{len(done)} whole GEMMs of the sweep, the largest K first (M = N = 4096, K = {ks}; "
+                      f"fp64 triple loop over all outputs and all K), {spent:.1f} s",
             "single_thread": {"value": v_one, "unit": UNIT, "cores": 1,
-                              "sample": f"rows 0..{rows1 - 1} of the same GEMM, {spent1:.1f} s"},
+                              "sample": f"rows 0..{rows - 1} of the K = {p.K} GEMM, {spent1:.1f} s"},
             "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
@@ -632,7 +641,7 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
     if extra is not None:
         line["square_8192_bf16"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(problems[-1], xs[-1])
+        line["cpu_baseline"] = cpu_baseline_sample(problems, xs)
     return line
 
 
