@@ -592,6 +592,69 @@ def test_two_gemms_on_two_streams():
             pts.gemm_destroy(h)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_gemm_started_while_another_holds_half_the_sms(sched):
+    """A long GEMM (one 128 x 256 tile per CTA on half the SMs) starts first on
+    one stream; 5120^2 x 4096 starts on another while it runs.  Part of the
+    second grid then finds no free SM: the static grid's later clusters wait
+    for the occupier, CLC's resident clusters take their units over, and the
+    stream-K pieces of the second GEMM run with part of the grid not yet
+    resident (a piece that adds a partial waits only for a piece that has
+    already claimed, so is resident).  Coverage exact and both results within
+    tolerance."""
+    import time
+    half = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    xo = wl.make_inputs(wl.Problem("occupier", half * 128, 256, 16384, wl.BF16, "normal_sqrtk", 7300))
+    xm = wl.make_inputs(wl.Problem("main", 5120, 5120, 4096, wl.BF16, "normal_sqrtk", 7301))
+    ho = pts.gemm_create(0, pts.make_opts(cta_group=1, split=1))
+    hm = pts.gemm_create(0, pts.make_opts(cta_group=1, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    s_occ, s_main = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        po, pm = xo.problem, xm.problem
+        info = pts.gemm_query(hm, pm.M, pm.N, pm.K, pm.dtype, sched)
+        assert info.split_k == 1   # the stream-K share is part of this plan
+        Ao, Bo = xo.A.cuda(), xo.B.cuda()
+        Am, Bm = xm.A.cuda(), xm.B.cuda()
+        Co = torch.empty(po.M, po.N, dtype=torch.bfloat16, device="cuda")
+        Cm = torch.empty(pm.M, pm.N, dtype=torch.bfloat16, device="cuda")
+        # one call each first: a handle's first call sets up its kernel and grows
+        # its workspace (cudaMalloc may wait for the device), which would keep
+        # the two GEMMs from overlapping
+        pts.gemm_run(ho, po.M, po.N, po.K, Ao, Bo, Co, po.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s_occ)
+        pts.gemm_run(hm, pm.M, pm.N, pm.K, Am, Bm, Cm, pm.dtype, sched, 1.0, 1.0, s_main)
+        torch.cuda.synchronize()
+        Co.fill_(float("nan"))
+        Cm.fill_(float("nan"))
+        torch.cuda.synchronize()
+        pts.gemm_run(ho, po.M, po.N, po.K, Ao, Bo, Co, po.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s_occ)
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 25e-6:   # let the occupier's CTAs become resident
+            pass
+        pts.gemm_run(hm, pm.M, pm.N, pm.K, Am, Bm, Cm, pm.dtype, sched, 1.0, 1.0, s_main)
+        torch.cuda.synchronize()
+        assert pts.gemm_check(ho, s_occ)[0] == 0
+        st, recs, dev = pts.gemm_read_debug(hm, int(info.work_items), s_main)
+        assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
+        check_records(recs, info, sched, pm.K)
+        if sched == pts.GEMM_SCHED_STATIC:
+            # the scenario happened: clusters that found no free SM started
+            # only when the occupier (about 0.08 ms) let go of its SMs
+            ref = recs[0].t_mma_start
+            first = {}
+            for i in range(int(info.work_items)):
+                r = recs[i]
+                if r.visits:
+                    t = ((r.t_mma_start - ref + (1 << 31)) & 0xFFFFFFFF) - (1 << 31)   # wrap-safe, ns
+                    first[r.owner] = min(first.get(r.owner, t), t)
+            assert max(first.values()) - min(first.values()) > 20_000, "no cluster waited for the occupier"
+        assert compare_sampled(xm, Cm, info.tile_m, info.tile_n, what="under a half-GPU occupier") <= TOL[pm.dtype]
+        assert compare_sampled(xo, Co, 128, 256, what="the occupier") <= TOL[po.dtype]
+    finally:
+        pts.gemm_destroy(ho)
+        pts.gemm_destroy(hm)
+
+
 # ------------------------------------------------------------ bounded waits
 
 @pytest.mark.parametrize("shape", list(SHAPES))
