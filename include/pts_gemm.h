@@ -210,7 +210,10 @@ gemm_status_t gemm_create(gemm_handle_t *out, int device, const gemm_opts_t *opt
  * flags it used at zero, so a replay starts exactly like a fresh launch.
  * The workspace is grown (cudaMalloc, cudaMemset) by the first call that
  * needs more than the handle holds, which a capturing stream does not allow:
- * make one call of the same shape before capturing. */
+ * make one call of the same shape before capturing.  That growth may also
+ * wait for work already queued on other streams of the device, so a call that
+ * should overlap another stream's kernels is best preceded by one of the same
+ * shape. */
 gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        const void *A, const void *B, void *C,
                        gemm_dtype_t dtype, gemm_sched_t sched,
