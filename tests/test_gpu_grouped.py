@@ -177,6 +177,8 @@ def test_grouped_empty_lists_launch_nothing(handles):
     assert info.tiles == 0 and info.grid_ctas == 0
 
 
+# the capture below is meant to stay empty (the call refuses a capturing stream)
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_grouped_invalid_arguments(handles):
     h, _, _ = handles
     lib = pts.load()
