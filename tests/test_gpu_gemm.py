@@ -480,6 +480,25 @@ def test_long_and_skinny_problems(shape):
         pts.gemm_destroy(h)
 
 
+MANY = [(262144, 24, 64, wl.BF16), (16, 131072, 64, wl.F16), (65536, 40, 128, wl.E4M3)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", MANY, ids=[f"{m}x{n}x{k}-{wl.DTYPE_NAMES[d]}" for m, n, k, d in MANY])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_many_tiles_along_one_dimension(handle, shape, sched):
+    """Thousands of tiles along M (one tile column) or hundreds to a thousand
+    along N (one tile row): the grouped order crosses hundreds of group
+    boundaries or keeps one short group, non-persistent grids of thousands of
+    clusters, static strides over many waves.  Every work item's record is
+    checked against the scheduler model; outputs on a sample."""
+    h, _ = handle
+    M, N, K, dt = shape
+    dist = "normal" if dt == wl.E4M3 else "normal_sqrtk"
+    x = wl.make_inputs(wl.Problem("many", M, N, K, dt, dist, M + 3 * N + K))
+    _run_checked(h, x, sched, full=False)
+
+
 # ---------------------------------------------------------------- full sizes
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
