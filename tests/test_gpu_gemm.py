@@ -643,22 +643,10 @@ def test_gemm_started_while_another_holds_half_the_sms(sched):
         pts.gemm_run(ho, po.M, po.N, po.K, Ao, Bo, Co, po.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s_occ)
         pts.gemm_run(hm, pm.M, pm.N, pm.K, Am, Bm, Cm, pm.dtype, sched, 1.0, 1.0, s_main)
         torch.cuda.synchronize()
-        Co.fill_(float("nan"))
-        Cm.fill_(float("nan"))
-        torch.cuda.synchronize()
-        pts.gemm_run(ho, po.M, po.N, po.K, Ao, Bo, Co, po.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s_occ)
-        t0 = time.perf_counter()
-        while time.perf_counter() - t0 < 25e-6:   # let the occupier's CTAs become resident
-            pass
-        pts.gemm_run(hm, pm.M, pm.N, pm.K, Am, Bm, Cm, pm.dtype, sched, 1.0, 1.0, s_main)
-        torch.cuda.synchronize()
-        assert pts.gemm_check(ho, s_occ)[0] == 0
-        st, recs, dev = pts.gemm_read_debug(hm, int(info.work_items), s_main)
-        assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
-        check_records(recs, info, sched, pm.K)
-        if sched == pts.GEMM_SCHED_STATIC:
-            # the scenario happened: clusters that found no free SM started
-            # only when the occupier (about 0.08 ms) let go of its SMs
+
+        def waited(recs):
+            # the static grid's clusters that found no free SM started only when
+            # the occupier (about 0.07 ms) let go of its SMs
             ref = recs[0].t_mma_start
             first = {}
             for i in range(int(info.work_items)):
@@ -666,7 +654,26 @@ def test_gemm_started_while_another_holds_half_the_sms(sched):
                 if r.visits:
                     t = ((r.t_mma_start - ref + (1 << 31)) & 0xFFFFFFFF) - (1 << 31)   # wrap-safe, ns
                     first[r.owner] = min(first.get(r.owner, t), t)
-            assert max(first.values()) - min(first.values()) > 20_000, "no cluster waited for the occupier"
+            return max(first.values()) - min(first.values()) > 20_000
+
+        for attempt in range(3):   # the host's 25 us spin can overrun (the occupier is then done)
+            Co.fill_(float("nan"))
+            Cm.fill_(float("nan"))
+            torch.cuda.synchronize()
+            pts.gemm_run(ho, po.M, po.N, po.K, Ao, Bo, Co, po.dtype, pts.GEMM_SCHED_STATIC, 1.0, 1.0, s_occ)
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < 25e-6:   # let the occupier's CTAs become resident
+                pass
+            pts.gemm_run(hm, pm.M, pm.N, pm.K, Am, Bm, Cm, pm.dtype, sched, 1.0, 1.0, s_main)
+            torch.cuda.synchronize()
+            assert pts.gemm_check(ho, s_occ)[0] == 0
+            st, recs, dev = pts.gemm_read_debug(hm, int(info.work_items), s_main)
+            assert st == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
+            check_records(recs, info, sched, pm.K)
+            if sched != pts.GEMM_SCHED_STATIC or waited(recs):
+                break
+        if sched == pts.GEMM_SCHED_STATIC:
+            assert waited(recs), "no cluster waited for the occupier"
         assert compare_sampled(xm, Cm, info.tile_m, info.tile_n, what="under a half-GPU occupier") <= TOL[pm.dtype]
         assert compare_sampled(xo, Co, 128, 256, what="the occupier") <= TOL[po.dtype]
     finally:
