@@ -734,11 +734,59 @@ def extra_configs(pts, dev, stream):
         out["half_occupied"] = half_occupied(pts, dev, stream)
         out["bf16_grouped_vark"] = grouped_vark(pts, dev, stream)
         out["fp16_4096_ksweep_one_grouped_launch"] = sweep_as_grouped(pts, dev, stream)
+        out["fp16_4096_tile_plans"] = tile_plans_small_k(pts, dev, stream)
     finally:
         pts.gemm_destroy(h)
-    out["note"] = ("library's CTA group per GEMM (pairs from 14 k-blocks per tile); median of back-to-back "
+    out["note"] = ("library's CTA group per GEMM (pairs from 14 k-blocks per tile for the persistent "
+                   "schedulers, from 64 for the non-persistent grid); median of back-to-back "
                    "launches; inputs generated on the GPU from seeded generators (parity for these shapes is in "
                    "the tests)")
+    return out
+
+
+def tile_plans_small_k(pts, dev, stream, ks=(128, 256, 512, 1024), n=20, nbuf=4):
+    """The fp16 4096^2 sweep's small-K end under each tile plan the library
+    has: the wide 128x256 tile as single CTAs and as CTA pairs (256x256), the
+    narrow 128x128 tile as single CTAs (two per SM) and as CTA pairs (256x128,
+    one CTA per SM), and the library's own choice.  Per scheduler, microseconds
+    per launch over `n` chained launches on `nbuf` rotating buffer sets; the
+    stream-K share off in the fixed plans, so that they differ in the tile
+    alone."""
+    plans = {"wide_cg1": dict(cta_group=1, tile_n=256, split_k=-1),
+             "wide_cg2": dict(cta_group=2, tile_n=256, split_k=-1),
+             "narrow_cg1": dict(cta_group=1, tile_n=128),
+             "narrow_cg2": dict(cta_group=2, tile_n=128),
+             "library": {}}
+    out = {"K": list(ks)}
+    for name in plans:
+        out[name] = {sn: [] for sn in SCHED_NAMES}
+    for K in ks:
+        p = wl.fp16_4096_ksweep([K])[0]
+        ins = [device_inputs(p, 9500 + 10 * K + i) for i in range(nbuf)]
+        Cs = [torch.empty(p.M, p.N, dtype=torch.float16, device="cuda") for _ in range(nbuf)]
+        for name, kw in plans.items():
+            h = pts.gemm_create(dev, pts.make_opts(**kw))
+            try:
+                for si, sn in enumerate(SCHED_NAMES):
+                    def run(i):
+                        A, B, _, _ = ins[i % nbuf]
+                        pts.gemm_run(h, p.M, p.N, p.K, A, B, Cs[i % nbuf], p.dtype, si, 1.0, 1.0, stream)
+                    for i in range(3):
+                        run(i)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for i in range(n):
+                        run(i)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if pts.gemm_check(h, stream)[0] != 0:
+                        raise RuntimeError(f"device error in the tile-plan sweep ({name}, K={K})")
+                    out[name][sn].append(round(e0.elapsed_time(e1) / n * 1e3, 2))
+            finally:
+                pts.gemm_destroy(h)
+        del ins, Cs
+    out["note"] = (f"microseconds per launch, {n} chained launches on {nbuf} rotating buffer sets; "
+                   "wide = 128x256 per CTA, narrow = 128x128 per CTA; cg2 = CTA pairs")
     return out
 
 
@@ -996,7 +1044,8 @@ def main():
     ap.add_argument("--ks", type=int, nargs="*", default=None, help="subset of the sweep's K values")
     ap.add_argument("--scheds", nargs="*", default=SCHED_NAMES, choices=SCHED_NAMES)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2],
-                    help="0 = the library's choice per GEMM (single CTAs below 14 k-blocks per tile)")
+                    help="0 = the library's choice per GEMM (single CTAs below 14 k-blocks per tile, "
+                         "below 64 for the non-persistent grid)")
     ap.add_argument("--split-k", type=int, default=0, choices=[0, 1, -1],
                     help="stream-K share of the last waves: 0 = the library's choice, 1 = always, -1 = never")
     ap.add_argument("--epilogue", type=int, default=0, choices=[0, 1, 2],

@@ -77,7 +77,9 @@ typedef enum {
 
 typedef struct gemm_opts {
     int cta_group;                  /* 1 (128x256 tile per CTA) or 2 (256x256 per CTA pair);
-                                       0 = per call: pairs when a tile has >= 14 k-blocks */
+                                       0 = per call: pairs when a tile has >= 14 k-blocks
+                                       (the persistent schedulers) or >= 64 (the
+                                       non-persistent grid) */
     int group_size_m;               /* tile-rows per group of the tile order; 0 = 8 */
     int stages;                     /* shared-memory ring depth in stages (a stage holds one
                                        k-block for single CTAs, two for CTA pairs); 0 = the

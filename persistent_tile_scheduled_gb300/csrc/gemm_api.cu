@@ -13,7 +13,7 @@
 
 #include "../../include/pts_gemm.h"
 #include "gemm_launch.h"
-#include "gemm_params.h"
+#include "gemm_plan.h"
 
 namespace {
 
@@ -210,7 +210,8 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
                                 : (forced_wide_only ? pts::kTileN
                                                     : pts::choose_tile_n(pl.num_kb, h->opts.cta_group, int(sched)));
     pl.cg = pl.bn == pts::kTileNNarrow ? (h->opts.cta_group == 2 ? 2 : 1)
-                                        : (h->opts.cta_group != 0 ? h->opts.cta_group : pts::choose_cta_group(pl.num_kb));
+                                        : (h->opts.cta_group != 0 ? h->opts.cta_group
+                                                                  : pts::choose_cta_group(pl.num_kb, int(sched)));
     const int64_t tile_m = int64_t(pts::kRowsPerCta) * pl.cg;
     pl.tiles_m = (M + tile_m - 1) / tile_m;
     pl.tiles_n = (N + pl.bn - 1) / pl.bn;

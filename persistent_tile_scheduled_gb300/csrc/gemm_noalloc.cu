@@ -17,7 +17,7 @@
 
 #include "../../include/pts_gemm.h"
 #include "gemm_launch.h"
-#include "gemm_params.h"
+#include "gemm_plan.h"
 
 namespace {
 

@@ -113,17 +113,6 @@ constexpr int kPartialFloats = kRowsPerCta * kTileN;
 // whole tiles that follow.
 constexpr int kSkMaxPieces = 3;      // record slots per stream-K unit
 constexpr int kSkMaxParts = 2;       // pieces per tile
-// Use it when it saves each cluster at least this many k-blocks' time.  The
-// price, measured on GB300 (fp16 4096^2, CTA pairs, per-item records): a
-// writer piece's epilogue takes 5.5-5.8 us against 1.1-1.5 us for a whole
-// tile (its 128 KB fp32 partial per CTA; staging that partial through shared
-// memory and bulk copies measured slower still, 6.9-7.7 us), a reader's
-// 3.5-4.7 us; hidden behind a long next tile, not behind a short one.
-// Chained launches, without / with the share: K = 1536 (24 k-blocks, 15 saved
-// per cluster) 38.2 / 38.8 us, K = 1792 (28, 18 saved) 42.5 / 43.2, K = 2048
-// (32, 20 saved) 48.7 / 48.1, K = 3072 68.6 / 64.8, K = 4096 91.2 / 84.2.
-constexpr int kSkMinSavedKb = 20;
-
 __host__ __device__ inline int64_t sk_unit_begin(int64_t c, int64_t L, int64_t U) { return c * L / U; }
 
 // The unit whose range holds k-block x of the region: the largest c with
@@ -137,88 +126,12 @@ __host__ __device__ inline int sk_pieces(int64_t c, int64_t L, int64_t U, int64_
     return static_cast<int>((b - 1) / num_kb - a / num_kb + 1);
 }
 
-// Tiles in the stream-K region for `tiles` tiles of `num_kb` k-blocks on
-// `resident` clusters (0 = do not use it).  force: 1 = whenever the last wave
-// is partial, -1 = never, 0 = when it saves kSkMinSavedKb k-blocks' time.
-inline int64_t choose_stream_k(int64_t tiles, int64_t resident, int64_t num_kb, int force)
-{
-    if (force < 0 || num_kb < 1 || resident < 1 || tiles < resident) return 0;
-    const int64_t r = tiles % resident;
-    if (r == 0) return 0;
-    if (force == 0 && num_kb * (resident - r) < kSkMinSavedKb * resident) return 0;
-    return r + resident;
-}
-
-// CTA group when the caller leaves it to the library.  CTA pairs (cta_group
-// 2) load a third less per SM for the same MMA work, so their mainloop runs
-// faster under full load, but a pair costs more per launch to start, fill
-// and finish.  Measured on GB300 on fp16 4096^2 with cold inputs (eight
-// buffer sets in turn), single vs pair per launch, without the stream-K
-// share: K = 640 22.9-23.1 vs 24.3-24.5 us, K = 768 25.5 vs 25.7, K = 896
-// 27.8-28.3 vs 27.4-27.5, K = 1152 33.1-33.2 vs 32.7-32.8.  So pairs from
-// 14 k-blocks per tile.
-constexpr int kPairMinKb = 14;
-
-inline int choose_cta_group(int64_t num_kb) { return num_kb >= kPairMinKb ? 2 : 1; }
-
-// Column slices per tile for a problem of `tiles` tiles on `resident`
-// clusters.  Only a problem smaller than one wave is sliced (quarters when it
-// fits in a quarter wave, halves when it fits in half): there slicing puts
-// idle SMs to work.  Past one wave the slices' smaller stages leave the
-// latency-bound load pipeline with fewer bytes in flight, and a slice takes
-// nearly as long as a whole tile, so later waves are not sliced.
-inline int choose_split(int64_t tiles, int64_t resident)
-{
-    if (tiles >= resident) return 1;
-    if (4 * tiles <= resident) return 4;
-    if (2 * tiles <= resident) return 2;
-    return 1;
-}
-
-// CTAs per SM: the wide tile's ring and staging take nearly all of an SM's
-// shared memory; the narrow tile's fit twice (two stages of 32 KB, 32 KB of
-// epilogue staging, about 97 KB per CTA), and its accumulators take 256 of
-// the SM's 512 TMEM columns.  A second resident CTA gives the SM a second,
-// independent load -> MMA -> epilogue pipeline: while one CTA waits for its
-// operands or drains its output, the other computes.  That pays where tiles
-// are short (few k-blocks) and the per-tile latencies dominate; for long
-// tiles the narrow tile's two-stage ring and its 4/3 times higher operand
-// traffic per flop lose to the wide tile.  ("[Persistent] Performance on
-// 09-persistent-matmul on A100 worse than non-persistent": the best
-// persistent configuration there was 128x128x64 tiles with twice as many
-// programs as SMs.)
-//
-// Measured on GB300 (fp16 4096^2, 40 chained launches per point, microseconds
-// per launch; wide = 128 x 256 single CTAs, narrow = 128 x 128, two per SM):
-//   K     static wide / narrow   CLC wide / narrow   non-persistent wide / narrow
-//   128   11.8 / 11.8            12.9 / 11.8         23.5 / 20.8
-//   256   13.1 / 16.8            13.6 / 16.6         26.2 / 25.3
-//   512   19.5 / 24.2            19.4 / 24.1         31.5 / 32.7
-//   1024  29.6 / 38.9            29.7 / 39.0         41.9 / 47.0
-// The persistent grids gain nothing: at small K a launch is bound by the
-// latency of its operand loads, and the SM's operands in flight are what
-// sets the pace -- four 48 KB stages for the wide tile, 2 x 2 stages of 32 KB
-// for the narrow pair -- so the narrow tile ties at 2 k-blocks and loses
-// beyond.  The non-persistent grid, which starts a CTA per tile, gains from
-// two CTAs per SM up to 4 k-blocks.
-//
-// The narrow tile also comes as a CTA pair (256 x 128 per pair, tcgen05
-// cta_group::2), but at one CTA per SM, with the deepest ring that fits: the
-// two CTAs of a pair then sit on two SMs by construction.  Nothing available
-// here documents where the hardware puts a pair's two CTAs when one SM could
-// hold both, and a pair's MMA cannot run with both on one SM, so pairs are
-// never given a second CTA per SM.
+// CTAs per SM: one for the wide tile and for any CTA pair; two for the narrow
+// single CTA, whose ring, staging and accumulators fit twice in an SM (why
+// pairs never get two, and when the library uses the narrow tile, is with
+// choose_tile_n in gemm_plan.h).
 __host__ __device__ constexpr int ctas_per_sm(int cg, int bn) { return (bn == kTileNNarrow && cg == 1) ? 2 : 1; }
 constexpr int kNarrowStages = 2;        // ring stages of the narrow single CTA
-// Narrow tiles when the caller leaves both the tile and the CTA group to the
-// library: for the non-persistent grid (sched 0) on tiles of at most this
-// many k-blocks.
-constexpr int kNarrowMaxKb = 4;
-
-inline int choose_tile_n(int64_t num_kb, int cta_group_opt, int sched)
-{
-    return (cta_group_opt == 0 && sched == SCHED_NONPERSISTENT && num_kb <= kNarrowMaxKb) ? kTileNNarrow : kTileN;
-}
 
 // K-blocks per ring stage.  A stage's fixed costs (its barrier waits, the
 // expect-tx arrival, the commit that frees it) are paid once per stage, so a

@@ -232,7 +232,8 @@ def test_automatic_stream_k_share():
 
 
 def test_automatic_cta_group():
-    """CTA pairs from 14 k-blocks per tile, single CTAs below."""
+    """CTA pairs from 14 k-blocks per tile for the persistent schedulers, from
+    64 for the non-persistent grid; single CTAs below."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=0))
     try:
         assert pts.gemm_query(h, 4096, 4096, 512, pts.GEMM_F16, 1).cta_group == 1      # 8 k-blocks
@@ -241,6 +242,16 @@ def test_automatic_cta_group():
         assert pts.gemm_query(h, 4096, 4096, 8192, pts.GEMM_BF16, 1).cta_group == 2    # 128
         assert pts.gemm_query(h, 8192, 8192, 1664, pts.GEMM_E4M3, 1).cta_group == 1    # 13 (128-wide k-blocks)
         assert pts.gemm_query(h, 8192, 8192, 1792, pts.GEMM_E4M3, 1).cta_group == 2    # 14
+        assert pts.gemm_query(h, 4096, 4096, 840, pts.GEMM_F16, 2).cta_group == 2      # CLC as static
+        NP = pts.GEMM_SCHED_NONPERSISTENT
+        assert pts.gemm_query(h, 4096, 4096, 1024, pts.GEMM_F16, NP).cta_group == 1    # 16
+        assert pts.gemm_query(h, 4096, 4096, 4032, pts.GEMM_F16, NP).cta_group == 1    # 63
+        assert pts.gemm_query(h, 4096, 4096, 4096, pts.GEMM_F16, NP).cta_group == 2    # 64
+        assert pts.gemm_query(h, 8192, 8192, 8192, pts.GEMM_BF16, NP).cta_group == 2   # 128
+        x1 = wl.custom(640, 1000, 2048, wl.F16, "normal_sqrtk", 13)                   # 32: single CTAs
+        C1 = run_device(h, x1, NP)
+        assert pts.gemm_check(h)[0] == 0
+        assert compare_full(x1, C1) <= TOL[wl.F16]
         x = wl.custom(640, 1000, 8192, wl.BF16, "normal_sqrtk", 12)
         C = run_device(h, x, pts.GEMM_SCHED_CLC)
         assert pts.gemm_check(h)[0] == 0

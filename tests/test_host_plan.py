@@ -1,4 +1,4 @@
-"""The launch plan's host-side rules (csrc/gemm_params.h), compiled for the
+"""The launch plan's host-side rules (csrc/gemm_plan.h, csrc/gemm_params.h), compiled for the
 host and checked on the CPU: the stream-K partition helpers against the
 scheduler model (oracle/sched.py, which writes the partition out k-block by
 k-block), and the thresholds and shared-memory budget the launcher uses."""
@@ -20,7 +20,7 @@ CASES = [(5, 3, 4), (7, 3, 1), (104, 76, 64), (256, 76, 64), (300, 152, 5), (31,
 
 PROGRAM = r"""
 #include <cstdio>
-#include "gemm_params.h"
+#include "gemm_plan.h"
 using namespace pts;
 int main() {
     const long long cases[][3] = {%CASES%};
@@ -46,7 +46,12 @@ int main() {
         printf("%s[%lld, %lld, %d]", i ? ", " : "", sp[i][0], sp[i][1], choose_split(sp[i][0], sp[i][1]));
     printf("], \"cta_group\": [");
     for (int kb = 1; kb <= 40; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb));
-    printf("], \"pair_min_kb\": %d, \"sk_min_saved_kb\": %d", kPairMinKb, kSkMinSavedKb);
+    printf("], \"cta_group_np\": [");
+    for (int kb = 1; kb <= 80; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb, SCHED_NONPERSISTENT));
+    printf("], \"cta_group_clc\": [");
+    for (int kb = 1; kb <= 40; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb, SCHED_CLC));
+    printf("], \"pair_min_kb\": %d, \"pair_min_kb_np\": %d, \"sk_min_saved_kb\": %d", kPairMinKb,
+           kPairMinKbNonPersistent, kSkMinSavedKb);
     printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]", kb_per_stage(1), kb_per_stage(2),
            smem_bytes(1, 4), smem_bytes(2, 3), smem_bytes(1, 5));
     printf(", \"narrow\": {\"smem\": %d, \"smem3\": %d, \"stages\": %d, \"per_sm\": [%d, %d, %d, %d], "
@@ -120,6 +125,11 @@ def test_slices_and_cta_group_thresholds(plan):
         assert split == want, (tiles, resident)
     k = plan["pair_min_kb"]
     assert plan["cta_group"] == [2 if kb >= k else 1 for kb in range(1, 41)]
+    assert plan["cta_group_clc"] == plan["cta_group"]
+    # the non-persistent grid keeps single CTAs much longer (a pair cluster per tile costs more)
+    knp = plan["pair_min_kb_np"]
+    assert knp > k
+    assert plan["cta_group_np"] == [2 if kb >= knp else 1 for kb in range(1, 81)]
 
 
 def test_shared_memory_budget(plan):
