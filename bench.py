@@ -256,11 +256,11 @@ def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_g
     total_ms = ev[0].elapsed_time(ev[steps])
     # per-K breakdown (outside the timed region): an event around every GEMM.
     # The pass starts behind one untimed GEMM, so that the first timed launch
-    # does not also pay for waking an idle stream; three passes, the median
-    # per K.
+    # does not also pay for waking an idle stream; seven passes, the median
+    # per K (a launch of 15-20 us timed alone varies by 10 % from pass to pass).
     n = len(problems)
     passes = []
-    for _ in range(3):
+    for _ in range(7):
         kev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         with torch.cuda.stream(stream):
             p0, (A0, B0, C0) = problems[-1], bufs[-1]
