@@ -106,9 +106,9 @@ typedef struct gemm_opts {
     int group_order;                /* gemm_run_grouped's order of the problems in the work-id
                                        list: 0 = default (1); 1 = most k-blocks first (stable:
                                        equal K keep the given order); 2 = as given */
-    int tile_n;                     /* output tile columns of gemm_run: 0 = per call (128 when
-                                       cta_group is 0 and a tile has <= 4 k-blocks under the
-                                       non-persistent scheduler or <= 2 under CLC, else 256);
+    int tile_n;                     /* output tile columns of gemm_run: 0 = per call (128 for the
+                                       non-persistent scheduler when a tile has <= 4 k-blocks and
+                                       cta_group is 0, else 256);
                                        256 = the wide tile (one CTA, or CTA pair, per SM);
                                        128 = the narrow tile: 128 x 128 per CTA; with cta_group
                                        0 or 1 single CTAs, two resident per SM; with cta_group 2

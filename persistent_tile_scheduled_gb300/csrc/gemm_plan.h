@@ -110,20 +110,17 @@ inline int choose_split(int64_t tiles, int64_t resident)
 // library: for the non-persistent grid (sched 0) on tiles of at most this
 // many k-blocks.
 constexpr int kNarrowMaxKb = 4;
-// and for CLC on tiles of at most this many: with two CTAs per SM, one
-// computes while the other waits for its claim's response, which on tiles
-// this short is a large share of a tile.  Measured on GB300 (fp16 4096^2 x
-// 128, chained launches, wide / narrow, us): CLC 12.9 / 11.8 and 13.9 / 12.4
-// on two boxes, static 11.8 / 11.8 and 12.9 / 13.0; at K = 256 CLC 13.6 /
-// 16.6 and 14.8 / 18.0.
-constexpr int kNarrowMaxKbClc = 2;
+// CLC is left on the wide tile even at 2 k-blocks, where the narrow tile's
+// second CTA per SM hides the claim latency (fp16 4096^2 x 128, chained
+// launches of that one shape, wide / narrow: 12.9 / 11.8 and 13.9 / 12.4 us on
+// two boxes): in a sequence of GEMMs of different K, the first wide-tile launch
+// after a narrow one pays about 3 us for the change of kernel, which takes the
+// gain back (measured in the K sweep: CLC at K = 256 went from 436-442 to 381
+// TFLOP/s when K = 128 before it took the narrow tile).
 
 inline int choose_tile_n(int64_t num_kb, int cta_group_opt, int sched)
 {
-    if (cta_group_opt != 0) return kTileN;
-    if (sched == SCHED_NONPERSISTENT && num_kb <= kNarrowMaxKb) return kTileNNarrow;
-    if (sched == SCHED_CLC && num_kb <= kNarrowMaxKbClc) return kTileNNarrow;
-    return kTileN;
+    return (cta_group_opt == 0 && sched == SCHED_NONPERSISTENT && num_kb <= kNarrowMaxKb) ? kTileNNarrow : kTileN;
 }
 
 }  // namespace pts

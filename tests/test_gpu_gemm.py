@@ -372,19 +372,17 @@ def test_narrow_tile_runs_two_ctas_on_one_sm(sched):
 
 def test_automatic_tile_choice():
     """With the shape left to the library, the non-persistent grid takes the
-    narrow tile for tiles of at most 4 k-blocks and CLC for tiles of at most
-    2; static, and a caller that fixes the CTA group, get the wide tile."""
+    narrow tile for tiles of at most 4 k-blocks; the persistent grids, and a
+    caller that fixes the CTA group, get the wide tile."""
     h = pts.gemm_create(0, pts.make_opts())
     h1 = pts.gemm_create(0, pts.make_opts(cta_group=1))
     try:
-        for dt, K, np_narrow, clc_narrow in ((wl.F16, 128, True, True), (wl.F16, 136, True, False),
-                                             (wl.F16, 256, True, False), (wl.F16, 320, False, False),
-                                             (wl.E4M3, 256, True, True), (wl.E4M3, 512, True, False),
-                                             (wl.E4M3, 640, False, False), (wl.BF16, 4096, False, False)):
+        for dt, K, narrow in ((wl.F16, 128, True), (wl.F16, 256, True), (wl.F16, 320, False),
+                              (wl.E4M3, 512, True), (wl.E4M3, 640, False), (wl.BF16, 4096, False)):
             info = pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_NONPERSISTENT)
-            assert info.tile_n == (128 if np_narrow else 256), (dt, K)
-            assert pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_CLC).tile_n == (128 if clc_narrow else 256)
-            assert pts.gemm_query(h, 4096, 4096, K, dt, pts.GEMM_SCHED_STATIC).tile_n == 256
+            assert info.tile_n == (128 if narrow else 256), (dt, K)
+            for sched in (pts.GEMM_SCHED_STATIC, pts.GEMM_SCHED_CLC):
+                assert pts.gemm_query(h, 4096, 4096, K, dt, sched).tile_n == 256
             for sched in SCHEDS:
                 assert pts.gemm_query(h1, 4096, 4096, K, dt, sched).tile_n == 256
     finally:

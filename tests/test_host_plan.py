@@ -145,9 +145,9 @@ def test_narrow_tile_rules(plan):
     with the 1 KB each CTA reserves (a third stage would not); its pair form
     runs one CTA per SM, with a ring of four two-k-block stages (48 KB each:
     128 rows of A and 64 of B per k-block) in the 227 KB a CTA may use (a fifth
-    would not fit); the library picks the narrow tile only when the CTA group
-    is left to it (so never the pair form): for the non-persistent grid on
-    tiles of at most 4 k-blocks, for CLC on tiles of at most 2."""
+    would not fit); the library picks the narrow tile only for the
+    non-persistent grid, on tiles of at most 4 k-blocks, when the CTA group is
+    left to it (so never the pair form)."""
     n = plan["narrow"]
     assert n["stages"] == 2 and n["per_sm"] == [1, 1, 2, 1]
     assert 2 * (n["smem"] + 1024) <= 233472 < 2 * (n["smem3"] + 1024)
@@ -156,5 +156,5 @@ def test_narrow_tile_rules(plan):
     assert five - four == 2 * (128 + 64) * 128
     assert n["max_kb"] == 4
     for kb, cg, sched, tile in n["tile"]:
-        want = 128 if (cg == 0 and ((sched == 0 and kb <= 4) or (sched == 2 and kb <= 2))) else 256
+        want = 128 if (cg == 0 and sched == 0 and kb <= 4) else 256
         assert tile == want, (kb, cg, sched)
