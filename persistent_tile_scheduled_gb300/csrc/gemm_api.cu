@@ -68,11 +68,11 @@ struct gemm_ctx {
     cudaEvent_t ev_tab[kGroupSlots] = {};
     int tab_cur = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    // per dtype and kernel variant (0: wide tile, single CTAs; 1: wide, pairs; 2: narrow tile,
-    // single CTAs; 3: narrow tile, pairs)
-    bool smem_set[3][4] = {};
-    int occ_smem[3][4] = {};                  // smem the cached occupancy was computed for
-    int occ_clusters[3][4] = {};
+    // per dtype, kernel variant (0: wide tile, single CTAs; 1: wide, pairs; 2: narrow tile,
+    // single CTAs; 3: narrow tile, pairs) and build (0: the common launch's kernel, 1: full)
+    bool smem_set[3][4][2] = {};
+    int occ_smem[3][4][2] = {};               // smem the cached occupancy was computed for
+    int occ_clusters[3][4][2] = {};
     MapEntry maps[kMapCache];
 };
 
@@ -124,14 +124,16 @@ const CUtensorMap *get_map(gemm_ctx *h, const void *ptr, uint64_t rows, uint64_t
 // tile, single CTAs; 3 narrow tile, CTA pairs.
 int variant_of(int cg, int bn) { return (bn == pts::kTileNNarrow ? 2 : 0) + cg - 1; }
 
-pts::KernelOps ops_for(int kind, int cg, int bn)
+pts::KernelOps ops_for(int kind, int cg, int bn, bool full)
 {
-    if (bn == pts::kTileNNarrow) return cg == 2 ? pts::kernel_ops_narrow_cg2(kind) : pts::kernel_ops_narrow(kind);
-    return cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind);
+    if (bn == pts::kTileNNarrow)
+        return cg == 2 ? pts::kernel_ops_narrow_cg2(kind, full) : pts::kernel_ops_narrow(kind, full);
+    return cg == 2 ? pts::kernel_ops_cg2(kind, full) : pts::kernel_ops_cg1(kind, full);
 }
 
 struct Plan {
     int cg, bn = pts::kTileN, stages, smem;
+    bool full = true;        // the kernel with every feature, or the common launch's (see kernel_full)
     int64_t tiles_m, tiles_n, tiles;
     int split;               // column slices per tile (1, 2 or 4)
     int64_t sk_tiles;        // stream-K region: its tiles and units (0 = none)
@@ -172,21 +174,32 @@ gemm_status_t kernel_shape(gemm_ctx *h, gemm_dtype_t dtype, Plan &pl)
     if (pl.smem > h->max_smem_optin) return GEMM_ERR_INVALID_ARG;
     const int kind = static_cast<int>(dtype);
     const int ci = variant_of(pl.cg, pl.bn);
-    pts::KernelOps ops = ops_for(kind, pl.cg, pl.bn);
-    if (!h->smem_set[kind][ci]) {
+    const int fi = pl.full ? 1 : 0;
+    pts::KernelOps ops = ops_for(kind, pl.cg, pl.bn, pl.full);
+    if (!h->smem_set[kind][ci][fi]) {
         if (ops.set_smem(h->max_smem_optin) != cudaSuccess) return cuda_fail(cudaErrorInvalidValue);
-        h->smem_set[kind][ci] = true;
+        h->smem_set[kind][ci][fi] = true;
     }
-    if (h->occ_smem[kind][ci] != pl.smem) {
+    if (h->occ_smem[kind][ci][fi] != pl.smem) {
         int n = 0;
         if (ops.max_active_clusters(pl.smem, &n) != cudaSuccess) return cuda_fail(cudaErrorInvalidValue);
-        h->occ_smem[kind][ci] = pl.smem;
-        h->occ_clusters[kind][ci] = n;
+        h->occ_smem[kind][ci][fi] = pl.smem;
+        h->occ_clusters[kind][ci][fi] = n;
     }
-    pl.max_active_clusters = h->occ_clusters[kind][ci];
+    pl.max_active_clusters = h->occ_clusters[kind][ci][fi];
     if (pl.max_active_clusters < 1) return GEMM_ERR_CUDA;
     pl.ctas_per_sm = static_cast<int>((int64_t(pl.max_active_clusters) * pl.cg + h->sm_count - 1) / h->sm_count);
     return GEMM_OK;
+}
+
+// Whether a launch needs the kernel built with every feature: debug records
+// or test hooks, the direct-store epilogue or an L2 prefetch distance (a
+// grouped launch always does).  Otherwise it runs the common launch's kernel,
+// which has those paths compiled out and starts faster.
+bool kernel_full(const gemm_ctx *h)
+{
+    const int prefetch = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
+    return h->opts.debug_flags != 0 || h->opts.epilogue == 2 || prefetch > 0;
 }
 
 int64_t resident_clusters(const gemm_ctx *h, const Plan &pl)
@@ -217,6 +230,7 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     pl.tiles_n = (N + pl.bn - 1) / pl.bn;
     pl.tiles = pl.tiles_m * pl.tiles_n;
     if (pl.tiles > (int64_t(1) << 30)) return GEMM_ERR_INVALID_ARG;
+    pl.full = kernel_full(h);
     gemm_status_t st = kernel_shape(h, dtype, pl);
     if (st != GEMM_OK) return st;
     int64_t resident = resident_clusters(h, pl);
@@ -358,7 +372,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     h->last_sk_units = pl.sk_units;
     h->last_num_kb = pl.num_kb;
 
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn)
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn, pl.full)
                         .launch(ma, mb, mc, p, static_cast<int>(pl.grid_ctas), pl.smem, stream,
                                 h->opts.overlap_launch >= 0);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -439,6 +453,7 @@ gemm_status_t plan_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t c
     pl.split = 1;
     pl.sk_tiles = pl.sk_units = 0;
     pl.units = pl.work = tiles;
+    pl.full = true;   // the grouped decoder is one of the features
     gemm_status_t st = kernel_shape(h, dtype, pl);
     if (st != GEMM_OK) return st;
     const int64_t resident = resident_clusters(h, pl);
@@ -566,7 +581,7 @@ gemm_status_t launch_grouped(gemm_ctx *h, const gemm_group_problem_t *q, int64_t
     const CUtensorMap *mb[3] = {&none, &none, &none};
     // A launch right after an upload does not overlap the previous grid: the
     // copy sits between them in the stream.
-    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn)
+    cudaError_t e = ops_for(static_cast<int>(dtype), pl.cg, pl.bn, pl.full)
                         .launch(none, mb, none, p, static_cast<int>(pl.grid_ctas), pl.smem, stream,
                                 h->opts.overlap_launch >= 0 && !uploaded);
     if (e != cudaSuccess) return cuda_fail(e);

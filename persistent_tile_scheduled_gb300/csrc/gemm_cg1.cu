@@ -11,12 +11,12 @@ __global__ void zero_fill_kernel(uint4 *c, long long n16)
         c[t] = make_uint4(0, 0, 0, 0);
 }
 
-KernelOps kernel_ops_cg1(int kind)
+KernelOps kernel_ops_cg1(int kind, bool full)
 {
     switch (kind) {
-    case 0: return Inst<0, 1>::ops();
-    case 1: return Inst<1, 1>::ops();
-    default: return Inst<2, 1>::ops();
+    case 0: return full ? Inst<0, 1, kTileN, true>::ops() : Inst<0, 1, kTileN, false>::ops();
+    case 1: return full ? Inst<1, 1, kTileN, true>::ops() : Inst<1, 1, kTileN, false>::ops();
+    default: return full ? Inst<2, 1, kTileN, true>::ops() : Inst<2, 1, kTileN, false>::ops();
     }
 }
 

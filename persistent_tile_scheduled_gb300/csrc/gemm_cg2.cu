@@ -4,12 +4,12 @@
 
 namespace pts {
 
-KernelOps kernel_ops_cg2(int kind)
+KernelOps kernel_ops_cg2(int kind, bool full)
 {
     switch (kind) {
-    case 0: return Inst<0, 2>::ops();
-    case 1: return Inst<1, 2>::ops();
-    default: return Inst<2, 2>::ops();
+    case 0: return full ? Inst<0, 2, kTileN, true>::ops() : Inst<0, 2, kTileN, false>::ops();
+    case 1: return full ? Inst<1, 2, kTileN, true>::ops() : Inst<1, 2, kTileN, false>::ops();
+    default: return full ? Inst<2, 2, kTileN, true>::ops() : Inst<2, 2, kTileN, false>::ops();
     }
 }
 

@@ -5,7 +5,7 @@
 
 namespace pts {
 
-template <int KIND, int CG, int BN = kTileN>
+template <int KIND, int CG, int BN = kTileN, bool FULL = true>
 struct Inst {
     // Raise the dynamic shared-memory limit, and ask for the largest shared-
     // memory share of the SM's unified L1/shared storage: without that
@@ -14,9 +14,9 @@ struct Inst {
     static cudaError_t set_smem(int smem)
     {
         cudaError_t e =
-            cudaFuncSetAttribute(gemm_kernel<KIND, CG, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(gemm_kernel<KIND, CG, BN, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(gemm_kernel<KIND, CG, BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        return cudaFuncSetAttribute(gemm_kernel<KIND, CG, BN, FULL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                     static_cast<int>(cudaSharedmemCarveoutMaxShared));
     }
 
@@ -73,7 +73,7 @@ struct Inst {
             if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
             if (e == cudaSuccess) e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
             cudaFuncAttributes fa;
-            if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_kernel<KIND, CG, BN>);
+            if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_kernel<KIND, CG, BN, FULL>);
             if (e != cudaSuccess) return e;
             const int by_smem = smem_sm / (smem + static_cast<int>(fa.sharedSizeBytes) + reserved);
             const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;   // allocated per warp in units of 256
@@ -86,7 +86,7 @@ struct Inst {
             *out = per_sm * sms;
             return cudaSuccess;
         }
-        return cudaOccupancyMaxActiveClusters(out, gemm_kernel<KIND, CG, BN>, &cfg);
+        return cudaOccupancyMaxActiveClusters(out, gemm_kernel<KIND, CG, BN, FULL>, &cfg);
     }
 
     static cudaError_t launch(const CUtensorMap &a, const CUtensorMap *const b[3], const CUtensorMap &c,
@@ -95,7 +95,7 @@ struct Inst {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[2];
         fill_config(cfg, attr, grid_ctas, smem, stream, overlap);
-        return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG, BN>, a, *b[0], *b[1], *b[2], c, p);
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, CG, BN, FULL>, a, *b[0], *b[1], *b[2], c, p);
     }
 
     static KernelOps ops() { return KernelOps{&set_smem, &max_active_clusters, &launch}; }

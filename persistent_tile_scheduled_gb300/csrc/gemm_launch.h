@@ -18,13 +18,15 @@ struct KernelOps {
                           const GemmParams &p, int grid_ctas, int smem, cudaStream_t stream, bool overlap);
 };
 
-// kind: 0 fp16, 1 bf16, 2 e4m3
-KernelOps kernel_ops_cg1(int kind);
-KernelOps kernel_ops_cg2(int kind);
+// kind: 0 fp16, 1 bf16, 2 e4m3.  full: the kernel with every feature (grouped
+// launches, debug records, the direct-store epilogue, L2 prefetch, test
+// hooks); else the common launch's kernel, with those compiled out.
+KernelOps kernel_ops_cg1(int kind, bool full);
+KernelOps kernel_ops_cg2(int kind, bool full);
 // the narrow tile: 128 x 128 per CTA, single CTAs, two per SM
-KernelOps kernel_ops_narrow(int kind);
+KernelOps kernel_ops_narrow(int kind, bool full);
 // the narrow tile as CTA pairs: 256 x 128 per pair, one CTA per SM
-KernelOps kernel_ops_narrow_cg2(int kind);
+KernelOps kernel_ops_narrow_cg2(int kind, bool full);
 cudaError_t launch_zero_fill(void *c, long long bytes, cudaStream_t stream);
 
 }  // namespace pts

@@ -4,12 +4,12 @@
 
 namespace pts {
 
-KernelOps kernel_ops_narrow(int kind)
+KernelOps kernel_ops_narrow(int kind, bool full)
 {
     switch (kind) {
-    case 0: return Inst<0, 1, kTileNNarrow>::ops();
-    case 1: return Inst<1, 1, kTileNNarrow>::ops();
-    default: return Inst<2, 1, kTileNNarrow>::ops();
+    case 0: return full ? Inst<0, 1, kTileNNarrow, true>::ops() : Inst<0, 1, kTileNNarrow, false>::ops();
+    case 1: return full ? Inst<1, 1, kTileNNarrow, true>::ops() : Inst<1, 1, kTileNNarrow, false>::ops();
+    default: return full ? Inst<2, 1, kTileNNarrow, true>::ops() : Inst<2, 1, kTileNNarrow, false>::ops();
     }
 }
 

@@ -5,12 +5,12 @@
 
 namespace pts {
 
-KernelOps kernel_ops_narrow_cg2(int kind)
+KernelOps kernel_ops_narrow_cg2(int kind, bool full)
 {
     switch (kind) {
-    case 0: return Inst<0, 2, kTileNNarrow>::ops();
-    case 1: return Inst<1, 2, kTileNNarrow>::ops();
-    default: return Inst<2, 2, kTileNNarrow>::ops();
+    case 0: return full ? Inst<0, 2, kTileNNarrow, true>::ops() : Inst<0, 2, kTileNNarrow, false>::ops();
+    case 1: return full ? Inst<1, 2, kTileNNarrow, true>::ops() : Inst<1, 2, kTileNNarrow, false>::ops();
+    default: return full ? Inst<2, 2, kTileNNarrow, true>::ops() : Inst<2, 2, kTileNNarrow, false>::ops();
     }
 }
 

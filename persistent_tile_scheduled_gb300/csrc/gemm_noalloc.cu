@@ -88,7 +88,7 @@ gemm_status_t setup_device(int dev, const DeviceSetup **out)
         n.stages[cg - 1] = st;
         n.smem[cg - 1] = pts::smem_bytes(cg, st);
         for (int kind = 0; kind < 3; ++kind) {
-            pts::KernelOps ops = cg == 2 ? pts::kernel_ops_cg2(kind) : pts::kernel_ops_cg1(kind);
+            pts::KernelOps ops = cg == 2 ? pts::kernel_ops_cg2(kind, true) : pts::kernel_ops_cg1(kind, true);
             if (ops.set_smem(n.max_smem) != cudaSuccess
                 || ops.max_active_clusters(n.smem[cg - 1], &n.clusters[kind][cg - 1]) != cudaSuccess
                 || n.clusters[kind][cg - 1] < 1) {
@@ -212,7 +212,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
 
     int64_t clusters = work;
     if (sched == GEMM_SCHED_STATIC && clusters > resident) clusters = resident;
-    pts::KernelOps ops = cta_group == 2 ? pts::kernel_ops_cg2(dtype) : pts::kernel_ops_cg1(dtype);
+    pts::KernelOps ops = cta_group == 2 ? pts::kernel_ops_cg2(dtype, true)   // full: it writes coverage records
+                                        : pts::kernel_ops_cg1(dtype, true);
     cudaError_t e = ops.launch(ma, mbs, mc, p, static_cast<int>(clusters * cta_group), s->smem[ci], st, true);
     if (e != cudaSuccess) return fail(e);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);

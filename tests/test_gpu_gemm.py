@@ -309,6 +309,66 @@ def test_run_host_batch_matches_device_path(handle):
         assert torch.equal(w.view(torch.int16), q[5].view(torch.int16))
 
 
+# ------------------------------------------------- the common launch's kernel
+
+COMMON = [(300, 520, 208), (640, 1000, 1040), (2000, 48, 64), (1000, 1800, 2000), (1, 8, 16)]
+
+
+@pytest.mark.parametrize("shape_name", list(SHAPES))
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16, wl.E4M3])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_common_launch_kernel_matches_the_full_one(shape_name, dtype, sched):
+    """A launch that needs none of the debug and extra features runs a kernel
+    built with them compiled out.  It must give the same bits as the full
+    kernel (selected here by asking for debug records) on every tile shape,
+    dtype and scheduler -- ragged shapes, column slices, the stream-K share --
+    and match the oracle."""
+    kw = SHAPES[shape_name]
+    h_common = pts.gemm_create(0, pts.make_opts(**kw))
+    h_full = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS, **kw))
+    try:
+        for M, N, K in COMMON:
+            if dtype == wl.E4M3:
+                K = (K + 15) // 16 * 16
+            dist = "normal" if dtype == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("common", M, N, K, dtype, dist, 31 + M + N + K))
+            C0 = run_device(h_common, x, sched)
+            assert pts.gemm_check(h_common)[0] == 0
+            C1 = run_device(h_full, x, sched)
+            assert pts.gemm_check(h_full)[0] == 0
+            assert torch.equal(C0.view(torch.int16), C1.view(torch.int16)), (shape_name, M, N, K)
+            assert compare_full(x, C0, what="common-launch kernel") <= TOL[dtype]
+    finally:
+        pts.gemm_destroy(h_common)
+        pts.gemm_destroy(h_full)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,arg", [("fp16_4096_ksweep", 128), ("fp16_4096_ksweep", 1024),
+                                      ("fp16_4096_ksweep", 4096), ("bf16_8192_ksweep", 8192), ("e4m3_8192", None)],
+                         ids=["fp16-K128", "fp16-K1024", "fp16-K4096", "bf16-8192", "e4m3-8192"])
+def test_common_launch_kernel_at_full_size(name, arg):
+    """The workloads bench.py times, with the library's defaults: the common
+    launch's kernel gives the bits of the full kernel under every scheduler,
+    and matches the oracle on a sample."""
+    h_common = pts.gemm_create(0, pts.make_opts())
+    h_full = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS))
+    try:
+        x = wl.make_inputs(_full_problem(name, arg))
+        p = x.problem
+        for sched in SCHEDS:
+            C0 = run_device(h_common, x, sched)
+            assert pts.gemm_check(h_common)[0] == 0
+            C1 = run_device(h_full, x, sched)
+            assert pts.gemm_check(h_full)[0] == 0
+            assert torch.equal(C0.view(torch.int16), C1.view(torch.int16)), (name, arg, sched)
+            info = pts.gemm_query(h_common, p.M, p.N, p.K, p.dtype, sched)
+            assert compare_sampled(x, C0, info.tile_m, info.tile_n, what="common-launch kernel") <= TOL[p.dtype]
+    finally:
+        pts.gemm_destroy(h_common)
+        pts.gemm_destroy(h_full)
+
+
 # ------------------------------------------------------------- narrow tile
 
 def test_narrow_tile_keeps_two_ctas_per_sm():
