@@ -254,24 +254,36 @@ def time_sweep(pts, h, bufs, problems, sched, steps, warmup, stream, dist, use_g
     if st != 0:
         raise RuntimeError(f"device status {dev:#x} in the timed region")
     total_ms = ev[0].elapsed_time(ev[steps])
-    # per-K breakdown (outside the timed region): an event around every GEMM.
-    # The pass starts behind one untimed GEMM, so that the first timed launch
-    # does not also pay for waking an idle stream; seven passes, the median
-    # per K (a launch of 15-20 us timed alone varies by 10 % from pass to pass).
+    # per-K breakdown (outside the timed region): every GEMM timed alone, with
+    # an event on each side, right behind an untimed launch of the same shape
+    # on other buffers.  So its kernel is the one that just ran -- the first
+    # launch of a kernel after another one can pay up to about 3 us more (in
+    # the sweep's order about 2 us on the first CTA-pair K) -- while its own
+    # operands are not in L2 (a launch right behind one on the same buffers
+    # would find them there: 2.5 us less at K = 128).  The untimed launch uses the next
+    # problem's buffers (larger K, so large enough) or, for the last, a spare
+    # set.  Seven passes, the median per K (a launch of 15-20 us timed alone
+    # varies by 10 % from pass to pass).
     n = len(problems)
+    pl = problems[-1]
+    spare = (torch.empty_like(bufs[-1][0]), torch.empty_like(bufs[-1][1]), torch.empty_like(bufs[-1][2]))
+    spare[0].copy_(bufs[-1][0])
+    spare[1].copy_(bufs[-1][1])
     passes = []
     for _ in range(7):
-        kev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
-            p0, (A0, B0, C0) = problems[-1], bufs[-1]
-            pts.gemm_run(h, p0.M, p0.N, p0.K, A0, B0, C0, p0.dtype, sched, 1.0, 1.0, stream)
             for i, (p, (A, B, C)) in enumerate(zip(problems, bufs)):
-                kev[i].record(stream)
+                Aw, Bw, Cw = bufs[i + 1] if i + 1 < n else spare
+                pts.gemm_run(h, p.M, p.N, p.K, Aw, Bw, Cw, p.dtype, sched, 1.0, 1.0, stream)
+                kev[i][0].record(stream)
                 pts.gemm_run(h, p.M, p.N, p.K, A, B, C, p.dtype, sched, 1.0, 1.0, stream)
-            kev[n].record(stream)
+                kev[i][1].record(stream)
         torch.cuda.synchronize()
-        passes.append([kev[i].elapsed_time(kev[i + 1]) for i in range(n)])
+        passes.append([a.elapsed_time(b) for a, b in kev])
+    del spare
     per_k = [statistics.median(v) for v in zip(*passes)]
+    assert all(q.M == pl.M and q.N == pl.N and q.K <= pl.K for q in problems)
     return total_ms, per_k, (t0, t1)
 
 
