@@ -85,7 +85,11 @@ typedef struct gemm_opts {
                                        k-block for single CTAs, two for CTA pairs); 0 = the
                                        most that fits (4 and 3) */
     int max_clusters;               /* static scheduler: cap on resident clusters; 0 = occupancy */
-    unsigned debug_flags;           /* GEMM_DEBUG_* */
+    unsigned debug_flags;           /* GEMM_DEBUG_*.  Any debug flag, epilogue 2 or an L2
+                                       prefetch makes gemm_run use the kernel built with every
+                                       feature; without them it uses a build with those paths
+                                       compiled out, which gives the same bits and starts about
+                                       1 us sooner per launch at small K (measured on GB300) */
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
     int split;                      /* column slices: 0 = automatic (a problem smaller than one
