@@ -93,8 +93,11 @@ typedef struct gemm_opts {
     int fault_arg;                  /* argument of GEMM_DEBUG_CLC_STOP_AT / _FAULT_SKIP_TMA */
     unsigned long long timeout_ns;  /* limit of every device-side wait; 0 = 1 s */
     int split;                      /* column slices: 0 = automatic (a problem smaller than one
-                                       wave); 1 = never; 2 or 4 = cut EVERY tile into that many
-                                       column slices (testing) */
+                                       wave; or, with the wide tile and a persistent scheduler,
+                                       the tiles of a partial last wave when they fill at most
+                                       half of it: two column halves each, unless the stream-K
+                                       share is used instead); 1 = never; 2 or 4 = cut EVERY
+                                       tile into that many column slices (testing) */
     int split_k;                    /* stream-K share of the last waves: 0 = automatic (when it
                                        saves time), 1 = whenever the tiles leave a partial last
                                        wave, -1 = never.  Not with split 2 or 4. */
@@ -192,6 +195,10 @@ typedef struct gemm_launch_info {
     int64_t work_items;             /* work items = record slots (gemm_read_debug's n_work) */
     int64_t units;                  /* units the schedulers hand out */
     int ctas_per_sm;                /* CTAs the kernel keeps resident per SM (1 wide, 2 narrow) */
+    int64_t tail_tiles;             /* tiles of the partial last wave run as two column halves
+                                       each (the last in tile order; 0 = none); work ids
+                                       tiles - tail_tiles + 2j and + 2j + 1 are the left and
+                                       right half of tile tiles - tail_tiles + j */
 } gemm_launch_info_t;
 
 typedef struct gemm_ctx *gemm_handle_t;

@@ -54,7 +54,7 @@ Item = Tuple[int, int, int, int, int, int]
 
 
 def work_units(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_tiles: int = 0,
-               sk_units: int = 0) -> List[List[Item]]:
+               sk_units: int = 0, tail_tiles: int = 0) -> List[List[Item]]:
     """The units the schedulers hand out, in unit order, each the list of its
     work items ``(record slot, grouped-order tile, first column, columns,
     first k-block, end k-block)``.
@@ -62,6 +62,9 @@ def work_units(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_ti
     * Whole tiles (``split == 1``, no stream-K region): unit u is tile u.
     * Column slices (``split`` 2 or 4): unit u is columns
       ``(u % split) * tile_n/split`` onwards of tile ``u // split``.
+    * Tail halves (``tail_tiles = R > 0``, whole tiles otherwise): units
+      ``0 .. T-R-1`` are those tiles, whole; then each of the last R tiles
+      comes as two units, its left and then its right half of the columns.
     * Stream-K share (``sk_units = U > 0``): the first ``sk_tiles`` tiles form
       a region of ``L = sk_tiles * num_kb`` k-blocks, tile after tile.  Unit
       ``c < U`` owns the k-blocks ``x`` with ``floor(c*L/U) <= x <
@@ -71,14 +74,16 @@ def work_units(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_ti
       slots ``3U, 3U+1, ...``).  Items are listed in the order a unit runs
       them.
 
-    The pages hand out whole tiles only; the column slices and the stream-K
-    share are the library's additions for the tail of a grid (they change
+    The pages hand out whole tiles only; the column slices, the tail halves
+    and the stream-K share are the library's additions for the tail of a
+    grid (they change
     which cluster computes what, never the result beyond fp32 summation
     order).  The stream-K partition is written out here k-block by k-block,
     not by the closed forms the kernel uses, so the two can be compared.
     """
-    if split not in (1, 2, 4) or (split > 1 and sk_units):
-        raise ValueError((split, sk_units))
+    if split not in (1, 2, 4) or (split > 1 and sk_units) or tail_tiles < 0 \
+            or (tail_tiles and (split > 1 or sk_units or tail_tiles > T)):
+        raise ValueError((split, sk_units, tail_tiles))
     units: List[List[Item]] = []
     if sk_units:
         U, L = sk_units, sk_tiles * num_kb
@@ -105,22 +110,26 @@ def work_units(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_ti
         for u in range(T * split):
             units.append([(u, u // split, (u % split) * step, step, 0, num_kb)])
     else:
-        for u in range(T):
+        for u in range(T - tail_tiles):
             units.append([(u, u, 0, tile_n, 0, num_kb)])
+        half = tile_n // 2
+        for t in range(T - tail_tiles, T):
+            for h in (0, 1):
+                units.append([(len(units), t, h * half, half, 0, num_kb)])
     return units
 
 
 def work_items(T: int, split: int = 1, tile_n: int = 256, num_kb: int = 1, sk_tiles: int = 0,
-               sk_units: int = 0) -> List[Item]:
+               sk_units: int = 0, tail_tiles: int = 0) -> List[Item]:
     """Every work item of :func:`work_units`, in unit order."""
-    return [it for u in work_units(T, split, tile_n, num_kb, sk_tiles, sk_units) for it in u]
+    return [it for u in work_units(T, split, tile_n, num_kb, sk_tiles, sk_units, tail_tiles) for it in u]
 
 
-def record_slots(T: int, split: int = 1, sk_tiles: int = 0, sk_units: int = 0) -> int:
+def record_slots(T: int, split: int = 1, sk_tiles: int = 0, sk_units: int = 0, tail_tiles: int = 0) -> int:
     """Record slots of a launch: three per stream-K unit plus one per other unit."""
     if sk_units:
         return 3 * sk_units + T - sk_tiles
-    return T * split
+    return T * split + tail_tiles
 
 
 def grouped_items(problems, BM: int, BN: int, group_m: int, kb=None) -> List[Tuple[int, int, int]]:

@@ -138,6 +138,7 @@ struct Plan {
     int split;               // column slices per tile (1, 2 or 4)
     int64_t sk_tiles;        // stream-K region: its tiles and units (0 = none)
     int64_t sk_units;
+    int64_t tail = 0;        // last tiles run as two column halves each (0 = none)
     int64_t num_kb;          // k-blocks per whole tile
     int64_t units;           // work ids the schedulers hand out
     int64_t work;            // work items (record slots)
@@ -240,10 +241,13 @@ gemm_status_t make_plan(gemm_ctx *h, int64_t M, int64_t N, int64_t K, gemm_dtype
     if (pl.bn == pts::kTileNNarrow && pl.split > 2) pl.split = 2;
     pl.sk_tiles = 0;
     pl.sk_units = 0;
+    pl.tail = 0;
+    // the partial last wave: column halves of its tiles or the stream-K share
     if (pl.bn == pts::kTileN && pl.split == 1
-        && (pl.sk_tiles = pts::choose_stream_k(pl.tiles, resident, pl.num_kb, h->opts.split_k)) > 0)
+        && (pl.sk_tiles = pts::choose_last_wave(pl.tiles, resident, pl.num_kb, h->opts.split == 0,
+                                                h->opts.split_k, int(sched), pl.tail)) > 0)
         pl.sk_units = resident;
-    pl.units = pl.sk_units > 0 ? pl.sk_units + pl.tiles - pl.sk_tiles : pl.tiles * pl.split;
+    pl.units = pl.sk_units > 0 ? pl.sk_units + pl.tiles - pl.sk_tiles : pl.tiles * pl.split + pl.tail;
     pl.work = pl.sk_units > 0 ? pts::kSkMaxPieces * pl.sk_units + pl.tiles - pl.sk_tiles : pl.units;
     if (pl.work > (int64_t(1) << 31) - 1) return GEMM_ERR_INVALID_ARG;
     int64_t clusters = pl.units;
@@ -319,7 +323,8 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
     const uint32_t brows = uint32_t(pl.bn / pl.cg);
     const int cdt = dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16;
-    const bool slices = pl.split > 1;
+    const bool slices = pl.split > 1 || pl.tail > 0;
+    const int slice_div = pl.tail > 0 ? 2 : pl.split;
     CUtensorMap ma, mb0, mb_slice, mc;
     const CUtensorMap *m;
     if (!(m = get_map(h, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems))) return GEMM_ERR_CUDA;
@@ -328,15 +333,15 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     mb0 = *m;
     mb_slice = mb0;
     if (slices) {
-        if (!(m = get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(pl.split), kelems)))
+        if (!(m = get_map(h, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(slice_div), kelems)))
             return GEMM_ERR_CUDA;
         mb_slice = *m;
     }
     if (!(m = get_map(h, C, uint64_t(M), uint64_t(N), cdt, pts::kEpiRowsPerWarp, pts::kEpiChunkCols)))
         return GEMM_ERR_CUDA;
     mc = *m;
-    const CUtensorMap *mb[3] = {&mb0, (slices && pl.split == 2) ? &mb_slice : &mb0,
-                                (slices && pl.split == 4) ? &mb_slice : &mb0};
+    const CUtensorMap *mb[3] = {&mb0, (slices && slice_div == 2) ? &mb_slice : &mb0,
+                                (slices && slice_div == 4) ? &mb_slice : &mb0};
 
     pts::GemmParams p{};
     p.M = static_cast<int32_t>(M);
@@ -359,6 +364,7 @@ gemm_status_t launch(gemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A
     p.prefetch_kb = h->opts.prefetch < 0 ? 0 : (h->opts.prefetch == 0 ? pts::kDefaultPrefetchKb : h->opts.prefetch);
     p.epi_direct = h->opts.epilogue == 2 ? 1 : 0;
     p.clc_lead = h->opts.clc_depth;
+    p.tail_tiles = static_cast<int32_t>(pl.tail);
     p.c_ptr = C;
     p.out_scale = out_scale;
     p.debug_flags = h->opts.debug_flags;
@@ -855,6 +861,7 @@ gemm_status_t gemm_query(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_
     info->split_k = pl.sk_units > 0 ? 1 : 0;
     info->sk_tiles = pl.sk_tiles;
     info->sk_units = pl.sk_units;
+    info->tail_tiles = pl.tail;
     info->work_items = pl.work;
     info->units = pl.units;
     info->grid_ctas = (M == 0 || N == 0 || K == 0) ? 0 : pl.grid_ctas;

@@ -152,6 +152,8 @@ __device__ __forceinline__ int group_of(int w, const GemmParams &p)
 //    tile (only slots of pieces that exist are handed out); s >= 3U is the
 //    whole tile sk_tiles + s - 3U.
 //  - With column slices (split 2 or 4): slice s % split of tile s / split.
+//  - With tail halves (tail_tiles = R > 0): s < T - R is the whole tile s;
+//    s = T - R + j is the column half j % 2 of tile T - R + j / 2.
 //  - Otherwise the whole tile s.
 // Tiles are numbered in grouped order (tile_of).  (A grouped launch's items
 // are decoded by the scheduler warp, which caches its problem table.)
@@ -187,6 +189,11 @@ __device__ __forceinline__ WorkTile work_tile(int s, const GemmParams &p)
         const int h = s - tile * p.split;
         t.n_len = BN / p.split;
         t.n_off = h * t.n_len;
+    } else if (p.tail_tiles > 0 && s >= p.num_tiles - p.tail_tiles) {
+        const int j = s - (p.num_tiles - p.tail_tiles);
+        tile = p.num_tiles - p.tail_tiles + j / 2;
+        t.n_len = BN / 2;
+        t.n_off = (j & 1) * t.n_len;
     }
     tile_of(tile, p.tiles_m, p.tiles_n, p.group_m, t.tm, t.tn);
     t.idx = t.tm * p.tiles_n + t.tn;
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(CG, BN))
     // registers).
     // tmB / tmB2 / tmB4: B boxes of BN/CG, BN/CG/2 and BN/CG/4 rows, for whole
     // tiles and for the column slices (halves, quarters) of a problem smaller
-    // than one wave
+    // than one wave or of the tiles of a partial last wave (halves)
     // FULL = false: the common launch -- one problem, no debug records, the
     // TMA-store epilogue, no L2 prefetch, no test hooks -- with the code of
     // those features compiled out.  Less code to fetch at the start of a
@@ -420,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(CG, BN))
     if (warp == 0 && lane == 0 && !grouped) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if (p.split == 2) prefetch_tmap(&tmB2);
+        if (p.split == 2 || p.tail_tiles > 0) prefetch_tmap(&tmB2);
         if (p.split == 4) prefetch_tmap(&tmB4);
         prefetch_tmap(&tmC);
     }

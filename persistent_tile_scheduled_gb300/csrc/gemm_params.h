@@ -76,6 +76,8 @@ struct GemmParams {
     int32_t prefetch_kb;        // L2 prefetch distance ahead of the operand loads, in k-blocks (0 = none)
     int32_t epi_direct;         // 1: the epilogue stores C rows straight from registers (no TMA store)
     int32_t clc_lead;           // CLC: units claimed ahead of the producer (1 or 2)
+    int32_t tail_tiles;         // the last tail_tiles tiles (grouped order) run as two column halves
+                                // each; 0 = none (not with split > 1 or a stream-K region)
     void *c_ptr;                // C (for the direct-store epilogue)
     float out_scale;            // 1, or 1/(scale_a*scale_b) for e4m3
     uint32_t debug_flags;

@@ -1,5 +1,6 @@
-// Launch-plan rules of the host: the CTA group, tile width, column slices and
-// stream-K share a problem gets when the caller leaves them to the library.
+// Launch-plan rules of the host: the CTA group, tile width, column slices,
+// tail halves and stream-K share a problem gets when the caller leaves them
+// to the library.
 // Host-only (the kernels never read them); each threshold comes from the
 // measurement on GB300 quoted beside it.
 #pragma once
@@ -70,6 +71,52 @@ inline int choose_split(int64_t tiles, int64_t resident)
     if (4 * tiles <= resident) return 4;
     if (2 * tiles <= resident) return 2;
     return 1;
+}
+
+// Column halves for the tail.  With T tiles on G resident clusters and
+// R = T mod G, the last wave keeps only R clusters busy, each for a whole
+// tile.  When 2R <= G the last R tiles (grouped order) are each cut into two
+// column halves, run as 2R units: every cluster still busy in the last wave
+// has half a tile.  A half tile takes about two thirds of a whole one (its
+// k-blocks carry half the MMA work but not half the per-k-block cost) and
+// needs no fixup, so it keeps the result's bits.  Measured on GB300 (fp16
+// 4096^2, R = 28 of 76 pairs or 56 of 152 single CTAs, chained launches,
+// whole / halves, us per launch): K = 384 16.1 / 14.8, 640 21.6 / 20.6,
+// 1024 28.6 / 27.5, 1536 38.1 / 36.8, 1920 45.0 / 43.5; bf16 8192^2
+// (R = 36) K = 1024 84.6 / 83.2, 2048 152.1 / 151.2.  Returns R, or 0.
+inline int64_t choose_tail(int64_t tiles, int64_t resident)
+{
+    if (resident < 2 || tiles <= resident) return 0;
+    const int64_t r = tiles % resident;
+    return (r > 0 && 2 * r <= resident) ? r : 0;
+}
+
+// Where both apply, the halves are used below this many k-blocks per tile and
+// the stream-K share from here (when it saves kSkMinSavedKb): the share
+// evens the last wave out fully but pays its fixup, the halves leave the last
+// wave at two thirds of a tile but pay nothing.  Measured on GB300 (fp16
+// 4096^2, chained launches, share / halves, us per launch): K = 2048 47.1 /
+// 45.4, 2560 54.9 / 54.3, 3072 63.7 / 63.8, 3584 72.7 / 73.5, 4096 81.9 /
+// 83.0; bf16 8192^2 K = 3072 220.8 / 221.0, 4096 288.5 / 287.9.
+constexpr int kTailMaxKb = 48;
+
+// The partial last wave of `tiles` tiles of `num_kb` k-blocks on `resident`
+// clusters (wide tile, no column slices): returns the stream-K region's tiles
+// (0 = none) and sets `tail` to the tiles run as column halves (0 = none).
+// split_auto: the caller left column slicing to the library (else no
+// halves); sk_force as for choose_stream_k.  Halves only for the persistent
+// schedulers: the non-persistent grid launches a cluster per half and gains
+// nothing from them (measured on GB300, fp16 4096^2, chained, without /
+// with halves: K = 1024 40.0 / 40.0 us, 1536 49.9 / 50.0; in place of the
+// stream-K share K = 2048 57.1 / 59.6, 2560 65.9-71.5 / 75.7).
+inline int64_t choose_last_wave(int64_t tiles, int64_t resident, int64_t num_kb, bool split_auto, int sk_force,
+                                int sched, int64_t &tail)
+{
+    const int64_t r = (split_auto && sched != SCHED_NONPERSISTENT) ? choose_tail(tiles, resident) : 0;
+    const bool halves_first = r > 0 && sk_force == 0 && num_kb < kTailMaxKb;
+    const int64_t sk = halves_first ? 0 : choose_stream_k(tiles, resident, num_kb, sk_force);
+    tail = sk > 0 ? 0 : r;
+    return sk;
 }
 
 // The narrow tile (tile_n 128).  The wide tile's ring and staging take nearly

@@ -51,7 +51,7 @@ class gemm_launch_info_t(ctypes.Structure):
                 ("max_active_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
                 ("split", ctypes.c_int), ("split_k", ctypes.c_int), ("sk_tiles", ctypes.c_int64),
                 ("sk_units", ctypes.c_int64), ("work_items", ctypes.c_int64), ("units", ctypes.c_int64),
-                ("ctas_per_sm", ctypes.c_int)]
+                ("ctas_per_sm", ctypes.c_int), ("tail_tiles", ctypes.c_int64)]
 
 
 class gemm_host_problem_t(ctypes.Structure):

@@ -93,10 +93,11 @@ def check_records(records, info, sched: int, K: int, group_m: int = 8):
     W, split, BN = int(info.work_items), int(info.split), int(info.tile_n)
     G = int(info.grid_ctas) // cg
     num_kb = -(-int(K) // int(info.tile_k))
+    R = int(info.tail_tiles)
     units = osched.work_units(T, split, tile_n=BN, num_kb=num_kb, sk_tiles=int(info.sk_tiles),
-                              sk_units=int(info.sk_units))
+                              sk_units=int(info.sk_units), tail_tiles=R)
     assert len(units) == int(info.units)
-    assert W == osched.record_slots(T, split, int(info.sk_tiles), int(info.sk_units))
+    assert W == osched.record_slots(T, split, int(info.sk_tiles), int(info.sk_units), R)
     items = [it for u in units for it in u]
     used = {it[0] for it in items}
     for w in range(W):

@@ -90,7 +90,8 @@ def test_struct_layouts_match_the_header():
              offsetof(gemm_launch_info_t, grid_ctas), offsetof(gemm_launch_info_t, threads));
       printf("%zu %zu %zu %zu\n", offsetof(gemm_launch_info_t, sk_tiles), offsetof(gemm_launch_info_t, work_items),
              offsetof(gemm_launch_info_t, units), offsetof(gemm_launch_info_t, ctas_per_sm));
-      printf("%zu %zu\n", offsetof(gemm_opts_t, tile_n), offsetof(gemm_opts_t, clc_depth));
+      printf("%zu %zu %zu\n", offsetof(gemm_opts_t, tile_n), offsetof(gemm_opts_t, clc_depth),
+             offsetof(gemm_launch_info_t, tail_tiles));
       return 0;
     }
     """
@@ -110,7 +111,7 @@ def test_struct_layouts_match_the_header():
             g.gemm_launch_info_t.grid_ctas.offset, g.gemm_launch_info_t.threads.offset,
             g.gemm_launch_info_t.sk_tiles.offset, g.gemm_launch_info_t.work_items.offset,
             g.gemm_launch_info_t.units.offset, g.gemm_launch_info_t.ctas_per_sm.offset,
-            g.gemm_opts_t.tile_n.offset, g.gemm_opts_t.clc_depth.offset]
+            g.gemm_opts_t.tile_n.offset, g.gemm_opts_t.clc_depth.offset, g.gemm_launch_info_t.tail_tiles.offset]
     assert got == want
 
 

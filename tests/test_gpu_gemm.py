@@ -174,6 +174,46 @@ def test_forced_stream_k_share(cg, G, sched):
         pts.gemm_destroy(h)
 
 
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("G", [3, 5])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_tail_halves(cg, G, sched):
+    """A partial last wave of R <= G/2 tiles on G clusters: under the
+    persistent schedulers those tiles run as two column halves each, so every
+    cluster busy in the last wave holds half a tile (the non-persistent grid
+    keeps whole tiles).  Records bit-exact against the scheduler model, parity against the
+    oracle, and the same bits as with whole tiles (split 1, no stream-K
+    share): a half changes which cluster computes a column, not its sum.
+    Ragged shapes, every dtype."""
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg, max_clusters=G, debug_flags=pts.GEMM_DEBUG_RECORDS))
+    h1 = pts.gemm_create(0, pts.make_opts(cta_group=cg, max_clusters=G, split=1, split_k=-1))
+    tails = 0
+    try:
+        for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (640, 1000, 1040, wl.F16), (257, 264, 512, wl.E4M3),
+                              (1000, 1800, 2000, wl.BF16), (1100, 1304, 640, wl.F16)]:
+            info = pts.gemm_query(h, M, N, K, dt, sched)
+            T = int(info.tiles)
+            R = T % G
+            want = R if (sched != pts.GEMM_SCHED_NONPERSISTENT and T > G and 0 < 2 * R <= G) else 0
+            assert int(info.tail_tiles) == want, (M, N, K)
+            assert info.split_k == 0 or not want, (M, N, K)   # the halves replace the share
+            if want:
+                assert info.units == T + R and info.work_items == T + R and info.split == 1
+                assert int(pts.gemm_query(h1, M, N, K, dt, sched).tail_tiles) == 0
+            tails += want > 0
+            dist = "normal" if dt == wl.E4M3 else "uniform"
+            x = wl.make_inputs(wl.Problem("tail", M, N, K, dt, dist, M + N + K + 10 * G))
+            C, _ = _run_checked(h, x, sched)
+            if info.split_k == 0:   # (the share's fixup sums in another order)
+                C1 = run_device(h1, x, sched)
+                assert pts.gemm_check(h1)[0] == 0
+                assert torch.equal(C, C1), (M, N, K)
+    finally:
+        pts.gemm_destroy(h)
+        pts.gemm_destroy(h1)
+    assert tails > 0 or sched == pts.GEMM_SCHED_NONPERSISTENT
+
+
 @pytest.mark.parametrize("cg,stages", [(1, 2), (1, 3), (1, 4), (2, 2), (2, 3)])
 def test_every_ring_depth(cg, stages):
     """Shallower rings than the default: a single CTA's stage holds one k-block,

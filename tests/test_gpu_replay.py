@@ -148,12 +148,13 @@ def test_graph_with_the_same_stream_k_gemm_twice():
 def test_bench_step_replayed_matches_oracle():
     """bench.py's own step (the 32 GEMMs of the fp16 4096 K sweep, library
     defaults, static scheduler), captured as bench.py --graph captures it and
-    replayed twice; the K = 2048 and K = 4096 outputs (CTA pairs with the
+    replayed twice; the K = 3072 and K = 4096 outputs (CTA pairs with the
     stream-K share) are checked against the oracle after each replay, and
-    the K = 128 one (single CTAs, whole tiles) on a sample."""
+    the K = 2048 one (CTA pairs) and the K = 128 one (single CTAs), both with
+    their last wave's tiles in column halves, on a sample."""
     import bench
     problems = wl.fp16_4096_ksweep()
-    checked = {128, 2048, 4096}
+    checked = {128, 2048, 3072, 4096}
     xs, bufs = {}, []
     gen = torch.Generator(device="cuda").manual_seed(12)
     for q in problems:
@@ -168,8 +169,10 @@ def test_bench_step_replayed_matches_oracle():
     h = pts.gemm_create(0, pts.make_opts(cta_group=0, epilogue=0, split_k=0))
     s = torch.cuda.Stream()
     try:
-        for K in (2048, 4096):
+        # the step holds launches with the stream-K share and with tail halves
+        for K in (3072, 4096):
             assert pts.gemm_query(h, 4096, 4096, K, wl.F16, pts.GEMM_SCHED_STATIC).split_k == 1
+        assert pts.gemm_query(h, 4096, 4096, 2048, wl.F16, pts.GEMM_SCHED_STATIC).tail_tiles > 0
         with torch.cuda.stream(s):
             bench.sweep_pass(pts, h, bufs, problems, pts.GEMM_SCHED_STATIC, s)
         assert pts.gemm_check(h, s)[0] == 0

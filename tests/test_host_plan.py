@@ -24,6 +24,7 @@ PROGRAM = r"""
 using namespace pts;
 int main() {
     const long long cases[][3] = {%CASES%};
+    int first = 1;
     printf("{\"cases\": [");
     for (unsigned i = 0; i < sizeof(cases) / sizeof(cases[0]); ++i) {
         const long long T = cases[i][0], G = cases[i][1], kb = cases[i][2];
@@ -50,7 +51,23 @@ int main() {
     for (int kb = 1; kb <= 80; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb, SCHED_NONPERSISTENT));
     printf("], \"cta_group_clc\": [");
     for (int kb = 1; kb <= 40; ++kb) printf("%s%d", kb > 1 ? ", " : "", choose_cta_group(kb, SCHED_CLC));
-    printf("], \"pair_min_kb\": %d, \"pair_min_kb_np\": %d, \"sk_min_saved_kb\": %d", kPairMinKb,
+    printf("], \"last_wave\": [");
+    const long long lw[][2] = {{256, 76}, {512, 152}, {1024, 76}, {270, 76}, {304, 76}, {300, 76}, {76, 76},
+                               {40, 76}, {5, 3}, {7, 3}, {114, 76}, {115, 76}, {400, 76}};
+    first = 1;
+    for (unsigned i = 0; i < sizeof(lw) / sizeof(lw[0]); ++i)
+        for (int kb = 2; kb <= 130; kb += 4)
+            for (int aut = 0; aut <= 1; ++aut)
+                for (int f = -1; f <= 1; ++f)
+                    for (int sched = 0; sched <= 2; ++sched) {
+                        int64_t tail = -7;
+                        const long long sk = choose_last_wave(lw[i][0], lw[i][1], kb, aut != 0, f, sched, tail);
+                        printf("%s[%lld, %lld, %d, %d, %d, %d, %lld, %lld]", first ? "" : ", ", lw[i][0], lw[i][1], kb,
+                               aut, f, sched, sk, (long long)tail);
+                        first = 0;
+                    }
+    printf("], \"tail_max_kb\": %d", kTailMaxKb);
+    printf(", \"pair_min_kb\": %d, \"pair_min_kb_np\": %d, \"sk_min_saved_kb\": %d", kPairMinKb,
            kPairMinKbNonPersistent, kSkMinSavedKb);
     printf(", \"kb_per_stage\": [%d, %d], \"smem\": [%d, %d, %d]", kb_per_stage(1), kb_per_stage(2),
            smem_bytes(1, 4), smem_bytes(2, 3), smem_bytes(1, 5));
@@ -59,7 +76,7 @@ int main() {
            smem_bytes(1, kNarrowStages, kTileNNarrow), smem_bytes(1, 3, kTileNNarrow), kNarrowStages,
            ctas_per_sm(1, kTileN), ctas_per_sm(2, kTileN), ctas_per_sm(1, kTileNNarrow), ctas_per_sm(2, kTileNNarrow),
            smem_bytes(2, 4, kTileNNarrow), smem_bytes(2, 5, kTileNNarrow), kNarrowMaxKb);
-    int first = 1;
+    first = 1;
     for (int kb = 1; kb <= 10; ++kb)
         for (int cg = 0; cg <= 2; ++cg)
             for (int sched = 0; sched <= 2; ++sched) {
@@ -117,6 +134,30 @@ def test_stream_k_is_used_only_when_it_saves_enough(plan):
         R = T % G
         want = case["sk_force"] if (case["sk_force"] and kb * (G - R) >= m * G) else 0
         assert case["sk_auto"] == want, case
+
+
+def test_last_wave_halves_or_stream_k(plan):
+    """The partial last wave of T tiles on G clusters (R = T mod G): its R tiles
+    run as column halves under the persistent schedulers when 2R <= G and
+    the caller left slicing to the library, unless the stream-K share is
+    forced or the tiles are long enough (tail_max_kb k-blocks) for the share,
+    where it saves enough, to be used instead; never both."""
+    m, tmax = plan["sk_min_saved_kb"], plan["tail_max_kb"]
+    seen = set()
+    for T, G, kb, aut, force, sched, sk, tail in plan["last_wave"]:
+        R = T % G
+        halves = R if (aut and sched != 0 and T > G and R and 2 * R <= G) else 0
+        share = R + G if (T >= G and R) else 0
+        if force < 0:
+            want_sk = 0
+        elif force > 0:
+            want_sk = share
+        else:
+            want_sk = share if (share and kb * (G - R) >= m * G and not (halves and kb < tmax)) else 0
+        assert sk == want_sk, (T, G, kb, aut, force, sched)
+        assert tail == (0 if want_sk else halves), (T, G, kb, aut, force, sched)
+        seen.add((bool(sk), bool(tail)))
+    assert seen == {(False, False), (True, False), (False, True)}
 
 
 def test_slices_and_cta_group_thresholds(plan):

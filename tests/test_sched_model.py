@@ -132,6 +132,35 @@ def test_stream_k_hand_worked(golden_dir):
     assert units[3:] == [[(9, 5, 0, 256, 0, 4)], [(10, 6, 0, 256, 0, 4)], [(11, 7, 0, 256, 0, 4)]]
 
 
+def test_tail_halves_hand_worked():
+    # T = 5 with the last 2 tiles in column halves: 3 whole units, then 4 halves
+    assert sm.work_units(5, num_kb=6, tail_tiles=2) == [
+        [(0, 0, 0, 256, 0, 6)], [(1, 1, 0, 256, 0, 6)], [(2, 2, 0, 256, 0, 6)],
+        [(3, 3, 0, 128, 0, 6)], [(4, 3, 128, 128, 0, 6)], [(5, 4, 0, 128, 0, 6)], [(6, 4, 128, 128, 0, 6)]]
+    assert sm.record_slots(5, tail_tiles=2) == 7
+    for bad in (dict(split=2, tail_tiles=1), dict(sk_tiles=4, sk_units=2, tail_tiles=1), dict(tail_tiles=6),
+                dict(tail_tiles=-1)):
+        with pytest.raises(ValueError):
+            sm.work_units(5, num_kb=4, **bad)
+
+
+@pytest.mark.parametrize("T,G", [(256, 76), (512, 152), (1024, 76), (320, 76), (4, 3), (41, 20), (21, 20)])
+def test_tail_halves_partition_and_last_wave(T, G):
+    """The last R = T mod G tiles in halves (when 2R <= G): every tile is still
+    covered exactly once, and under the static assignment no cluster has more
+    than half a tile in the last wave."""
+    R = T % G
+    assert 0 < 2 * R <= G
+    units = sm.work_units(T, num_kb=3, tail_tiles=R)
+    items = [it for u in units for it in u]
+    assert [i[0] for i in items] == list(range(sm.record_slots(T, tail_tiles=R)))
+    _cells_partition(items, T, 3)
+    load = [0] * G                                       # in half tiles
+    for u, its in enumerate(units):
+        load[u % G] += sum(it[3] for it in its) // 128
+    assert max(load) == 2 * (T // G) + 1 and min(load) == 2 * (T // G)
+
+
 def _cells_partition(items, T, num_kb, tile_n=256):
     cells = {}
     for _, t, off, n, k0, k1 in items:
