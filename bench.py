@@ -761,11 +761,11 @@ def tile_plans_small_k(pts, dev, stream, ks=(128, 256, 512, 1024), n=20, nbuf=4)
     has: the wide 128x256 tile as single CTAs and as CTA pairs (256x256), the
     narrow 128x128 tile as single CTAs (two per SM) and as CTA pairs (256x128,
     one CTA per SM), and the library's own choice.  Per scheduler, microseconds
-    per launch over `n` chained launches on `nbuf` rotating buffer sets; the
-    stream-K share off in the fixed plans, so that they differ in the tile
-    alone."""
-    plans = {"wide_cg1": dict(cta_group=1, tile_n=256, split_k=-1),
-             "wide_cg2": dict(cta_group=2, tile_n=256, split_k=-1),
+    per launch over `n` chained launches on `nbuf` rotating buffer sets; whole
+    tiles (no stream-K share, no tail halves) in the fixed plans, so that they
+    differ in the tile alone."""
+    plans = {"wide_cg1": dict(cta_group=1, tile_n=256, split=1, split_k=-1),
+             "wide_cg2": dict(cta_group=2, tile_n=256, split=1, split_k=-1),
              "narrow_cg1": dict(cta_group=1, tile_n=128),
              "narrow_cg2": dict(cta_group=2, tile_n=128),
              "library": {}}
@@ -798,7 +798,8 @@ def tile_plans_small_k(pts, dev, stream, ks=(128, 256, 512, 1024), n=20, nbuf=4)
                 pts.gemm_destroy(h)
         del ins, Cs
     out["note"] = (f"microseconds per launch, {n} chained launches on {nbuf} rotating buffer sets; "
-                   "wide = 128x256 per CTA, narrow = 128x128 per CTA; cg2 = CTA pairs")
+                   "wide = 128x256 per CTA, narrow = 128x128 per CTA; cg2 = CTA pairs; the fixed plans run "
+                   "whole tiles, library = the library's own plan")
     return out
 
 
