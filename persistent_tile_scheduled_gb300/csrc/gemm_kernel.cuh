@@ -475,7 +475,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(CG, BN))
             tma_prefetch_2d(one, mb, kb * KELEMS, yb);
         }
     }
-    pdl_wait();
+    // The scheduler warp of a single-problem launch waits only after it has
+    // published its first item (its decode reads no global memory), so the
+    // producers find that item in the ring when their own wait returns.
+    if (grouped || warp != kSchedWarp) pdl_wait();
 
     // ---- work-item broadcast ring -----------------------------------------
     // Slot r holds work item i (i % kRing == r), decoded: its id w (the
@@ -1063,7 +1066,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(CG, BN))
                     // may suspend the waiting warp.  Depth 2 lets the producer run a
                     // further item ahead, past what a parity can tell apart, so it
                     // waits on the started-item counter instead.
-                    ok = publish(i, w, item_of(w))
+                    ok = publish(i, w, item_of(w));
+                    if (!grouped && i == 0) pdl_wait();   // before any time-limited wait or global access
+                    ok = ok
                          && (lead == 0
                              || (lead == 1 ? ctl.wait_all(started_bar, static_cast<uint32_t>(i & 1), WHERE_STARTED)
                                            : ctl.wait_count_all(started_cnt, i + 2 - lead, WHERE_STARTED)));
