@@ -366,7 +366,9 @@ gemm_status_t gemm_read_debug(gemm_handle_t h, void *stream, gemm_tile_record_t 
  *   - Problems with more than GEMM_NOALLOC_MAX_WORK_ITEMS work items are
  *     rejected with GEMM_ERR_INVALID_ARG before anything is launched (work
  *     items = output tiles of 128x256 for cta_group 1 or 256x256 for
- *     cta_group 2, plus up to 3 per tile of a sliced last wave).
+ *     cta_group 2, plus up to 3 per tile of a problem smaller than one
+ *     wave, or 1 per tile of a partial last wave run as column halves; the
+ *     stream-K share is never used here).
  *   - The first call on a device does a one-time set-up on that device (the
  *     scratch array's device address via cudaGetSymbolAddress, kernel
  *     attributes, occupancy); make that first call before any stream capture.

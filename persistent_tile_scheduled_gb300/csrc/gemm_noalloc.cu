@@ -163,29 +163,35 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     const int ci = cta_group - 1;
     const int64_t resident = s->clusters[dtype][ci];
     const int split = pts::choose_split(tiles, resident);   // column slices below one wave
-    const int64_t work = tiles * split;
+    // column halves of a partial last wave (persistent schedulers; never the
+    // stream-K share, whose fixup workspace a static array could not hold)
+    const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
+    const int64_t num_kb = (K + kelems - 1) / kelems;
+    int64_t tail = 0;
+    if (split == 1) (void)pts::choose_last_wave(tiles, resident, num_kb, true, -1, int(sched), tail);
+    const int64_t work = tiles * split + tail;
     if (work > GEMM_NOALLOC_MAX_WORK_ITEMS) return GEMM_ERR_INVALID_ARG;   // one scratch record per item
 
     // status words and the records of this problem's work items must start at zero
     const size_t used = kStatusBytes + static_cast<size_t>(work) * sizeof(pts::TileRecord);
     if (cudaMemsetAsync(s->scratch, 0, used, st) != cudaSuccess) return fail(cudaErrorInvalidValue);
 
-    const uint32_t kelems = dtype == GEMM_E4M3 ? 128u : 64u;
     CUtensorMap ma, mb, mb_slice, mc;
     const uint32_t brows = uint32_t(pts::kTileN / cta_group);
     if (!encode_2d(s, &ma, A, uint64_t(M), uint64_t(K), dtype, pts::kRowsPerCta, kelems)
         || !encode_2d(s, &mb, B, uint64_t(N), uint64_t(K), dtype, brows, kelems)
-        || !encode_2d(s, &mb_slice, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(split), kelems)
+        || !encode_2d(s, &mb_slice, B, uint64_t(N), uint64_t(K), dtype, brows / uint32_t(tail > 0 ? 2 : split),
+                      kelems)
         || !encode_2d(s, &mc, C, uint64_t(M), uint64_t(N), dtype == GEMM_F16 ? GEMM_F16 : GEMM_BF16,
                       pts::kEpiRowsPerWarp, pts::kEpiChunkCols))
         return GEMM_ERR_CUDA;
-    const CUtensorMap *mbs[3] = {&mb, split == 2 ? &mb_slice : &mb, split == 4 ? &mb_slice : &mb};
+    const CUtensorMap *mbs[3] = {&mb, (split == 2 || tail > 0) ? &mb_slice : &mb, split == 4 ? &mb_slice : &mb};
 
     pts::GemmParams p{};
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.num_kb = static_cast<int32_t>((K + kelems - 1) / kelems);
+    p.num_kb = static_cast<int32_t>(num_kb);
     p.tiles_m = static_cast<int32_t>(tiles_m);
     p.tiles_n = static_cast<int32_t>(tiles_n);
     p.num_tiles = static_cast<int32_t>(tiles);
@@ -202,6 +208,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     p.prefetch_kb = pts::kDefaultPrefetchKb;
     p.epi_direct = 0;
     p.clc_lead = pts::kDefaultClcLead;
+    p.tail_tiles = static_cast<int32_t>(tail);
     p.c_ptr = C;
     p.out_scale = out_scale;
     p.debug_flags = pts::DBG_RECORDS;

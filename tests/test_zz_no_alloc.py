@@ -10,7 +10,9 @@ records) in a static device array shared by all calls.
 For problems smaller than one wave of resident clusters both entry points
 take the same plan (CTA group, ring depth, column slices, no stream-K share),
 so gemm_run_noalloc must return exactly the bits gemm_run returns, and both
-must meet the oracle's bound.  Two calls in a row, on problems of different
+must meet the oracle's bound.  The same holds past one wave while gemm_run
+takes no stream-K share (short tiles): both then run a partial last wave as
+column halves.  Two calls in a row, on problems of different
 sizes, check that the shared scratch is cleared between calls (the second
 call would otherwise find the first call's tile records).  This file is
 collected last on purpose.
@@ -22,7 +24,7 @@ import persistent_tile_scheduled_gb300 as pts
 import workloads as wl
 from oracle import gemm as og
 
-from helpers import TOL, dequant, out_u
+from helpers import TOL, compare_sampled, dequant, out_u
 
 pytestmark = pytest.mark.gpu
 
@@ -79,6 +81,31 @@ def test_noalloc_matches_gemm_run_on_two_calls_in_a_row(cg, dtype, sched):
             assert err <= TOL[p.dtype], err
     finally:
         pts.gemm_destroy(h)
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=["nonpersistent", "static", "clc"])
+@pytest.mark.parametrize("cg", [1, 2])
+def test_noalloc_partial_last_wave(cg, sched):
+    """A problem of several waves (fp16 4096^2 x 256) whose partial last wave
+    the persistent schedulers run as column halves, in both entry points:
+    gemm_run_noalloc gives gemm_run's bits, its coverage records are exact,
+    and a sample meets the oracle's bound."""
+    x = wl.make_inputs(wl.Problem("noalloc_tail", 4096, 4096, 256, wl.F16, "normal_sqrtk", 45 + cg))
+    p = x.problem
+    h = pts.gemm_create(0, pts.make_opts(cta_group=cg))
+    try:
+        info = pts.gemm_query(h, p.M, p.N, p.K, p.dtype, sched)
+        assert info.split_k == 0 and info.tiles > info.max_active_clusters
+        assert (int(info.tail_tiles) > 0) == (sched != pts.GEMM_SCHED_NONPERSISTENT)
+        A, B, C_existing = _run_existing(h, x, sched)
+    finally:
+        pts.gemm_destroy(h)
+    C = torch.full((p.M, p.N), float("nan"), dtype=C_existing.dtype, device="cuda")
+    st, dev = pts.gemm_run_noalloc(p.M, p.N, p.K, A, B, C, p.dtype, sched, cta_group=cg, check=True)
+    assert st == 0 and dev == 0, f"{pts.gemm_status_string(st)}, device word {dev:#x}"
+    assert torch.equal(_bits(C), _bits(C_existing))
+    err = compare_sampled(x, C, int(info.tile_m), int(info.tile_n))
+    assert err <= TOL[p.dtype], err
 
 
 def test_noalloc_asynchronous_call_matches():
