@@ -633,6 +633,12 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
         "data": "synthetic (seeded N(0,1)/sqrt(K), rounded to fp16)",
         "config": {"workload": WORKLOAD, "tile": TILE_DESC[args.cta_group], "group_size_m": 8,
                    "cta_group": args.cta_group, "split_k": args.split_k, "sched": HEADLINE,
+                   "last_wave": ("the library's choice per GEMM: with the static and CLC schedulers a partial "
+                                 "last wave of at most half the clusters runs as column halves of its tiles "
+                                 "below 48 k-blocks per tile (K < 3072), else the stream-K share of the last "
+                                 "waves where it saves >= 20 k-blocks per cluster; the non-persistent grid "
+                                 "takes only the share"
+                                 if args.split_k == 0 else "as --split-k sets it"),
                    "launch": ("CUDA graph of the 32 gemm_run launches per step" if args.graph
                               else "32 gemm_run calls per step, launched one by one"),
                    "l2": "no flush: one step's 32 distinct A,B,C sets (2.1 GB) exceed the 129 MB L2",
