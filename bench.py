@@ -344,6 +344,26 @@ def cpu_baseline_sample(problems, xs, budget_s=10.0):
             "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
+def oracle_full_configs():
+    """The oracle as it stands, whole GEMMs, on all host threads: the small
+    configuration (fp16 512^3), the fp16 sweep's two ends (4096^2 x 128 and
+    x 4096) and e4m3 8192^3 (about 1.1 TFLOP of fp64 work).  A measurement of
+    the CPU baseline on full problems, not part of the default run."""
+    from oracle import gemm as og
+    rows = []
+    for p in wl.fp16_512() + wl.fp16_4096_ksweep([128, 4096]) + wl.e4m3_8192():
+        x = wl.make_inputs(p)
+        t0 = time.perf_counter()
+        og.gemm(p.M, p.N, p.K, x.bits("A").reshape(-1), x.bits("B").reshape(-1), p.dtype,
+                1.0 / (float(x.scale_a) * float(x.scale_b)) if p.dtype == wl.E4M3 else 1.0, nthreads=0)
+        dt = time.perf_counter() - t0
+        rows.append({"problem": p.name, "M": p.M, "N": p.N, "K": p.K, "seconds": round(dt, 3),
+                     "tflops": round(gemm_flops(p.M, p.N, p.K) / dt / 1e12, 5)})
+        log(f"oracle {p.name}: {dt:.2f} s")
+    return {"oracle_full": rows, "cores": og.max_threads(), "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "kind": "oracle", "note": "fp64 triple loop over every output and every k, with sum |a||b| beside it"}
+
+
 def run_ours(args, dist, rank, world, local):
     import persistent_tile_scheduled_gb300 as pts
     torch.cuda.set_device(local)
@@ -1084,7 +1104,13 @@ def main():
     ap.add_argument("--grouped-only", action="store_true",
                     help="only the grouped 64-problem measurement (for profiling it), restricted by --cta-group and "
                          "--scheds; prints its numbers, not the benchmark line")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="only time the oracle on whole configuration problems (host cores, about a minute); "
+                         "prints those times, not the benchmark line")
     args = ap.parse_args()
+    if args.oracle_configs:
+        print(json.dumps(oracle_full_configs()), flush=True)
+        return
     if args.square_only:
         import persistent_tile_scheduled_gb300 as pts
         pts.load(build_if_missing=False)
