@@ -27,8 +27,9 @@
 // grid and takes that cluster's id as its next unit, never asking again after
 // one failed request.  The non-persistent mode runs exactly one unit per
 // cluster ("question about persistent kernel concept": a thread block per tile).
-// A unit is a whole tile, a column slice of one, or a stream-K unit's pieces
-// (see work_tile()).
+// A unit is a whole tile, a column slice of one (below one wave, or a half of
+// a tile of a partial last wave), or a stream-K unit's pieces (see
+// work_tile()).
 //
 // Every mbarrier wait is bounded: on time-out the kernel records an error in
 // the device status block, tells every role (and the peer CTA) to stop, drains
