@@ -639,12 +639,12 @@ def test_full_size_sampled(handle, name, arg):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("K", [128, 1024, 1792, 2560, 4096])
+@pytest.mark.parametrize("K", [128, 1024, 1792, 2560, 3072, 4096])
 def test_bench_configuration_sampled(K):
     """The exact launch configuration bench.py times: library defaults (CTA
-    group, ring depth, stream-K share chosen per GEMM) on sweep GEMMs that take
-    each plan: single CTAs without and with the stream-K share, CTA pairs with
-    it."""
+    group, ring depth, last-wave plan chosen per GEMM) on sweep GEMMs that take
+    each plan: single CTAs and CTA pairs with the last wave's tiles in column
+    halves, and CTA pairs with the stream-K share."""
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     h = pts.gemm_create(0, pts.make_opts(debug_flags=pts.GEMM_DEBUG_RECORDS))
@@ -652,6 +652,7 @@ def test_bench_configuration_sampled(K):
         x = wl.make_inputs(wl.fp16_4096_ksweep([K])[0])
         info = pts.gemm_query(h, 4096, 4096, K, pts.GEMM_F16, pts.GEMM_SCHED_STATIC)
         assert info.cta_group == (2 if K // 64 >= 14 else 1)
+        assert (info.split_k, int(info.tail_tiles) > 0) == ((1, False) if K // 64 >= 48 else (0, True))
         for sched in SCHEDS:
             _run_checked(h, x, sched, full=False)
     finally:
