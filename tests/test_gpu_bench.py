@@ -55,6 +55,11 @@ def test_roofline_block(line):
     assert r["achieved"] == pytest.approx(line["value"], rel=1e-3)
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-3)
     assert r["traffic"] is None or r["traffic"] > 0
+    # a short run (3 steps) is compared with the burst peak
+    peaks = line["peaks"]
+    assert r["peak"] == peaks["tensor_tflops"] and "burst" in r["peak_source"]
+    assert r["frac_burst"] == pytest.approx(r["frac"], rel=1e-3)
+    assert r["frac_sustained"] == pytest.approx(r["achieved"] / peaks["tensor_tflops_sustained"], rel=1e-3)
 
 
 def test_end_to_end_leg_counts_its_bytes(line):
