@@ -615,7 +615,7 @@ def test_many_tiles_along_one_dimension(handle, shape, sched):
 
 FULL = ([("fp16_4096_ksweep", k) for k in (128, 2048, 4096)]
         + [("bf16_8192_ksweep", k) for k in (256, 8192)]
-        + [("e4m3_8192", None)]
+        + [("e4m3_8192", None), ("e4m3_8192_k", 2048)]
         + [("bf16_tail", i) for i in range(3)])
 
 
@@ -626,6 +626,8 @@ def _full_problem(name, arg):
         return wl.bf16_8192_ksweep([arg])[0]
     if name == "e4m3_8192":
         return wl.e4m3_8192()[0]
+    if name == "e4m3_8192_k":   # e4m3 at a K whose last wave runs as column halves
+        return wl.Problem(f"e4m3_8192_k{arg}", 8192, 8192, arg, wl.E4M3, "normal", 4000 + arg)
     return wl.bf16_tail()[arg]
 
 
