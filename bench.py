@@ -614,6 +614,15 @@ def end_to_end(pts, h, xs, problems, args, dist, world, flops_step, stream):
             "steps": e2e_steps, "link_gbs": round((bi + bo) / e2e_s / 1e9, 1)}
 
 
+def roofline_peak(timed_s, burst, sustained):
+    """The tensor peak a run of `timed_s` seconds of timed work is compared
+    with: the sustained one from LONG_RUN_S on (when it is known), else the
+    burst one.  Returns (peak, whether it is the sustained one)."""
+    if sustained and timed_s >= LONG_RUN_S:
+        return sustained, True
+    return burst, False
+
+
 def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops_step):
     peaks, peaks_src = load_peaks()
     tensor_peak = peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
@@ -630,8 +639,7 @@ def finish(args, per_sched, problems, world, clocks, e2e, extra, rank, xs, flops
     # (on GB300: 200 steps, 0.33 s, ran at a median 2002 MHz with sw_power_cap;
     # 20 steps, 30 ms, at 2070 MHz with no throttle reason).
     timed_s = head["ms_per_step"] * args.steps / 1e3
-    sustained = timed_s >= LONG_RUN_S and bool(tensor_peak_sus)
-    peak = tensor_peak_sus if sustained else tensor_peak
+    peak, sustained = roofline_peak(timed_s, tensor_peak, tensor_peak_sus)
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
                 "frac": round(achieved / peak, 4) if peak else None,
                 "traffic": traffic if isinstance(traffic, (int, float)) else None,
