@@ -231,10 +231,11 @@ def test_every_ring_depth(cg, stages):
 
 
 @pytest.mark.parametrize("cg", [1, 2])
-@pytest.mark.parametrize("split,split_k,G", [(1, -1, 0), (2, 0, 0), (1, 1, 5)])
+@pytest.mark.parametrize("split,split_k,G", [(1, -1, 0), (2, 0, 0), (1, 1, 5), (0, 0, 5)])
 def test_direct_store_epilogue(cg, split, split_k, G):
     """The epilogue that stores C rows straight from registers (no TMA store):
-    whole tiles, column slices, stream-K pieces."""
+    whole tiles, column slices, stream-K pieces, and the library's own plan on
+    5 clusters (tail halves where the last wave leaves at most 2 tiles)."""
     h = pts.gemm_create(0, pts.make_opts(cta_group=cg, epilogue=2, split=split, split_k=split_k, max_clusters=G,
                                          debug_flags=pts.GEMM_DEBUG_RECORDS))
     try:
