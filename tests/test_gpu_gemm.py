@@ -683,15 +683,15 @@ def test_clc_claiming_two_units_ahead(shape, stop_at):
     """clc_depth 2: a cluster claims its next unit one unit earlier than with
     depth 1 (still one request at a time).  Coverage stays exact, with and
     without a request that behaves as failed, on ragged and multi-wave
-    problems, stream-K units included."""
+    problems, stream-K units and tail halves included."""
     flags = pts.GEMM_DEBUG_RECORDS | (pts.GEMM_DEBUG_CLC_STOP_AT if stop_at is not None else 0)
     h = pts.gemm_create(0, pts.make_opts(clc_depth=2, debug_flags=flags, fault_arg=stop_at or 0, **SHAPES[shape]))
     try:
         for (M, N, K, dt) in [(300, 520, 208, wl.BF16), (2048, 2048, 256, wl.F16), (1000, 1800, 2000, wl.BF16),
-                              (640, 1000, 512, wl.E4M3)]:
+                              (640, 1000, 512, wl.E4M3), (4096, 4096, 256, wl.F16)]:
             dist = "normal" if dt == wl.E4M3 else "uniform"
             x = wl.make_inputs(wl.Problem("clc2", M, N, K, dt, dist, M + N + K + 5))
-            _run_checked(h, x, pts.GEMM_SCHED_CLC)
+            _run_checked(h, x, pts.GEMM_SCHED_CLC, full=M < 4096)
     finally:
         pts.gemm_destroy(h)
 
