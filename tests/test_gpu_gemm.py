@@ -673,6 +673,9 @@ def test_clc_injected_request_failure_keeps_coverage(stop_at):
     try:
         x = wl.custom(2048, 2048, 256, wl.BF16, "uniform", 11)
         _run_checked(h, x, pts.GEMM_SCHED_CLC)
+        x = wl.custom(4096, 4096, 256, wl.BF16, "uniform", 12)   # several waves, the last in column halves
+        assert pts.gemm_query(h, 4096, 4096, 256, wl.BF16, pts.GEMM_SCHED_CLC).tail_tiles > 0
+        _run_checked(h, x, pts.GEMM_SCHED_CLC, full=False)
     finally:
         pts.gemm_destroy(h)
 
